@@ -1,0 +1,63 @@
+"""The oracle's pins are strong enough to catch plausible mistakes.
+
+Each case copies the oracle's C source, plants one mistake (a dropped term,
+a wrong sign, a wrong index, a swapped operand), compiles the copy on the
+CPU and checks that the torch float64 autograd pin rejects it.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import oracle as orc
+from test_oracle_pins import rel_err, torch_reference
+
+SRC = os.path.join(os.path.dirname(orc.__file__), "fa_oracle.c")
+
+MUTATIONS = {
+    "gqa_index_in_dq": ("const double* k = J->Kh + ((int64_t)j * Hkv + (h / G)) * D;",
+                        "const double* k = J->Kh + ((int64_t)j * Hkv + (h % Hkv)) * D;"),
+    "mask_term_dropped": ("s[j] += mv;", "s[j] += 0.0 * mv;"),
+    "ds_sign": ("const double ds = p * (dp[j] - delta);", "const double ds = p * (dp[j] + delta);"),
+    "causal_off_by_one": ("if (J->causal && (int64_t)j > (int64_t)J->M - J->N + i) return 0;",
+                          "if (J->causal && (int64_t)j >= (int64_t)J->M - J->N + i) return 0;"),
+    "dk_scale_dropped": ("dk[c] += J->scale * ds * q[c];", "dk[c] += ds * q[c];"),
+    "dv_uses_ds": ("dv[c] += p * d[c];", "dv[c] += ds * d[c];"),
+    "q4_nibbles_swapped": ("int lo = blk[2 + t] & 15, hi = blk[2 + t] >> 4;",
+                           "int hi = blk[2 + t] & 15, lo = blk[2 + t] >> 4;"),
+    "lse_max_dropped": ("const double lse = mx + log(sum);", "const double lse = log(sum);"),
+    "dp_uses_k_in_phase2": ("for (int t = 0; t < RB; ++t) acc2[t] += oc * vc[t];",
+                            "for (int t = 0; t < RB; ++t) acc2[t] += oc * (kt + (vc - vt))[t];"),
+    "q8_scale_ignored": ("out[32 * b + t] = (double)(int8_t)blk[2 + t] * d;",
+                         "out[32 * b + t] = (double)(int8_t)blk[2 + t] * 0.01;"),
+}
+
+
+@pytest.fixture(scope="module")
+def problem():
+    return synth.make_problem("mut", N=9, M=33, H=4, Hkv=2, D=64, Dv=64, k_type="q4_0", v_type="q8_0",
+                              mask="finite", mask_p=0.2, mask_heads=4, causal=True, seed=77)
+
+
+def test_unmutated_copy_passes(problem, tmp_path):
+    lib = orc.load(orc.compile_source(SRC, str(tmp_path / "lib_ok.so")))
+    got = orc.fa_back(problem, lib=lib)
+    ref = torch_reference(problem)
+    assert max(rel_err(got[k], ref[k]) for k in ("lse", "delta", "dQ", "dK", "dV")) < 1e-12
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(problem, tmp_path, name):
+    old, new = MUTATIONS[name]
+    text = open(SRC).read()
+    assert text.count(old) == 1, name
+    src = tmp_path / f"mut_{name}.c"
+    src.write_text(text.replace(old, new))
+    lib = orc.load(orc.compile_source(str(src), str(tmp_path / f"lib_{name}.so")))
+    got = orc.fa_back(problem, lib=lib)
+    ref = torch_reference(problem)
+    errs = {k: rel_err(np.nan_to_num(got[k], nan=1e30, posinf=1e30, neginf=-1e30),
+                       np.nan_to_num(ref[k], nan=1e30, posinf=1e30, neginf=-1e30))
+            for k in ("lse", "delta", "dQ", "dK", "dV")}
+    assert max(errs.values()) > 1e-6, (name, errs)
