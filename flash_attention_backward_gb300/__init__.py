@@ -1,0 +1,13 @@
+"""GB300 (sm_103a) flash-attention backward over a raw F32/F16/q8_0/q4_0 K/V cache.
+
+The computation lives in libfa_back.so (hand-written CUDA, C ABI in include/fa_back.h).
+This package only marshals arguments: ``_native`` mirrors the C entry points under the same
+names, and ``backward`` allocates outputs and workspace with PyTorch and calls ``fa_back``
+on the current stream.
+"""
+from ._native import (  # noqa: F401
+    FA_F16, FA_F32, FA_Q4_0, FA_Q8_0, STATUS, NativeLibraryMissing, LIB_PATH,
+    fa_back, fa_back_get_error, fa_back_profile, fa_back_profile_read, fa_back_status_string,
+    fa_back_workspace_size, fa_row_bytes, lib,
+)
+from .api import FaBackError, Workspace, backward  # noqa: F401

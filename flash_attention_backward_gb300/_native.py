@@ -1,0 +1,85 @@
+"""ctypes binding of libfa_back.so: the C ABI under the same names, argument marshalling only."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa_back.so")
+
+FA_F32, FA_F16, FA_Q8_0, FA_Q4_0 = 0, 1, 2, 3
+STATUS = {0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_TYPE", 3: "FA_ERR_SHAPE", 4: "FA_ERR_ALIGN",
+          5: "FA_ERR_UNSUPPORTED", 6: "FA_ERR_DEVICE", 7: "FA_ERR_CUDA", 8: "FA_ERR_TIMEOUT",
+          9: "FA_ERR_WORKSPACE"}
+
+_lib = None
+
+
+class NativeLibraryMissing(RuntimeError):
+    """libfa_back.so is not built or cannot be loaded; there is no fallback path."""
+
+
+def lib():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise NativeLibraryMissing(
+            f"{LIB_PATH} is missing: build it with `python -m flash_attention_backward_gb300.build`")
+    try:
+        L = ctypes.CDLL(LIB_PATH)
+    except OSError as e:  # pragma: no cover - depends on the machine
+        raise NativeLibraryMissing(f"cannot load {LIB_PATH}: {e}") from e
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.fa_row_bytes.restype = ctypes.c_long
+    L.fa_row_bytes.argtypes = [i, i]
+    L.fa_back_workspace_size.restype = sz
+    L.fa_back_workspace_size.argtypes = [i] * 6
+    L.fa_back.restype = i
+    L.fa_back.argtypes = [vp, vp, i, vp, i, vp, i, vp, f, i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.fa_back_get_error.restype = i
+    L.fa_back_get_error.argtypes = []
+    L.fa_back_status_string.restype = ctypes.c_char_p
+    L.fa_back_status_string.argtypes = [i]
+    L.fa_back_profile.restype = i
+    L.fa_back_profile.argtypes = [i]
+    L.fa_back_profile_read.restype = i
+    L.fa_back_profile_read.argtypes = [vp, vp, vp, i]
+    _lib = L
+    return L
+
+
+def fa_row_bytes(type_: int, D: int) -> int:
+    return int(lib().fa_row_bytes(type_, D))
+
+
+def fa_back_workspace_size(N: int, M: int, H: int, Hkv: int, D: int, Dv: int) -> int:
+    return int(lib().fa_back_workspace_size(N, M, H, Hkv, D, Dv))
+
+
+def fa_back(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal,
+            dQ, dK, dV, lse, delta, workspace, workspace_bytes, stream) -> int:
+    """Direct call of the C entry point; pointers are integers (device addresses) or None."""
+    return int(lib().fa_back(q, k, k_type, v, v_type, mask, mask_heads, dO, float(scale), N, M, H, Hkv, D, Dv,
+                             int(causal), dQ, dK, dV, lse, delta, workspace, workspace_bytes, stream))
+
+
+def fa_back_get_error() -> int:
+    return int(lib().fa_back_get_error())
+
+
+def fa_back_status_string(status: int) -> str:
+    return lib().fa_back_status_string(status).decode()
+
+
+def fa_back_profile(enable: bool) -> int:
+    return int(lib().fa_back_profile(1 if enable else 0))
+
+
+def fa_back_profile_read(max_kernels: int = 16) -> dict:
+    """{kernel name: (summed ms, launches)} of the recorded fa_back calls; clears the record."""
+    ms = (ctypes.c_float * max_kernels)()
+    cnt = (ctypes.c_int * max_kernels)()
+    names = (ctypes.c_char_p * max_kernels)()
+    n = int(lib().fa_back_profile_read(ms, cnt, names, max_kernels))
+    return {names[k].decode(): (float(ms[k]), int(cnt[k])) for k in range(n) if cnt[k] > 0}

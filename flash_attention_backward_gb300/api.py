@@ -1,0 +1,66 @@
+"""PyTorch-facing wrapper: allocation with torch, one call of fa_back on the current stream."""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _native as nat
+
+
+class FaBackError(RuntimeError):
+    pass
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise FaBackError(f"fa_back failed: {nat.STATUS.get(rc, rc)} ({nat.fa_back_status_string(rc)})")
+
+
+class Workspace:
+    """Reusable device workspace (grown on demand, owned by PyTorch's allocator)."""
+
+    def __init__(self, device="cuda"):
+        self.device = torch.device(device)
+        self.buf: Optional[torch.Tensor] = None
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def backward(q: torch.Tensor, k: torch.Tensor, k_type: int, v: torch.Tensor, v_type: int, dO: torch.Tensor,
+             *, H: int, Hkv: int, D: int, Dv: int, M: int, scale: float, causal: bool = False,
+             mask: Optional[torch.Tensor] = None, mask_heads: int = 0, out: Optional[dict] = None,
+             workspace: Optional[Workspace] = None, stream: Optional[torch.cuda.Stream] = None) -> dict:
+    """Run the backward on device tensors.
+
+    q [N][H][D] f32, dO [N][H][Dv] f32, k/v uint8 raw cache rows [M][Hkv][row], mask int16/uint16
+    binary16 bits [Hm][N][M] or None.  Returns {"dQ", "dK", "dV", "lse", "delta"} (f32 tensors).
+    """
+    N = q.shape[0]
+    dev = q.device
+    if out is None:
+        out = {
+            "dQ": torch.empty((N, H, D), dtype=torch.float32, device=dev),
+            "dK": torch.empty((M, Hkv, D), dtype=torch.float32, device=dev),
+            "dV": torch.empty((M, Hkv, Dv), dtype=torch.float32, device=dev),
+            "lse": torch.empty((N, H), dtype=torch.float32, device=dev),
+            "delta": torch.empty((N, H), dtype=torch.float32, device=dev),
+        }
+    for t in (q, k, v, dO, mask, *out.values()):
+        if t is not None and not t.is_contiguous():
+            raise FaBackError("tensors must be contiguous")
+    ws_bytes = nat.fa_back_workspace_size(N, M, H, Hkv, D, Dv)
+    ws = (workspace or Workspace(dev)).get(ws_bytes)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    rc = nat.fa_back(_ptr(q), _ptr(k), k_type, _ptr(v), v_type, _ptr(mask), mask_heads, _ptr(dO), scale,
+                     N, M, H, Hkv, D, Dv, causal, _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]),
+                     _ptr(out["lse"]), _ptr(out["delta"]), ws.data_ptr(), ws.numel(), s.cuda_stream)
+    _check(rc)
+    return out

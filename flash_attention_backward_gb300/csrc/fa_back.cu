@@ -1,0 +1,383 @@
+// Host side of the flash-attention backward: argument checks, workspace layout, TMA tensor
+// maps and the launch sequence behind the C ABI declared in include/fa_back.h.
+//
+// Numerics (the reading of "CUDA: FLASH_ATTN_BACK kernels", CambrianTech/llama.cpp pull
+// request 63, for a binary16 tensor-core path):
+//  * every contraction runs as binary16 x binary16 -> f32 on tcgen05 (kind::f16);
+//  * Q, dO, K^, V^ are multiplied by powers of two (max magnitude below 2^14) before rounding,
+//    P by 2^15 and dS by a power of two derived from a norm bound, so no operand leaves the
+//    binary16 normal range and the scales divide out exactly;
+//  * V^ is shifted by its column mean r per KV head: dP'_ij = dO_i . (v^_j - r).  Since the
+//    softmax weights of a row sum to one, dP'_ij - delta'_i = dP_ij - delta_i, and the reported
+//    delta adds dO_i . r back.  The rounded operand then carries V's variation at binary16's
+//    relative precision, which the near-constant-V case needs;
+//  * dS = p * (dP' - delta') is formed by direct f32 subtraction (review of revision a0ea747);
+//  * the softmax statistics (running max, sum, sum of p*dP) use f32 with compensated chunk
+//    accumulation; split partials merge in a fixed order, so results are deterministic.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <limits>
+#include <mutex>
+
+#include "../../include/fa_back.h"
+#include "fa_kernels.cuh"
+
+namespace fab {
+
+__device__ int g_err = 0;
+
+struct Plan {
+  int G, R, nQT, BK, nKT, nsplit, kt_per_split, nsplit_dq;
+  int nblk_stats, nbv;
+  size_t off_stats, off_rmean, off_dOr, off_lse2, off_dlt, off_part, off_dqpart, off_q16, off_do16, off_bstat,
+      off_vsum, total;
+};
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static int block_keys(int D, int Dv) { return (D + Dv <= 256) ? 128 : 64; }
+
+static Plan make_plan(int N, int M, int H, int Hkv, int D, int Dv, int nsm) {
+  Plan P;
+  std::memset(&P, 0, sizeof(P));
+  P.G = H / Hkv;
+  P.R = N * P.G;
+  P.nQT = (P.R + 127) / 128;
+  P.BK = block_keys(D, Dv);
+  P.nKT = (M + P.BK - 1) / P.BK;
+  // split the keys of each row tile so the row passes fill the GPU about twice
+  const int base = std::max(1, P.nQT * Hkv);
+  int ns = (2 * nsm + base - 1) / base;
+  ns = std::max(1, std::min(ns, std::max(1, P.nKT)));
+  P.kt_per_split = P.nKT > 0 ? (P.nKT + ns - 1) / ns : 1;
+  P.nsplit = P.nKT > 0 ? (P.nKT + P.kt_per_split - 1) / P.kt_per_split : 1;
+  P.nsplit_dq = P.nsplit;
+  const long rows = 2L * N * H + 2L * M * Hkv;
+  P.nblk_stats = (int)std::max(1L, std::min(4L * nsm, (rows + 7) / 8));
+  P.nbv = std::max(1, std::min(256, (M + 255) / 256));
+  size_t o = 0;
+  P.off_stats = o; o = align256(o + sizeof(Stats));
+  P.off_rmean = o; o = align256(o + sizeof(float) * (size_t)Hkv * Dv);
+  P.off_dOr = o; o = align256(o + sizeof(float) * (size_t)Hkv * P.R);
+  P.off_lse2 = o; o = align256(o + sizeof(float) * (size_t)Hkv * P.R);
+  P.off_dlt = o; o = align256(o + sizeof(float) * (size_t)Hkv * P.R);
+  P.off_part = o; o = align256(o + sizeof(float) * 3 * (size_t)P.nsplit * Hkv * P.R);
+  P.off_dqpart = o; o = align256(o + (P.nsplit_dq > 1 ? sizeof(float) * (size_t)P.nsplit_dq * Hkv * P.R * D : 0));
+  P.off_q16 = o; o = align256(o + 2 * (size_t)Hkv * P.R * D);
+  P.off_do16 = o; o = align256(o + 2 * (size_t)Hkv * P.R * Dv);
+  P.off_bstat = o; o = align256(o + sizeof(float) * 8 * (size_t)P.nblk_stats);
+  P.off_vsum = o; o = align256(o + sizeof(float) * (size_t)P.nbv * Hkv * Dv);
+  P.total = o;
+  return P;
+}
+
+static int device_sms(int* major, int* minor) {
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (major) cudaDeviceGetAttribute(major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (minor) cudaDeviceGetAttribute(minor, cudaDevAttrComputeCapabilityMinor, dev);
+  return nsm;
+}
+
+// ------------------------------------------------------------------------------------------------
+// tensor maps
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// binary16 tensor [d2][d1][d0] (d0 fastest); boxes of 64 x 128 x 1 with the 128-byte swizzle.
+static bool make_map(CUtensorMap* m, void* base, int d0, int d1, int d2) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
+  cuuint64_t strides[2] = {(cuuint64_t)d0 * 2, (cuuint64_t)d0 * d1 * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------------------------------------
+// measurement hook: one CUDA event before the sequence and one after each launch
+
+constexpr int kProfCalls = 256, kProfSlots = 16;
+static const char* const kKernelNames[kProfSlots] = {
+    "k_row_stats", "k_vsum", "k_finalize", "k_convert", "k_rows_lse", "k_lse_merge", "k_rows_dq", "k_dq_reduce",
+    "k_cols", "", "", "", "", "", "", ""};
+enum { KS_STATS = 0, KS_VSUM, KS_FINAL, KS_CONVERT, KS_ROWS_LSE, KS_MERGE, KS_ROWS_DQ, KS_DQ_REDUCE, KS_COLS, KS_N };
+
+struct Profiler {
+  std::mutex mu;
+  bool on = false;
+  int ncalls = 0;
+  cudaEvent_t ev[kProfCalls][kProfSlots + 1];
+  bool used[kProfCalls][kProfSlots];
+  bool created = false;
+};
+static Profiler g_prof;
+
+// Per-call recorder: mark(slot) after launching kernel `slot`.
+struct CallRec {
+  int call = -1;
+  cudaStream_t s = nullptr;
+  void begin(cudaStream_t st) {
+    s = st;
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    if (!g_prof.on || g_prof.ncalls >= kProfCalls) return;
+    if (!g_prof.created) {
+      for (int c = 0; c < kProfCalls; ++c)
+        for (int k = 0; k <= kProfSlots; ++k) cudaEventCreate(&g_prof.ev[c][k]);
+      g_prof.created = true;
+    }
+    call = g_prof.ncalls++;
+    for (int k = 0; k < kProfSlots; ++k) g_prof.used[call][k] = false;
+    cudaEventRecord(g_prof.ev[call][kProfSlots], s);  // start marker
+  }
+  // kernel `slot` was just launched: its duration is measured from the previous marker
+  void mark(int slot) {
+    if (call < 0) return;
+    cudaEventRecord(g_prof.ev[call][slot], s);
+    g_prof.used[call][slot] = true;
+  }
+};
+
+// ------------------------------------------------------------------------------------------------
+// launch sequence for one (D, Dv)
+
+template <typename K>
+static cudaError_t set_smem(K kernel, int bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int D, int Dv>
+static cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& tmQ, const CUtensorMap& tmO,
+                             cudaStream_t s, CallRec& rec) {
+  constexpr int BK = (D + Dv <= 256) ? 128 : 64;
+  using RL = RowsCfg<D, Dv, BK, 0>;
+  using RQ = RowsCfg<D, Dv, BK, 1>;
+  using CC = ColsCfg<D, Dv, BK>;
+  static_assert(RQ::SMEM <= 232448 && CC::SMEM <= 232448, "shared memory budget");
+  static_assert(RQ::TCOLS <= 512 && CC::TCOLS <= 512, "tensor memory budget");
+  cudaError_t e;
+  if ((e = set_smem(k_rows<D, Dv, BK, 0>, RL::SMEM)) != cudaSuccess) return e;
+  if ((e = set_smem(k_rows<D, Dv, BK, 1>, RQ::SMEM)) != cudaSuccess) return e;
+  if ((e = set_smem(k_cols<D, Dv, BK>, CC::SMEM)) != cudaSuccess) return e;
+
+  dim3 grows(P.nQT, p.Hkv, P.nsplit);
+  k_rows<D, Dv, BK, 0><<<grows, 128, RL::SMEM, s>>>(tmQ, tmO, p);
+  rec.mark(KS_ROWS_LSE);
+  k_lse_merge<<<(unsigned)(((long)p.Hkv * P.R + 255) / 256), 256, 0, s>>>(p);
+  rec.mark(KS_MERGE);
+  k_rows<D, Dv, BK, 1><<<grows, 128, RQ::SMEM, s>>>(tmQ, tmO, p);
+  rec.mark(KS_ROWS_DQ);
+  if (P.nsplit_dq > 1) {
+    k_dq_reduce<<<(unsigned)(((long)p.Hkv * P.R * (D / 4) + 255) / 256), 256, 0, s>>>(p);
+    rec.mark(KS_DQ_REDUCE);
+  }
+  if (P.nKT > 0) {
+    k_cols<D, Dv, BK><<<dim3(P.nKT, p.Hkv), 128, CC::SMEM, s>>>(tmQ, tmO, p);
+    rec.mark(KS_COLS);
+  }
+  return cudaGetLastError();
+}
+
+using RunFn = cudaError_t (*)(const Params&, const Plan&, const CUtensorMap&, const CUtensorMap&, cudaStream_t,
+                              CallRec&);
+
+static RunFn pick(int D, int Dv) {
+#define FAB_CASE(a, b) \
+  if (D == a && Dv == b) return run_shape<a, b>;
+  FAB_CASE(64, 64)
+  FAB_CASE(64, 128)
+  FAB_CASE(64, 256)
+  FAB_CASE(128, 64)
+  FAB_CASE(128, 128)
+  FAB_CASE(128, 256)
+  FAB_CASE(256, 64)
+  FAB_CASE(256, 128)
+  FAB_CASE(256, 256)
+#undef FAB_CASE
+  return nullptr;
+}
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace fab
+
+using namespace fab;
+
+extern "C" long fa_row_bytes(int type, int D) {
+  if (D <= 0) return -1;
+  switch (type) {
+    case FA_F32: return 4L * D;
+    case FA_F16: return 2L * D;
+    case FA_Q8_0: return (D % 32) ? -1 : (D / 32) * 34L;
+    case FA_Q4_0: return (D % 32) ? -1 : (D / 32) * 18L;
+  }
+  return -1;
+}
+
+extern "C" size_t fa_back_workspace_size(int N, int M, int H, int Hkv, int D, int Dv) {
+  if (N < 0 || M < 0 || H <= 0 || Hkv <= 0 || H % Hkv) return 0;
+  int nsm = device_sms(nullptr, nullptr);
+  if (nsm <= 0) nsm = 152;
+  return make_plan(N, M, H, Hkv, D, Dv, nsm).total;
+}
+
+extern "C" fa_status fa_back(const float* q, const void* k, int k_type, const void* v, int v_type,
+                             const uint16_t* mask, int mask_heads, const float* dO, float scale, int N, int M,
+                             int H, int Hkv, int D, int Dv, int causal, float* dQ, float* dK, float* dV,
+                             float* lse, float* delta, void* workspace, size_t workspace_bytes, void* stream) {
+  // ---- argument checks (nothing is enqueued on failure)
+  if (k_type < FA_F32 || k_type > FA_Q4_0 || v_type < FA_F32 || v_type > FA_Q4_0) return FA_ERR_TYPE;
+  if (N < 0 || M < 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || Hkv > 256) return FA_ERR_SHAPE;
+  if (mask && mask_heads != 1 && mask_heads != H) return FA_ERR_SHAPE;
+  if (!pick(D, Dv)) return FA_ERR_UNSUPPORTED;
+  if ((long)N * (H / Hkv) > (1L << 30) || M > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  const long rbk = fa_row_bytes(k_type, D), rbv = fa_row_bytes(v_type, Dv);
+  if (rbk <= 0 || rbv <= 0) return FA_ERR_SHAPE;
+  const bool needQ = N > 0, needK = M > 0;
+  if ((needQ && (!q || !dO || !dQ || !lse || !delta)) || (needK && (!k || !v || !dK || !dV))) return FA_ERR_NULL;
+  const void* ptrs16[] = {q, dO, dQ, dK, dV, lse, delta, k, v, mask};
+  for (const void* pp : ptrs16)
+    if (pp && !aligned(pp, 16)) return FA_ERR_ALIGN;
+  int major = 0, minor = 0;
+  const int nsm = device_sms(&major, &minor);
+  if (nsm <= 0) return FA_ERR_CUDA;
+  if (major != 10 || minor != 3) return FA_ERR_DEVICE;
+  const Plan P = make_plan(N, M, H, Hkv, D, Dv, nsm);
+  if (!workspace || workspace_bytes < P.total) return FA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return FA_ERR_ALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  // ---- degenerate shapes: every output element is still written
+  if (N == 0 || M == 0) {
+    const long nq = (long)N * H, nkd = (long)M * Hkv * D, nkv = (long)M * Hkv * Dv;
+    auto fill = [&](float* x, long n, float val) {
+      if (n > 0) k_fill<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(x, n, val);
+    };
+    fill(dK, nkd, 0.f);
+    fill(dV, nkv, 0.f);
+    fill(lse, nq, -std::numeric_limits<float>::infinity());
+    fill(delta, nq, 0.f);
+    fill(dQ, nq * D, 0.f);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
+
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  int* errp = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&errp), g_err) != cudaSuccess) return FA_ERR_CUDA;
+
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = q, p.dO = dO;
+  p.k = reinterpret_cast<const uint8_t*>(k), p.v = reinterpret_cast<const uint8_t*>(v);
+  p.k_type = k_type, p.v_type = v_type, p.rbk = (int)rbk, p.rbv = (int)rbv;
+  p.mask = mask, p.Hm = mask ? mask_heads : 1;
+  p.scale = scale;
+  p.N = N, p.M = M, p.H = H, p.Hkv = Hkv, p.G = P.G, p.D = D, p.Dv = Dv, p.R = P.R, p.causal = causal ? 1 : 0;
+  p.nQT = P.nQT, p.nKT = P.nKT, p.nsplit = P.nsplit, p.kt_per_split = P.kt_per_split;
+  p.dQ = dQ, p.dK = dK, p.dV = dV, p.lse = lse, p.delta = delta;
+  p.st = reinterpret_cast<Stats*>(ws + P.off_stats);
+  p.rmean = reinterpret_cast<float*>(ws + P.off_rmean);
+  p.dOr = reinterpret_cast<float*>(ws + P.off_dOr);
+  p.lse2 = reinterpret_cast<float*>(ws + P.off_lse2);
+  p.dlt = reinterpret_cast<float*>(ws + P.off_dlt);
+  p.part = reinterpret_cast<float*>(ws + P.off_part);
+  p.dqpart = reinterpret_cast<float*>(ws + P.off_dqpart);
+  p.q16 = reinterpret_cast<__half*>(ws + P.off_q16);
+  p.do16 = reinterpret_cast<__half*>(ws + P.off_do16);
+  p.bstat = reinterpret_cast<float*>(ws + P.off_bstat);
+  p.nblk_stats = P.nblk_stats;
+  p.vsum = reinterpret_cast<float*>(ws + P.off_vsum);
+  p.nbv = P.nbv;
+  p.err = errp;
+
+  CUtensorMap tmQ, tmO;
+  if (!make_map(&tmQ, p.q16, D, P.R, Hkv) || !make_map(&tmO, p.do16, Dv, P.R, Hkv)) return FA_ERR_CUDA;
+
+  CallRec rec;
+  rec.begin(s);
+  k_row_stats<<<P.nblk_stats, 256, 0, s>>>(p);
+  rec.mark(KS_STATS);
+  k_vsum<<<dim3((Hkv * Dv + 255) / 256, P.nbv), 256, 0, s>>>(p);
+  rec.mark(KS_VSUM);
+  k_finalize<<<1, 256, 0, s>>>(p);
+  rec.mark(KS_FINAL);
+  k_convert<<<(unsigned)std::min<long>(((long)N * H + 7) / 8, 8L * nsm), 256, 0, s>>>(p);
+  rec.mark(KS_CONVERT);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  return pick(D, Dv)(p, P, tmQ, tmO, s, rec) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+extern "C" fa_status fa_back_get_error(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
+  int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_err, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  return v ? (fa_status)v : FA_OK;
+}
+
+extern "C" const char* fa_back_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_NULL: return "a required pointer is NULL";
+    case FA_ERR_TYPE: return "unknown K or V cache type";
+    case FA_ERR_SHAPE: return "invalid shape (H % Hkv, mask heads, or a format's block size)";
+    case FA_ERR_ALIGN: return "misaligned pointer";
+    case FA_ERR_UNSUPPORTED: return "unsupported head size or problem size";
+    case FA_ERR_DEVICE: return "the current device is not sm_103";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "a kernel gave up on a bounded wait";
+    case FA_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+extern "C" fa_status fa_back_profile(int enable) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  g_prof.on = enable != 0;
+  return FA_OK;
+}
+
+extern "C" int fa_back_profile_read(float* ms_sum, int* launches, const char** names, int max_kernels) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  const int n = std::min(max_kernels, (int)KS_N);
+  for (int k = 0; k < n; ++k) {
+    if (ms_sum) ms_sum[k] = 0.f;
+    if (launches) launches[k] = 0;
+    if (names) names[k] = kKernelNames[k];
+  }
+  for (int c = 0; c < g_prof.ncalls; ++c) {
+    int prev = kProfSlots;  // start marker
+    for (int k = 0; k < KS_N; ++k) {
+      if (!g_prof.used[c][k]) continue;
+      float ms = 0.f;
+      if (cudaEventSynchronize(g_prof.ev[c][k]) == cudaSuccess &&
+          cudaEventElapsedTime(&ms, g_prof.ev[c][prev], g_prof.ev[c][k]) == cudaSuccess && k < n) {
+        if (ms_sum) ms_sum[k] += ms;
+        if (launches) launches[k] += 1;
+      }
+      prev = k;
+    }
+  }
+  g_prof.ncalls = 0;
+  return n;
+}

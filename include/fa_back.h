@@ -1,0 +1,121 @@
+/*
+ * fa_back.h -- C ABI of the GB300 (sm_103a) flash-attention backward over a raw K/V cache.
+ *
+ * The operation is ggml's FLASH_ATTN_BACK as described in "CUDA: FLASH_ATTN_BACK kernels"
+ * (CambrianTech/llama.cpp pull request 63; review of the first revision, "The math in
+ * fattn_back_q / fattn_back_kv"):
+ *
+ *   hk       = h / (H / Hkv)                                  GQA map
+ *   allowed  = (mask == NULL or mask[h % Hm][i][j] != -inf) and (!causal or j <= M - N + i)
+ *   s_ij     = scale * q_i . k^_j + mask[h % Hm][i][j]
+ *   lse_ih   = log sum_{allowed j} exp(s_ij)                  (-inf when no key is allowed)
+ *   p_ij     = exp(s_ij - lse_ih)                             (0 when not allowed)
+ *   delta_ih = sum_j p_ij (dO_i . v^_j)                       (= rowsum(dO o O), O never formed)
+ *   dS_ij    = p_ij (dO_i . v^_j - delta_ih)
+ *   dQ_i     = scale sum_j dS_ij k^_j
+ *   dK_j     = scale sum_{h in group(hk), i} dS_ij q_i
+ *   dV_j     = sum_{h in group(hk), i} p_ij dO_i
+ *
+ * k^ and v^ are decoded from the cache rows exactly as their block formats define (see
+ * fa_type).  The N x M score matrix is never materialised.  Fully masked rows give
+ * lse = -inf, delta = 0 and a zero dQ row (same review, "Masking and q8_0").
+ *
+ * Layouts (all row-major, the last index fastest; element sizes in parentheses):
+ *   q      [N][H][D]        f32     dO    [N][H][Dv]      f32
+ *   k      [M][Hkv][row_k]  raw     v     [M][Hkv][row_v] raw     (row = fa_row_bytes(type, D))
+ *   mask   [Hm][N][M]       IEEE binary16 bits; element (key j, query i, head hm) at
+ *                           (hm*N + i)*M + j  (ggml's [M, N, Hm] order); Hm = 1 or H
+ *   dQ     [N][H][D]        f32     dK    [M][Hkv][D]     f32     dV [M][Hkv][Dv] f32
+ *   lse    [N][H]           f32 (natural log)             delta [N][H] f32
+ *
+ * Ownership: every pointer is caller-owned DEVICE memory on the current device, including the
+ * workspace.  The library allocates no device memory and keeps no reference after return.
+ *
+ * Asynchrony: fa_back() validates its arguments on the host, enqueues its kernels on `stream`
+ * and returns without synchronising.  Outputs are valid once the stream's work completes.
+ *
+ * Errors: argument errors are reported before anything is enqueued and leave the outputs
+ * untouched.  A launch failure returns FA_ERR_CUDA.  A kernel that gives up on a bounded wait
+ * records FA_ERR_TIMEOUT in a device word that fa_back_get_error() reads after the caller has
+ * synchronised.
+ *
+ * Determinism: every output element has exactly one writer and every sum runs in a fixed
+ * order, so repeated calls with the same inputs give bit-identical outputs.
+ */
+#ifndef FA_BACK_H
+#define FA_BACK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Cache row formats.
+ *   FA_F32  : D IEEE binary32 values.
+ *   FA_F16  : D IEEE binary16 values.
+ *   FA_Q8_0 : D/32 blocks of 34 bytes: binary16 scale d, then 32 int8 codes; value = code * d.
+ *   FA_Q4_0 : D/32 blocks of 18 bytes: binary16 scale d, then 16 bytes; byte b holds element b
+ *             in its low nibble and element b+16 in its high nibble; value = (nibble - 8) * d.
+ * The q8_0 block follows the review's description of the kernel's q8_0 load (pull request 63);
+ * the q4_0 block is the raw-cache format the forward kernel of torad-labs/llama.cpp pull
+ * request 71 reads.  Rows of the cache are contiguous blocks. */
+typedef enum { FA_F32 = 0, FA_F16 = 1, FA_Q8_0 = 2, FA_Q4_0 = 3 } fa_type;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_NULL = 1,        /* a required pointer is NULL (mask may be NULL)                     */
+  FA_ERR_TYPE = 2,        /* k_type or v_type is not an fa_type                                 */
+  FA_ERR_SHAPE = 3,       /* N, M < 0; H, Hkv < 1; H % Hkv != 0; mask_heads not 1 or H         */
+  FA_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned (workspace: 256-byte aligned)     */
+  FA_ERR_UNSUPPORTED = 5, /* D or Dv not in {64, 128, 256}; size limits exceeded                */
+  FA_ERR_DEVICE = 6,      /* the current device is not compute capability 10.3                  */
+  FA_ERR_CUDA = 7,        /* a CUDA runtime call or kernel launch failed                        */
+  FA_ERR_TIMEOUT = 8,     /* a kernel gave up on a bounded wait (see fa_back_get_error)         */
+  FA_ERR_WORKSPACE = 9    /* workspace is NULL or smaller than fa_back_workspace_size()         */
+} fa_status;
+
+/* Bytes in one cache row of `type` holding D values (-1 if D does not fit the format). */
+long fa_row_bytes(int type, int D);
+
+/* Workspace bytes fa_back() needs on the current device for this shape. */
+size_t fa_back_workspace_size(int N, int M, int H, int Hkv, int D, int Dv);
+
+/*
+ * The backward.  scale multiplies q.k before the mask is added (the reading used for the
+ * pages' tests is scale = 1/sqrt(D)).  causal != 0 applies the causal tail j <= M - N + i.
+ * mask may be NULL; mask_heads (Hm) is ignored then.  Every element of dQ, dK, dV, lse and
+ * delta is written.  Pointers: q, dO, dQ, dK, dV, lse, delta and mask 16-byte aligned; k, v
+ * 16-byte aligned; workspace 256-byte aligned.
+ */
+fa_status fa_back(const float* q, const void* k, int k_type, const void* v, int v_type,
+                  const uint16_t* mask, int mask_heads, const float* dO, float scale, int N, int M,
+                  int H, int Hkv, int D, int Dv, int causal, float* dQ, float* dK, float* dV,
+                  float* lse, float* delta, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Sticky device-side status of the kernels enqueued so far on the current device
+ * (FA_OK or FA_ERR_TIMEOUT).  Synchronises the device, then clears the word. */
+fa_status fa_back_get_error(void);
+
+/* Human-readable name of a status code. */
+const char* fa_back_status_string(int status);
+
+/*
+ * Measurement hook (not part of the operation).  fa_back_profile(1) makes the following
+ * fa_back() calls on this process record a CUDA event after each of their kernel launches
+ * (at most 256 calls are recorded; later calls run unrecorded).  fa_back_profile(0) stops.
+ * fa_back_profile_read() synchronises on the recorded events and writes, for each kernel of
+ * the launch sequence, the summed device time in ms (ms_sum[k]) and the number of recorded
+ * launches (launches[k]); names[k] receives a static string naming the kernel.  It returns the
+ * number of kernels written (at most max_kernels) and clears the record.  The events are
+ * created on first use and kept until process exit; no device memory is allocated.
+ */
+fa_status fa_back_profile(int enable);
+int fa_back_profile_read(float* ms_sum, int* launches, const char** names, int max_kernels);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_BACK_H */

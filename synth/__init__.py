@@ -10,3 +10,4 @@ from .gen import (  # noqa: F401
     Problem, make_problem, from_config, config, CONFIGS, row_bytes,
     normal, uniform, quantize_rows, sample_indices,
 )
+from . import device  # noqa: F401,E402

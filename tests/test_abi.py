@@ -1,0 +1,82 @@
+"""Host-side checks of the C ABI: the library loads, exports what the header declares, and
+rejects bad arguments before touching a GPU."""
+import os
+import re
+
+import pytest
+
+import flash_attention_backward_gb300 as fb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa_back.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from flash_attention_backward_gb300 import build
+    build.build()
+    return fb.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    assert declared_functions() == sorted(
+        ["fa_back", "fa_back_get_error", "fa_back_profile", "fa_back_profile_read", "fa_back_status_string",
+         "fa_back_workspace_size", "fa_row_bytes"])
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_row_bytes(L):
+    assert fb.fa_row_bytes(fb.FA_F32, 256) == 1024
+    assert fb.fa_row_bytes(fb.FA_F16, 128) == 256
+    assert fb.fa_row_bytes(fb.FA_Q8_0, 256) == 8 * 34
+    assert fb.fa_row_bytes(fb.FA_Q4_0, 256) == 8 * 18
+    assert fb.fa_row_bytes(fb.FA_Q8_0, 48) == -1
+    assert fb.fa_row_bytes(7, 64) == -1
+
+
+def test_status_strings(L):
+    for code in range(10):
+        assert fb.fa_back_status_string(code)
+    assert "unknown" in fb.fa_back_status_string(99)
+
+
+def _call(**kw):
+    a = dict(q=0x1000, k=0x2000, k_type=2, v=0x3000, v_type=2, mask=None, mask_heads=0, dO=0x4000, scale=0.1,
+             N=8, M=32, H=4, Hkv=2, D=128, Dv=128, causal=0, dQ=0x5000, dK=0x6000, dV=0x7000, lse=0x8000,
+             delta=0x9000, workspace=0x10000, workspace_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return fb.fa_back(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(k_type=9), "FA_ERR_TYPE"),
+    (dict(v_type=-1), "FA_ERR_TYPE"),
+    (dict(H=6, Hkv=4), "FA_ERR_SHAPE"),
+    (dict(N=-1), "FA_ERR_SHAPE"),
+    (dict(mask=0xA000, mask_heads=2), "FA_ERR_SHAPE"),
+    (dict(D=96, Dv=96), "FA_ERR_UNSUPPORTED"),
+    (dict(D=512), "FA_ERR_UNSUPPORTED"),
+    (dict(q=None), "FA_ERR_NULL"),
+    (dict(dV=None), "FA_ERR_NULL"),
+    (dict(dQ=0x5004), "FA_ERR_ALIGN"),
+    (dict(k=0x2002), "FA_ERR_ALIGN"),
+])
+def test_argument_errors_are_reported_before_any_launch(L, kw, code):
+    assert fb.STATUS[_call(**kw)] == code
+
+
+def test_workspace_size_grows_with_the_problem(L):
+    a = fb.fa_back_workspace_size(64, 512, 8, 2, 128, 128)
+    b = fb.fa_back_workspace_size(2048, 75520, 24, 4, 256, 256)
+    assert 0 < a < b
+    assert fb.fa_back_workspace_size(8, 32, 6, 4, 64, 64) == 0  # H % Hkv != 0

@@ -1,0 +1,128 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Tolerance: NMSE <= 1e-5 per component (dQ, dK, dV, lse, delta tested separately), the bar the
+pages' CPU-oracle comparison uses; lse = -inf positions must agree exactly and fully masked rows
+must give delta = 0 and dQ = 0 exactly.
+"""
+import numpy as np
+import pytest
+
+import synth
+from metrics import NMSE_TOL, check_components, nmse
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fb():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import flash_attention_backward_gb300 as m
+    from flash_attention_backward_gb300 import build
+    build.build()
+    return m
+
+
+def run_gpu(fb, p, ws=None):
+    t = synth.device.to_torch(p, "cuda")
+    out = fb.backward(t["q"], t["k"], p.k_type, t["v"], p.v_type, t["dO"], H=p.H, Hkv=p.Hkv, D=p.D, Dv=p.Dv,
+                      M=p.M, scale=p.scale, causal=p.causal, mask=t["mask"], mask_heads=p.mask_heads,
+                      workspace=ws)
+    torch.cuda.synchronize()
+    assert fb.fa_back_get_error() == 0
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def parity(fb, p, tol=NMSE_TOL):
+    import oracle
+    ref = oracle.fa_back(p)
+    got = run_gpu(fb, p)
+    res = check_components(got, ref, tol)
+    dead = ~np.isfinite(ref["lse"])
+    assert np.all(got["dQ"][dead] == 0.0)
+    return res
+
+
+@pytest.mark.parametrize("cfg", ["0", "1", "1c", "1t", "2", "3"])
+def test_configs(fb, cfg):
+    p = synth.from_config(cfg)
+    res = parity(fb, p)
+    print(cfg, res)
+
+
+EDGE = {
+    # ragged rows and keys, several tiles, f16 cache, causal tail
+    "ragged_f16_causal": dict(N=37, M=301, H=6, Hkv=2, D=128, Dv=128, k_type="f16", v_type="f16", causal=True),
+    # more queries than keys under the causal tail: rows i < N-M see no key
+    "n_gt_m_causal": dict(N=100, M=40, H=4, Hkv=1, D=64, Dv=64, k_type="q8_0", v_type="q8_0", causal=True),
+    # Dv != D, mixed cache types
+    "d256_dv128": dict(N=50, M=700, H=8, Hkv=2, D=256, Dv=128, k_type="q8_0", v_type="q4_0"),
+    "d64_dv128_f32": dict(N=33, M=200, H=4, Hkv=4, D=64, Dv=128, k_type="f32", v_type="f32", causal=True),
+    "d128_dv256": dict(N=20, M=150, H=3, Hkv=1, D=128, Dv=256, k_type="f16", v_type="q8_0"),
+    # additive finite mask shared by all heads (Hm = 1) with -inf entries and dead rows
+    "finite_mask_hm1": dict(N=40, M=333, H=4, Hkv=2, D=128, Dv=128, k_type="q4_0", v_type="q4_0",
+                            mask="finite", mask_p=0.05, full_rows=3, mask_heads=1),
+    # one key, one query
+    "single_key": dict(N=5, M=1, H=2, Hkv=1, D=64, Dv=64, k_type="q8_0", v_type="q8_0"),
+    "single_query": dict(N=1, M=257, H=8, Hkv=2, D=256, Dv=256, k_type="q8_0", v_type="q8_0", causal=True),
+    # large-magnitude inputs (scales are chosen from the data)
+    "big_values": dict(N=16, M=128, H=2, Hkv=1, D=64, Dv=64, k_type="f32", v_type="f32", q_sigma=300.0,
+                       k_sigma=0.01, do_sigma=1e4, v_sigma=50.0),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EDGE))
+def test_edge_cases(fb, name):
+    p = synth.make_problem(name, seed=2000 + sorted(EDGE).index(name), **EDGE[name])
+    print(name, parity(fb, p))
+
+
+@pytest.mark.parametrize("N,M", [(0, 64), (16, 0)])
+def test_empty_inputs(fb, N, M):
+    p = synth.make_problem("empty", N=N, M=M, H=4, Hkv=2, D=128, Dv=128, k_type="q8_0", v_type="q8_0", seed=5)
+    got = run_gpu(fb, p)
+    assert np.all(got["dK"] == 0) and np.all(got["dV"] == 0)
+    assert np.all(np.isneginf(got["lse"])) and np.all(got["delta"] == 0) and np.all(got["dQ"] == 0)
+
+
+def test_bit_identical_reruns(fb):
+    p = synth.from_config("3")
+    a = run_gpu(fb, p)
+    b = run_gpu(fb, p)
+    for k in a:
+        assert np.array_equal(a[k], b[k], equal_nan=True), k
+
+
+def test_workspace_too_small_is_rejected(fb):
+    p = synth.from_config("1")
+    t = synth.device.to_torch(p, "cuda")
+    need = fb.fa_back_workspace_size(p.N, p.M, p.H, p.Hkv, p.D, p.Dv)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    outs = [torch.empty(1 << 20, device="cuda") for _ in range(5)]
+    rc = fb.fa_back(t["q"].data_ptr(), t["k"].data_ptr(), p.k_type, t["v"].data_ptr(), p.v_type, None, 0,
+                    t["dO"].data_ptr(), p.scale, p.N, p.M, p.H, p.Hkv, p.D, p.Dv, 1,
+                    *[o.data_ptr() for o in outs], ws.data_ptr(), need - 1, None)
+    assert fb.STATUS[rc] == "FA_ERR_WORKSPACE"
+
+
+@pytest.mark.slow
+def test_long_context_sampled(fb):
+    """N2048/M75520/H24/Hkv4/D256 q8_0, causal tail: every lse/delta, 64 dQ rows and 256 dK/dV
+    key positions against the oracle, plus invariants over the whole output."""
+    import oracle
+    p = synth.from_config("4")
+    got = run_gpu(fb, p)
+    rows = synth.sample_indices(1004, synth.gen.S_SAMPLE, p.N, 64)
+    keys = synth.sample_indices(1004, synth.gen.S_SAMPLE + 1, p.M, 256)
+    ref = oracle.fa_back(p, dq_rows=rows, dkv_keys=keys)
+    sub = {"lse": got["lse"], "delta": got["delta"], "dQ": got["dQ"][rows], "dK": got["dK"][keys],
+           "dV": got["dV"][keys]}
+    print(check_components(sub, ref))
+    # sum_j dS_ij = 0  =>  sum_j dK_j = 0;  sum_j p_ij = 1  =>  sum_j dV_j = sum_i dO_i
+    for hk in range(p.Hkv):
+        sk = got["dK"][:, hk].astype(np.float64).sum(axis=0)
+        scale_k = np.abs(got["dK"][:, hk].astype(np.float64)).sum(axis=0).max()
+        assert np.max(np.abs(sk)) <= 1e-3 * scale_k
+        want = p.dO[:, hk * p.G:(hk + 1) * p.G].astype(np.float64).sum(axis=(0, 1))
+        assert nmse(got["dV"][:, hk].astype(np.float64).sum(axis=0), want) < 1e-8
