@@ -112,11 +112,15 @@ def cpu_baseline(p, target_s: float = 12.0):
                               q=p.q[p.N - n:], k=p.k, v=p.v, dO=p.dO[p.N - n:], mask=None, mask_heads=0)
         return q
 
-    n = 2
-    t0 = time.perf_counter()
-    oracle.fa_back(sub(n))
-    t_small = time.perf_counter() - t0
-    n = int(max(2, min(p.N, n * target_s / max(t_small, 1e-3))))
+    # calibrate: time = a + b * n (a = decoding the cache, b = one query position)
+    ts = {}
+    for n in (2, 6):
+        t0 = time.perf_counter()
+        oracle.fa_back(sub(n))
+        ts[n] = time.perf_counter() - t0
+    b = max((ts[6] - ts[2]) / 4, 1e-4)
+    a = max(ts[2] - 2 * b, 0.0)
+    n = int(max(2, min(p.N, (target_s - a) / b)))
     s = sub(n)
     t0 = time.perf_counter()
     oracle.fa_back(s)

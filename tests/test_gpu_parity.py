@@ -125,4 +125,4 @@ def test_long_context_sampled(fb):
         scale_k = np.abs(got["dK"][:, hk].astype(np.float64)).sum(axis=0).max()
         assert np.max(np.abs(sk)) <= 1e-3 * scale_k
         want = p.dO[:, hk * p.G:(hk + 1) * p.G].astype(np.float64).sum(axis=(0, 1))
-        assert nmse(got["dV"][:, hk].astype(np.float64).sum(axis=0), want) < 1e-8
+        assert nmse(got["dV"][:, hk].astype(np.float64).sum(axis=0), want) <= NMSE_TOL
