@@ -41,6 +41,8 @@ def lib():
     L.fa_back_get_error.argtypes = []
     L.fa_back_status_string.restype = ctypes.c_char_p
     L.fa_back_status_string.argtypes = [i]
+    L.fa_back_noalloc.restype = i
+    L.fa_back_noalloc.argtypes = [vp, vp, i, vp, i, vp, i, vp, f, i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp]
     L.fa_back_profile.restype = i
     L.fa_back_profile.argtypes = [i]
     L.fa_back_profile_read.restype = i
@@ -83,3 +85,13 @@ def fa_back_profile_read(max_kernels: int = 16) -> dict:
     names = (ctypes.c_char_p * max_kernels)()
     n = int(lib().fa_back_profile_read(ms, cnt, names, max_kernels))
     return {names[k].decode(): (float(ms[k]), int(cnt[k])) for k in range(n) if cnt[k] > 0}
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def fa_back_noalloc(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal,
+                    dQ, dK, dV, lse, delta, stream) -> int:
+    """fa_back with the library's static scratch instead of a caller workspace (see the header)."""
+    return int(lib().fa_back_noalloc(q, k, k_type, v, v_type, mask, mask_heads, dO, float(scale), N, M, H, Hkv,
+                                     D, Dv, int(causal), dQ, dK, dV, lse, delta, stream))

@@ -1,0 +1,54 @@
+// fa_back_noalloc(): the backward for callers that cannot allocate device memory.
+//
+// Some callers cannot hand the library a workspace: graph executors that own every device
+// buffer through their own pool and expose no scratch pointer to an operator, and services
+// that allocate nothing once they are set up.  This entry point serves them from one file-scope
+// device array of FA_NOALLOC_SCRATCH_BYTES, resident on every GPU that loads the library until
+// the process exits.  It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+// routine.  The launch sequence is fa_back()'s, given that array as its workspace.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/fa_back.h"
+
+namespace {
+
+constexpr size_t kScratchBytes = FA_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch[kMaxDevices] = {};  // device address of g_noalloc_scratch, per device
+
+// Device address of the scratch array on the current device.  In host code the array's name
+// is only a host-side stand-in, so the address is looked up once per device with that device
+// current (this happens during the first call on the device).
+void* scratch_on(int dev, cudaError_t* err) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_scratch[dev]) {
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    g_scratch[dev] = p;
+  }
+  return g_scratch[dev];
+}
+
+}  // namespace
+
+extern "C" fa_status fa_back_noalloc(const float* q, const void* k, int k_type, const void* v, int v_type,
+                                     const uint16_t* mask, int mask_heads, const float* dO, float scale, int N,
+                                     int M, int H, int Hkv, int D, int Dv, int causal, float* dQ, float* dK,
+                                     float* dV, float* lse, float* delta, void* stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_DEVICE;
+  const size_t need = fa_back_workspace_size(N, M, H, Hkv, D, Dv);
+  if (need > kScratchBytes) return FA_ERR_WORKSPACE;  // larger than the static scratch
+  cudaError_t err = cudaSuccess;
+  void* scratch = scratch_on(dev, &err);
+  if (!scratch) return FA_ERR_CUDA;
+  return fa_back(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal, dQ, dK, dV,
+                 lse, delta, scratch, kScratchBytes, stream);
+}

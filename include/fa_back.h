@@ -114,6 +114,30 @@ const char* fa_back_status_string(int status);
 fa_status fa_back_profile(int enable);
 int fa_back_profile_read(float* ms_sum, int* launches, const char** names, int max_kernels);
 
+/*
+ * fa_back() for callers that cannot allocate device memory (no counterpart in the paper: the
+ * pages' operator has no workspace argument).  Some callers cannot hand the library a
+ * workspace: graph executors that own every device buffer through their own pool and give an
+ * operator no scratch pointer, and services that allocate nothing once they are set up.  This
+ * entry point takes the same arguments as fa_back() minus the workspace and uses instead one
+ * file-scope device array of FA_NOALLOC_SCRATCH_BYTES (64 MiB), which every GPU that loads the
+ * library holds until the process exits.  It calls no cudaMalloc, cudaFree or other allocating
+ * routine; the caller still passes every input and output.
+ *   - Problems whose fa_back_workspace_size() exceeds FA_NOALLOC_SCRATCH_BYTES are rejected
+ *     with FA_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on a device looks up the array's device address with that device
+ *     current; make that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last call's contents.
+ *     Nothing in it needs to start at zero: each call writes every scratch word before reading
+ *     it.  Calls whose work overlaps on the GPU (other streams, other threads) race on the
+ *     array; serialise them.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (64ull << 20)
+fa_status fa_back_noalloc(const float* q, const void* k, int k_type, const void* v, int v_type,
+                          const uint16_t* mask, int mask_heads, const float* dO, float scale, int N,
+                          int M, int H, int Hkv, int D, int Dv, int causal, float* dQ, float* dK,
+                          float* dV, float* lse, float* delta, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,68 @@
+"""fa_back_noalloc() against fa_back(): same results through the C ABI, two calls in a row.
+
+fa_back_noalloc() serves callers that cannot allocate device memory (pool-owning graph
+executors that give an operator no scratch pointer, services that allocate nothing after
+set-up) from the library's static device scratch.  The two problems differ in shape, so a
+second call that read stale scratch from the first would show up here.
+"""
+import numpy as np
+import pytest
+
+import synth
+from metrics import NMSE_TOL, check_components
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fb():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import flash_attention_backward_gb300 as m
+    from flash_attention_backward_gb300 import build
+    build.build()
+    return m
+
+
+def _outputs(p):
+    return {"dQ": torch.empty((p.N, p.H, p.D), device="cuda"), "dK": torch.empty((p.M, p.Hkv, p.D), device="cuda"),
+            "dV": torch.empty((p.M, p.Hkv, p.Dv), device="cuda"), "lse": torch.empty((p.N, p.H), device="cuda"),
+            "delta": torch.empty((p.N, p.H), device="cuda")}
+
+
+def _noalloc(fb, p, t):
+    out = _outputs(p)
+    mask = t["mask"].data_ptr() if t["mask"] is not None else None
+    rc = fb.fa_back_noalloc(t["q"].data_ptr(), t["k"].data_ptr(), p.k_type, t["v"].data_ptr(), p.v_type, mask,
+                            p.mask_heads, t["dO"].data_ptr(), p.scale, p.N, p.M, p.H, p.Hkv, p.D, p.Dv, p.causal,
+                            out["dQ"].data_ptr(), out["dK"].data_ptr(), out["dV"].data_ptr(), out["lse"].data_ptr(),
+                            out["delta"].data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert fb.STATUS[rc] == "FA_OK", fb.fa_back_status_string(rc)
+    torch.cuda.synchronize()
+    assert fb.fa_back_get_error() == 0
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def _with_workspace(fb, p, t):
+    out = fb.backward(t["q"], t["k"], p.k_type, t["v"], p.v_type, t["dO"], H=p.H, Hkv=p.Hkv, D=p.D, Dv=p.Dv, M=p.M,
+                      scale=p.scale, causal=p.causal, mask=t["mask"], mask_heads=p.mask_heads)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def test_noalloc_matches_fa_back_on_two_calls_in_a_row(fb):
+    for cfg in ("3", "1"):
+        p = synth.from_config(cfg)
+        t = synth.device.to_torch(p, "cuda")
+        ref = _with_workspace(fb, p, t)
+        got = _noalloc(fb, p, t)
+        check_components(got, ref, NMSE_TOL)
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch(fb):
+    N, M, H, Hkv, D = 16384, 262144, 32, 8, 256
+    assert fb.fa_back_workspace_size(N, M, H, Hkv, D, D) > fb._native.NOALLOC_SCRATCH_BYTES
+    rc = fb.fa_back_noalloc(0x1000, 0x2000, 2, 0x3000, 2, None, 0, 0x4000, 0.0625, N, M, H, Hkv, D, D, 1,
+                            0x5000, 0x6000, 0x7000, 0x8000, 0x9000, None)
+    assert fb.STATUS[rc] == "FA_ERR_WORKSPACE"
