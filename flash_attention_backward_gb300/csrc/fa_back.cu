@@ -33,8 +33,8 @@ __device__ int g_err = 0;
 struct Plan {
   int G, R, nQT, BK, nKT, nsplit, kt_per_split, nsplit_dq;
   int nblk_stats, nbv;
-  size_t off_stats, off_rmean, off_dOr, off_lse2, off_dlt, off_part, off_dqpart, off_q16, off_do16, off_bstat,
-      off_vsum, total;
+  size_t off_stats, off_rmean, off_rsh, off_dOr, off_lse2, off_dlt, off_part, off_dqpart, off_q16, off_do16,
+      off_bstat, off_vsum, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -62,6 +62,7 @@ static Plan make_plan(int N, int M, int H, int Hkv, int D, int Dv, int nsm) {
   size_t o = 0;
   P.off_stats = o; o = align256(o + sizeof(Stats));
   P.off_rmean = o; o = align256(o + sizeof(float) * (size_t)Hkv * Dv);
+  P.off_rsh = o; o = align256(o + sizeof(float) * (size_t)Hkv * Dv);
   P.off_dOr = o; o = align256(o + sizeof(float) * (size_t)Hkv * P.R);
   P.off_lse2 = o; o = align256(o + sizeof(float) * (size_t)Hkv * P.R);
   P.off_dlt = o; o = align256(o + sizeof(float) * (size_t)Hkv * P.R);
@@ -158,6 +159,24 @@ struct CallRec {
   }
 };
 
+// Raw cache rows of one tensor as a 3D map (row elements, KV head, key), elements of 2, 4 or 8
+// bytes so that one row is at most 256 elements; boxes cover one head and KE keys.
+static bool make_raw_map(CUtensorMap* m, const void* base, long rb, int Hkv, int M, int ke) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  int es = 2;
+  while (rb / es > 256) es *= 2;
+  const CUtensorMapDataType dt =
+      es == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : es == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32 : CU_TENSOR_MAP_DATA_TYPE_INT64;
+  cuuint64_t dims[3] = {(cuuint64_t)(rb / es), (cuuint64_t)Hkv, (cuuint64_t)M};
+  cuuint64_t strides[2] = {(cuuint64_t)rb, (cuuint64_t)rb * Hkv};
+  cuuint32_t box[3] = {(cuuint32_t)(rb / es), 1, (cuuint32_t)ke};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------------------------------------
 // launch sequence for one (D, Dv)
 
@@ -166,33 +185,59 @@ static cudaError_t set_smem(K kernel, int bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
+// Raw K/V staging of the row passes: entry size (keys) and ring depth that fit the budget.
+static void pick_raw(Params& q, int budget, int BK) {
+  const int pair = q.rbk_pad + q.rbv_pad;
+  int ke = std::min(32, BK);
+  while (ke > 1 && 2 * ke * pair > budget) ke >>= 1;
+  q.ke = ke;
+  q.raw_depth = std::max(2, std::min(4, budget / std::max(1, ke * pair)));
+}
+
 template <int D, int Dv>
 static cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& tmQ, const CUtensorMap& tmO,
                              cudaStream_t s, CallRec& rec) {
   constexpr int BK = (D + Dv <= 256) ? 128 : 64;
-  using RL = RowsCfg<D, Dv, BK, 0>;
-  using RQ = RowsCfg<D, Dv, BK, 1>;
-  using CC = ColsCfg<D, Dv, BK>;
-  static_assert(RQ::SMEM <= 232448 && CC::SMEM <= 232448, "shared memory budget");
-  static_assert(RQ::TCOLS <= 512 && CC::TCOLS <= 512, "tensor memory budget");
+  using RL = Rows2Cfg<D, Dv, BK, 0>;
+  using RQ = Rows2Cfg<D, Dv, BK, 1>;
+  using CC = Cols2Cfg<D, Dv, BK>;
+  static_assert(RL::RAW_BUDGET > 0 && RQ::RAW_BUDGET > 0 && CC::SMEM <= 232448, "shared memory budget");
+  static_assert(RL::TCOLS <= 512 && RQ::TCOLS <= 512 && CC::TCOLS <= 512, "tensor memory budget");
+  Params pl = p, pq = p;
+  pick_raw(pl, RL::RAW_BUDGET, BK);
+  pick_raw(pq, RQ::RAW_BUDGET, BK);
+  for (Params* q : {&pl, &pq})  // TMA destinations must start on 128-byte boundaries
+    if ((q->ke * q->rbk_pad) % 128 || (q->ke * q->rbv_pad) % 128) q->raw_bulk = 0;
+  // + 1024 for aligning the base, + 64 for the decoders' realigning reads past the last raw row
+  const int sm_l = RL::OFF_RAW + pl.raw_depth * pl.ke * (p.rbk_pad + p.rbv_pad) + 1024 + 64;
+  const int sm_q = RQ::OFF_RAW + pq.raw_depth * pq.ke * (p.rbk_pad + p.rbv_pad) + 1024 + 64;
+  if (sm_l > 232448 || sm_q > 232448) return cudaErrorInvalidValue;
   cudaError_t e;
-  if ((e = set_smem(k_rows<D, Dv, BK, 0>, RL::SMEM)) != cudaSuccess) return e;
-  if ((e = set_smem(k_rows<D, Dv, BK, 1>, RQ::SMEM)) != cudaSuccess) return e;
-  if ((e = set_smem(k_cols<D, Dv, BK>, CC::SMEM)) != cudaSuccess) return e;
+  if ((e = set_smem(k_rows2<D, Dv, BK, 0>, sm_l)) != cudaSuccess) return e;
+  if ((e = set_smem(k_rows2<D, Dv, BK, 1>, sm_q)) != cudaSuccess) return e;
+  if ((e = set_smem(k_cols2<D, Dv, BK>, CC::SMEM)) != cudaSuccess) return e;
 
+  CUtensorMap tkl, tvl, tkq, tvq;
+  std::memset(&tkl, 0, sizeof(tkl));
+  tvl = tkq = tvq = tkl;
+  if (p.raw_bulk) {
+    if (!make_raw_map(&tkl, p.k, p.rbk, p.Hkv, p.M, pl.ke) || !make_raw_map(&tvl, p.v, p.rbv, p.Hkv, p.M, pl.ke) ||
+        !make_raw_map(&tkq, p.k, p.rbk, p.Hkv, p.M, pq.ke) || !make_raw_map(&tvq, p.v, p.rbv, p.Hkv, p.M, pq.ke))
+      return cudaErrorInvalidValue;
+  }
   dim3 grows(P.nQT, p.Hkv, P.nsplit);
-  k_rows<D, Dv, BK, 0><<<grows, 128, RL::SMEM, s>>>(tmQ, tmO, p);
+  k_rows2<D, Dv, BK, 0><<<grows, 512, sm_l, s>>>(tmQ, tkl, tvl, pl);
   rec.mark(KS_ROWS_LSE);
   k_lse_merge<<<(unsigned)(((long)p.Hkv * P.R + 255) / 256), 256, 0, s>>>(p);
   rec.mark(KS_MERGE);
-  k_rows<D, Dv, BK, 1><<<grows, 128, RQ::SMEM, s>>>(tmQ, tmO, p);
+  k_rows2<D, Dv, BK, 1><<<grows, 512, sm_q, s>>>(tmQ, tkq, tvq, pq);
   rec.mark(KS_ROWS_DQ);
   if (P.nsplit_dq > 1) {
     k_dq_reduce<<<(unsigned)(((long)p.Hkv * P.R * (D / 4) + 255) / 256), 256, 0, s>>>(p);
     rec.mark(KS_DQ_REDUCE);
   }
   if (P.nKT > 0) {
-    k_cols<D, Dv, BK><<<dim3(P.nKT, p.Hkv), 128, CC::SMEM, s>>>(tmQ, tmO, p);
+    k_cols2<D, Dv, BK><<<dim3(P.nKT, p.Hkv), 512, CC::SMEM, s>>>(tmQ, tmO, p);
     rec.mark(KS_COLS);
   }
   return cudaGetLastError();
@@ -308,6 +353,10 @@ extern "C" fa_status fa_back(const float* q, const void* k, int k_type, const vo
   p.nblk_stats = P.nblk_stats;
   p.vsum = reinterpret_cast<float*>(ws + P.off_vsum);
   p.nbv = P.nbv;
+  p.rsh = reinterpret_cast<float*>(ws + P.off_rsh);
+  p.raw_bulk = (rbk % 16 == 0 && rbv % 16 == 0 && rbk <= 2048 && rbv <= 2048) ? 1 : 0;
+  p.rbk_pad = (int)((rbk + 15) / 16 * 16);
+  p.rbv_pad = (int)((rbv + 15) / 16 * 16);
   p.err = errp;
 
   CUtensorMap tmQ, tmO;

@@ -72,6 +72,12 @@ struct Params {
   int nblk_stats;
   float* vsum;    // [nbv][Hkv][Dv]
   int nbv;
+  float* rsh;     // [Hkv][Dv]  -r' * sV, an exact binary16 value (the decoders' V shift)
+  // raw K/V staging of the row passes
+  int raw_bulk;        // 1: rows are 16-byte multiples, copied by bulk async copies; 0: 4-byte async copies
+  int rbk_pad, rbv_pad;  // raw row strides in shared memory (16-byte multiples)
+  int ke;              // keys per raw ring entry
+  int raw_depth;       // ring entries (2..4)
   int* err;
 };
 
@@ -103,79 +109,189 @@ __device__ __forceinline__ float decode_elem(const uint8_t* row, int type, int c
   return (float)(nib - 8) * d;
 }
 
-// Decode 8 consecutive elements c0..c0+7 (c0 % 8 == 0) of a raw row; the codes are unpacked in
-// pairs and every value is exact in f32 (a q8_0 value has at most 7 + 11 significant bits).
-__device__ __forceinline__ void decode8(const uint8_t* row, int type, int c0, float* x) {
-  if (type == kTypeF32) {
-    const float4* p = reinterpret_cast<const float4*>(row + 4 * c0);
-    const float4 a = __ldg(p), b = __ldg(p + 1);
-    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
-  } else if (type == kTypeF16) {
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + 2 * c0));
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// Byte offset of the 8-value unit (row, c0) in a tile of DD/64 panels of [rows][64] binary16
+// (128-byte rows, 128-byte swizzle).
+__device__ __forceinline__ uint32_t panel_off_u(int rows, int row, int c0) {
+  return (uint32_t)(c0 >> 6) * (uint32_t)(rows * 128) + swz128((uint32_t)row * 128 + (uint32_t)((c0 & 63) >> 3) * 16);
+}
+
+// Two 8-bit values b0, b1 (bits 0..15 of x, already biased to 0..255) as binary16 1024 + b:
+// the bytes are placed under the exponent byte 0x64, which makes the mantissa the value.
+__device__ __forceinline__ __half2 bytes_as_h2_plus1024(uint32_t x) {
+  return u32_as_h2(__byte_perm(x, 0x64646464u, 0x5140));
+}
+
+// Decode 8 consecutive values c0..c0+7 (c0 % 8 == 0) of a raw row into four packed binary16
+// pairs, out = x^ * sig - shift (shift may be null; shift[c] is an exact binary16 value).
+// Codes are turned into exact binary16 integers in pairs; one fused multiply-add then applies
+// the block scale, the power-of-two operand scale and the shift with a single rounding.  The
+// row pointer may point to global or shared memory.
+__device__ __forceinline__ uint4 decode8_h(const uint8_t* row, int type, int c0, float sig, const float* shift) {
+  uint32_t w[4];
+  __half2 sh[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    sh[e] = shift ? __floats2half2_rn(shift[c0 + 2 * e], shift[c0 + 2 * e + 1]) : __floats2half2_rn(0.f, 0.f);
+  if (type == kTypeQ8 || type == kTypeQ4) {
+    const bool q8 = type == kTypeQ8;
+    const uint8_t* b = row + (q8 ? 34 : 18) * (c0 >> 5);
+    const float d = __half2float(*reinterpret_cast<const __half*>(b));
+    const __half2 ds = __float2half2_rn(d * sig);
+    const int o = c0 & 31;
+    const uint16_t* cp = reinterpret_cast<const uint16_t*>(b + 2 + (q8 ? o : (o & 15)));
+    const __half2 bias = q8 ? __float2half2_rn(1152.f) : __float2half2_rn(1032.f);
+    const int sh4 = (o >= 16) ? 4 : 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-      x[2 * e] = f.x, x[2 * e + 1] = f.y;
+      const uint32_t pr = cp[e];
+      const uint32_t x = q8 ? (pr ^ 0x8080u) : ((pr >> sh4) & 0x0f0fu);
+      const __half2 code = __hsub2(bytes_as_h2_plus1024(x), bias);  // q8_0: int8 code; q4_0: nibble - 8
+      w[e] = h2_as_u32(__hfma2(code, ds, sh[e]));
     }
-  } else if (type == kTypeQ8) {
-    const uint8_t* b = row + 34 * (c0 >> 5);
-    const float d = h2f(__ldg(reinterpret_cast<const unsigned short*>(b)));
-    const unsigned short* cp = reinterpret_cast<const unsigned short*>(b + 2 + (c0 & 31));
+  } else if (type == kTypeF16) {
+    const uint4 u = *reinterpret_cast<const uint4*>(row + 2 * c0);
+    const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+    const __half2 s2 = __float2half2_rn(sig);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w[e] = h2_as_u32(__hfma2(u32_as_h2(in[e]), s2, sh[e]));
+  } else {
+    const float4 a = *reinterpret_cast<const float4*>(row + 4 * c0);
+    const float4 c = *reinterpret_cast<const float4*>(row + 4 * c0 + 16);
+    const float x[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const unsigned short pr = __ldg(cp + e);  // two codes
-      x[2 * e] = (float)(int8_t)(pr & 0xff) * d;
-      x[2 * e + 1] = (float)(int8_t)(pr >> 8) * d;
+      const float2 f = __half22float2(sh[e]);
+      w[e] = h2_as_u32(__floats2half2_rn(fmaf(x[2 * e], sig, f.x), fmaf(x[2 * e + 1], sig, f.y)));
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// ---- decoders of the row passes: raw rows staged in shared memory -> binary16 operand tiles
+//
+// A decoder thread owns one column group of every row it handles: a whole 32-value block for
+// q8_0 / q4_0 (one scale load, the codes read as aligned 32-bit words and realigned with funnel
+// shifts), 8 values for f16 / f32.  Its V shifts are therefore fixed and held in registers.
+__device__ __forceinline__ int group_cols(int type) { return (type == kTypeQ8 || type == kTypeQ4) ? 32 : 8; }
+
+template <int DD, int NT>
+__device__ __forceinline__ void load_group_shift(const float* shift, int type, int dt, __half2* sh) {
+  const int cg = group_cols(type), g = dt % (DD / cg);
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const int c = g * cg + 2 * e;
+    sh[e] = (2 * e < cg) ? __floats2half2_rn(shift[c], shift[c + 1]) : __float2half2_rn(0.f);
+  }
+}
+
+// Four packed binary16 pairs from four bytes holding values v+1024 after the exponent trick.
+__device__ __forceinline__ void four_codes(uint32_t c, __half2 bias, __half2 ds, __half2 s0, __half2 s1, uint32_t& o0,
+                                           uint32_t& o1) {
+  const __half2 lo = u32_as_h2(__byte_perm(c, 0x64646464u, 0x5140));  // bytes 0, 1
+  const __half2 hi = u32_as_h2(__byte_perm(c, 0x64646464u, 0x7362));  // bytes 2, 3
+  o0 = h2_as_u32(__hfma2(__hsub2(lo, bias), ds, s0));
+  o1 = h2_as_u32(__hfma2(__hsub2(hi, bias), ds, s1));
+}
+
+// Decode raw rows 0..nrows-1 of one staged entry (shared address raw0, stride rb_pad) into
+// rows prow0.. of a tile of DD/64 panels of [BKR][64]; rows >= nvalid become zero.
+template <int DD, int BKR, int NT, bool SHIFT>
+__device__ __forceinline__ void decode_rows(int type, uint32_t raw0, int rb_pad, int nrows, int nvalid, int prow0,
+                                            uint32_t panels, float sig, const __half2* sh, int dt) {
+  const int cg = group_cols(type), ng = DD / cg, g = dt % ng, rs = NT / ng;
+  const __half2 z = __float2half2_rn(0.f);
+  if (type == kTypeQ8 || type == kTypeQ4) {
+    const bool q8 = type == kTypeQ8;
+    const int bbytes = q8 ? 34 : 18;
+    const __half2 bias = q8 ? __float2half2_rn(1152.f) : __float2half2_rn(1032.f);
+    for (int rr = dt / ng; rr < nrows; rr += rs) {
+      uint32_t o[16];
+      if (rr < nvalid) {
+        const uint32_t blk = raw0 + rr * rb_pad + g * bbytes;
+        const float d = __half2float(__ushort_as_half((unsigned short)lds_u16(blk)));
+        const __half2 ds = __float2half2_rn(d * sig);
+        const uint32_t cs = blk + 2, cb = cs & ~3u, shf = (cs & 3u) * 8;
+        if (q8) {
+          uint32_t w[9];
+#pragma unroll
+          for (int k = 0; k < 9; ++k) w[k] = lds_u32(cb + 4 * k);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t c = __funnelshift_r(w[k], w[k + 1], shf) ^ 0x80808080u;  // codes + 128
+            four_codes(c, bias, ds, SHIFT ? sh[2 * k] : z, SHIFT ? sh[2 * k + 1] : z, o[2 * k], o[2 * k + 1]);
+          }
+        } else {
+          uint32_t w[5];
+#pragma unroll
+          for (int k = 0; k < 5; ++k) w[k] = lds_u32(cb + 4 * k);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t c = __funnelshift_r(w[k], w[k + 1], shf);  // bytes 4k..4k+3
+            four_codes(c & 0x0f0f0f0fu, bias, ds, SHIFT ? sh[2 * k] : z, SHIFT ? sh[2 * k + 1] : z, o[2 * k],
+                       o[2 * k + 1]);  // values 4k..4k+3 (low nibbles)
+            four_codes((c >> 4) & 0x0f0f0f0fu, bias, ds, SHIFT ? sh[8 + 2 * k] : z, SHIFT ? sh[8 + 2 * k + 1] : z,
+                       o[8 + 2 * k], o[8 + 2 * k + 1]);  // values 16+4k.. (high nibbles)
+          }
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) o[k] = 0u;
+      }
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        sts_v4(panels + panel_off_u(BKR, prow0 + rr, g * 32 + 8 * m), o[4 * m], o[4 * m + 1], o[4 * m + 2],
+               o[4 * m + 3]);
     }
   } else {
-    const uint8_t* b = row + 18 * (c0 >> 5);
-    const float d = h2f(__ldg(reinterpret_cast<const unsigned short*>(b)));
-    const int o = c0 & 31;
-    const unsigned short* cp = reinterpret_cast<const unsigned short*>(b + 2 + (o & 15));
-    const int sh = o < 16 ? 0 : 4;
+    const bool f16 = type == kTypeF16;
+    const __half2 s2 = __float2half2_rn(sig);
+    for (int rr = dt / ng; rr < nrows; rr += rs) {
+      uint32_t o[4] = {0u, 0u, 0u, 0u};
+      if (rr < nvalid) {
+        const uint32_t a = raw0 + rr * rb_pad + g * (f16 ? 16 : 32);
+        if (f16) {
+          const uint4 v = lds_v4(a);
+          const uint32_t in[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const unsigned short pr = __ldg(cp + e);  // two bytes -> two nibbles of this half
-      x[2 * e] = (float)((int)((pr >> sh) & 15) - 8) * d;
-      x[2 * e + 1] = (float)((int)((pr >> (8 + sh)) & 15) - 8) * d;
+          for (int e = 0; e < 4; ++e) o[e] = h2_as_u32(__hfma2(u32_as_h2(in[e]), s2, SHIFT ? sh[e] : z));
+        } else {
+          const uint4 u0 = lds_v4(a), u1 = lds_v4(a + 16);
+          const uint32_t in[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(SHIFT ? sh[e] : z);
+            o[e] = h2_as_u32(__floats2half2_rn(fmaf(__uint_as_float(in[2 * e]), sig, f.x),
+                                               fmaf(__uint_as_float(in[2 * e + 1]), sig, f.y)));
+          }
+        }
+      }
+      sts_v4(panels + panel_off_u(BKR, prow0 + rr, g * 8), o[0], o[1], o[2], o[3]);
     }
   }
 }
 
-// Decode BK cache rows (keys j0.., KV head hk) into a binary16 operand tile: DD/64 panels of
-// [BK rows][64 columns], 128-byte rows, 128-byte swizzled.  Keys >= M become zero rows.
-// out = (x^ - shift[c]) * sigma  (shift may be null).
+// Byte offset of 8-value unit (row, c0) in a tile of DD/64 panels of [rows][64] binary16.
+__device__ __forceinline__ uint32_t panel_off(int rows, int row, int c0) {
+  return (uint32_t)(c0 >> 6) * (uint32_t)(rows * 128) + swz128((uint32_t)row * 128 + (uint32_t)((c0 & 63) >> 3) * 16);
+}
+
+// Decode BK cache rows (keys j0.., KV head hk) straight from global memory into a binary16
+// operand tile (DD/64 panels of [BK rows][64 columns], 128-byte swizzled).  Keys >= M become zero.
 template <int DD, int BK, int NT>
 __device__ __forceinline__ void decode_tile(const uint8_t* base, int type, int rb, int hk, int Hkv, int j0, int M,
-                                            uint8_t* panels, float sigma, const float* shift) {
-  constexpr int UPR = DD / 8;  // 8-element units per row
-  for (int u = threadIdx.x; u < BK * UPR; u += NT) {
+                                            uint8_t* panels, float sigma, const float* shift, int tid) {
+  constexpr int UPR = DD / 8;
+  const uint32_t pu = smem_u32(panels);
+  for (int u = tid; u < BK * UPR; u += NT) {
     const int row = u / UPR;
     const int c0 = (u % UPR) * 8;
     const int j = j0 + row;
-    float x[8];
-    if (j < M) {
-      decode8(base + ((size_t)j * Hkv + hk) * rb, type, c0, x);
-      if (shift) {
-        const float4 s0 = __ldg(reinterpret_cast<const float4*>(shift + c0));
-        const float4 s1 = __ldg(reinterpret_cast<const float4*>(shift + c0 + 4));
-        x[0] -= s0.x, x[1] -= s0.y, x[2] -= s0.z, x[3] -= s0.w;
-        x[4] -= s1.x, x[5] -= s1.y, x[6] -= s1.z, x[7] -= s1.w;
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] *= sigma;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = 0.f;
-    }
-    uint4 w;
-    __half2 h0 = __floats2half2_rn(x[0], x[1]), h1 = __floats2half2_rn(x[2], x[3]);
-    __half2 h2 = __floats2half2_rn(x[4], x[5]), h3 = __floats2half2_rn(x[6], x[7]);
-    w.x = *reinterpret_cast<uint32_t*>(&h0), w.y = *reinterpret_cast<uint32_t*>(&h1);
-    w.z = *reinterpret_cast<uint32_t*>(&h2), w.w = *reinterpret_cast<uint32_t*>(&h3);
-    const uint32_t off = (uint32_t)(c0 / 64) * (BK * 128) + swz128((uint32_t)row * 128 + (uint32_t)((c0 & 63) / 8) * 16);
-    *reinterpret_cast<uint4*>(panels + off) = w;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (j < M) w = decode8_h(base + ((size_t)j * Hkv + hk) * rb, type, c0, sigma, shift);
+    sts_v4(pu + panel_off(BK, row, c0), w);
   }
 }
 
@@ -287,7 +403,7 @@ __global__ void __launch_bounds__(256) k_finalize(Params p) {
     if (w == 0) am[t] = m;
     else nm[t] = m;
   }
-  // column means of V^ (chunks in order), per-head squared norm and max |r|
+  // column means of V^ (chunks in order) and max |r|
   float my_am = 0.f;
   const float invM = p.M > 0 ? 1.f / (float)p.M : 0.f;
   for (int idx = tid; idx < p.Hkv * p.Dv; idx += 256) {
@@ -297,19 +413,34 @@ __global__ void __launch_bounds__(256) k_finalize(Params p) {
     p.rmean[idx] = r;
     my_am = fmaxf(my_am, fabsf(r));
   }
+  ram[tid] = my_am;
   __syncthreads();
-  // squared norm of each head's r, taken in a fixed order by one thread per head
+  __shared__ float s_sV;
+  if (tid == 0) {
+    float ramax = 0.f;
+    for (int t = 0; t < 256; ++t) ramax = fmaxf(ramax, ram[t]);
+    ram[0] = ramax;
+    s_sV = pow2_scale_for(am[3] + ramax, 14);  // |v^ - r| <= |v^| + |r|
+  }
+  __syncthreads();
+  // the shift actually applied is r' = binary16(r * sV) / sV, so that -r' * sV is exact in binary16
+  for (int idx = tid; idx < p.Hkv * p.Dv; idx += 256) {
+    const float rs = __half2float(__float2half_rn(p.rmean[idx] * s_sV));
+    p.rmean[idx] = rs / s_sV;
+    p.rsh[idx] = -rs;
+  }
+  __syncthreads();
+  // squared norm of each head's r', taken in a fixed order by one thread per head
   if (tid < p.Hkv && tid < 1024) {
     float n2 = 0.f;
     for (int c = 0; c < p.Dv; ++c) n2 = fmaf(p.rmean[tid * p.Dv + c], p.rmean[tid * p.Dv + c], n2);
     rn2[tid] = n2;
   }
-  ram[tid] = my_am;
   __syncthreads();
   if (tid == 0) {
-    float rmax2 = 0.f, ramax = 0.f;
+    float rmax2 = 0.f;
+    const float ramax = ram[0];
     for (int h = 0; h < p.Hkv && h < 1024; ++h) rmax2 = fmaxf(rmax2, rn2[h]);
-    for (int t = 0; t < 256; ++t) ramax = fmaxf(ramax, ram[t]);
     Stats s;
     for (int t = 0; t < 4; ++t) s.amax[t] = am[t], s.norm2[t] = nm[t];
     s.rnorm = sqrtf(rmax2);
@@ -317,11 +448,10 @@ __global__ void __launch_bounds__(256) k_finalize(Params p) {
     s.sQ = pow2_scale_for(am[0], 14);
     s.sdO = pow2_scale_for(am[1], 14);
     s.sK = pow2_scale_for(am[2], 14);
-    const float vamax = am[3] + ramax;  // |v^ - r| <= |v^| + |r|
-    s.sV = pow2_scale_for(vamax, 14);
+    s.sV = s_sV;
     s.sP = 32768.f;
     // |dP'_ij - delta'_i| <= 2 max_j |dO_i . (v^_j - r)| <= 2 |dO_i| (|v^_j| + |r|), in scaled units
-    const float bound = 2.f * (sqrtf(nm[1]) * s.sdO) * ((sqrtf(nm[3]) + s.rnorm) * s.sV) * 1.0001f;
+    const float bound = 2.f * (sqrtf(nm[1]) * s.sdO) * ((sqrtf(nm[3]) + s.rnorm) * s.sV) * 1.01f;
     s.lam = pow2_scale_for(bound, 15);
     s.c2 = p.scale * kLog2e / (s.sQ * s.sK);
     s.dq_fac = p.scale / (s.lam * s.sdO * s.sV * s.sK);
@@ -364,33 +494,93 @@ __global__ void __launch_bounds__(256) k_convert(Params p) {
 
 // ------------------------------------------------------------------------------------------------
 // row-tile passes: LSE/D statistics (MODE 0) and dQ (MODE 1)
+//
+// A CTA owns 128 query rows (r = i*G + g of one KV head) and a range of key tiles of BK keys.
+// Warp roles (16 warps):
+//   warp 0      producer: async copies of raw K/V rows into a ring of `raw_depth` entries
+//               (and, in the dQ pass, the TMA load of the Q tile)
+//   warp 1      tensor-memory owner and MMA issuer (one lane)
+//   warps 4-11  softmax: thread = (row, half of the tile's columns)
+//   warps 12-15 decoders: raw rows -> binary16 K' and V' tiles (128-byte swizzled panels)
+//   warps 2-3   idle
+// Tensor memory: the LSE pass keeps Q and dO there as the A operands of S = Q K'^T and
+// dP = dO V'^T; the dQ pass keeps dO there and Q in shared memory, plus the dQ accumulator.
+// S and dP have one tensor-memory slot; the softmax warps copy them to registers and release
+// the slot at once, so the next tile's products overlap the softmax of this one.
 
 template <int D, int Dv, int BK, int MODE>
-struct RowsCfg {
-  static constexpr int QB = 128 * D * 2, OB = 128 * Dv * 2, KB = BK * D * 2, VB = BK * Dv * 2;
+struct Rows2Cfg {
+  static constexpr int NT = 512;
+  static constexpr int KSTAGES = 2, VSTAGES = MODE ? 1 : 2;
+  static constexpr int QB = MODE ? 128 * D * 2 : 0;
+  static constexpr int KB = BK * D * 2, VB = BK * Dv * 2;
   static constexpr int SB = MODE ? 128 * BK * 2 : 0;
-  static constexpr int OFF_Q = 0, OFF_O = QB, OFF_K = QB + OB, OFF_V = OFF_K + KB, OFF_S = OFF_V + VB;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + QB;
+  static constexpr int OFF_V = OFF_K + KSTAGES * KB;
+  static constexpr int OFF_S = OFF_V + VSTAGES * VB;
   static constexpr int OFF_BAR = OFF_S + SB;
-  static constexpr int SMEM = OFF_BAR + 64 + 1024;  // + alignment slack
-  static constexpr int TCOLS = pow2_at_least(MODE ? 2 * BK + D : 2 * BK);
+  static constexpr int BAR_BYTES = 2048;  // barriers, tensor-memory slot, LSE merge area
+  static constexpr int OFF_RAW = OFF_BAR + BAR_BYTES;
+  static constexpr int SMEM_MAX = 232448;
+  static constexpr int RAW_BUDGET = SMEM_MAX - 1024 - 64 - OFF_RAW;  // bytes for the raw ring
+  // tensor-memory columns
+  static constexpr int T_Q = 0;
+  static constexpr int T_O = MODE ? 0 : D / 2;
+  static constexpr int T_S = T_O + Dv / 2;
+  static constexpr int T_P = T_S + BK;
+  static constexpr int T_ACC = T_P + BK;
+  static constexpr int TCOLS = pow2_at_least(MODE ? T_ACC + D : T_P + BK);
+  static constexpr int HALF = BK / 2;  // columns per softmax thread
+};
+
+// barrier indices
+enum {
+  B_RAW_FULL = 0,   // [4]
+  B_RAW_EMPTY = 4,  // [4]
+  B_KV_FULL = 8,    // [2]
+  B_K_EMPTY = 10,   // [2]
+  B_V_EMPTY = 12,   // [2]
+  B_S_FULL = 14,
+  B_S_FREE,
+  B_DS_FULL,
+  B_DS_EMPTY,
+  B_ACC_FULL,
+  B_Q_FULL,
+  B_OPS_READY,
+  B_COUNT
+};
+
+struct Waiter {
+  volatile int* abort;
+  int* err;
+  __device__ __forceinline__ bool operator()(uint64_t* bar, uint32_t parity) const {
+    if (*abort) return false;
+    if (mbar_wait_bounded(bar, parity, kWaitLimitNs)) return true;
+    *abort = 1;
+    record_error(err, kErrTimeout);
+    return false;
+  }
 };
 
 template <int D, int Dv, int BK, int MODE>
-__global__ void __launch_bounds__(128, 1)
-    k_rows(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO, Params p) {
-  using C = RowsCfg<D, Dv, BK, MODE>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+__global__ void __launch_bounds__(512, 1)
+    k_rows2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+            const __grid_constant__ CUtensorMap tmV, Params p) {
+  using C = Rows2Cfg<D, Dv, BK, MODE>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQ = sm + C::OFF_Q;
-  uint8_t* sO = sm + C::OFF_O;
   uint8_t* sK = sm + C::OFF_K;
   uint8_t* sV = sm + C::OFF_V;
   uint8_t* sS = sm + C::OFF_S;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 16);
-  int* s_abort = reinterpret_cast<int*>(sm + C::OFF_BAR + 20);
+  uint8_t* sRaw = sm + C::OFF_RAW;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 8 * B_COUNT);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + C::OFF_BAR + 8 * B_COUNT + 4);
+  float* s_merge = reinterpret_cast<float*>(sm + C::OFF_BAR + 512);  // [128][3]
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qt = blockIdx.x, hk = blockIdx.y, split = blockIdx.z;
   const int r0 = qt * 128;
   const int R = p.R, G = p.G;
@@ -400,200 +590,345 @@ __global__ void __launch_bounds__(128, 1)
   if (p.causal) {
     const long i_hi = (long)min(R - 1, r0 + 127) / G;
     const long jmax = (long)p.M - p.N + i_hi;
-    const int ntv = jmax < 0 ? 0 : (int)(jmax / BK) + 1;
-    kt_end = min(kt_end, ntv);
+    kt_end = min(kt_end, jmax < 0 ? 0 : (int)(jmax / BK) + 1);
   }
+  const int ntiles = max(0, kt_end - kt_begin);
+  const int KE = p.ke, EPT = BK / KE, RD = p.raw_depth;
+  const int entry_bytes = KE * (p.rbk_pad + p.rbv_pad);
 
-  if (warp == 0) tmem_alloc(tslot, C::TCOLS);
+  if (warp == 1) tmem_alloc(tslot, C::TCOLS);
   if (tid == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
-    fence_mbar_init();
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&bar[B_RAW_FULL + s], p.raw_bulk ? 1 : 32);
+      mbar_init(&bar[B_RAW_EMPTY + s], 4);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar[B_KV_FULL + s], 4);
+      mbar_init(&bar[B_K_EMPTY + s], 1);
+      mbar_init(&bar[B_V_EMPTY + s], 1);
+    }
+    mbar_init(&bar[B_S_FULL], 1);
+    mbar_init(&bar[B_S_FREE], 8);
+    mbar_init(&bar[B_DS_FULL], 8);
+    mbar_init(&bar[B_DS_EMPTY], 1);
+    mbar_init(&bar[B_ACC_FULL], 1);
+    mbar_init(&bar[B_Q_FULL], 1);
+    mbar_init(&bar[B_OPS_READY], 8);
     *s_abort = 0;
-    prefetch_tmap(&tmQ);
-    prefetch_tmap(&tmO);
+    fence_mbar_init();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-  const uint32_t tS = tbase, tP = tbase + BK, tAcc = tbase + 2 * BK;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-
+  const Waiter wait{s_abort, p.err};
   const Stats st = *p.st;
-  // this thread's row
-  const int r = r0 + tid;
-  const bool rvalid = r < R;
-  const int i = rvalid ? r / G : 0;
-  const int h = hk * G + (rvalid ? r % G : 0);
-  const long jlast = rvalid ? (p.causal ? min((long)p.M - 1, (long)p.M - p.N + i) : (long)p.M - 1) : -1;
-  const uint16_t* mrow = p.mask ? p.mask + ((size_t)(h % p.Hm) * p.N + i) * p.M : nullptr;
-  float lse2 = -CUDART_INF_F, dl = 0.f;
-  if (MODE == 1 && rvalid) {
-    lse2 = p.lse2[(size_t)hk * R + r];
-    dl = p.dlt[(size_t)hk * R + r];
-  }
-  const bool live = MODE == 1 ? (lse2 > -CUDART_INF_F) : rvalid;
-  float m2 = -CUDART_INF_F, l = 0.f, lc = 0.f, sd = 0.f, sdc = 0.f;
 
-  bool have_tiles = kt_begin < kt_end;
-  if (have_tiles && tid == 0) {
-    mbar_arrive_expect_tx(&bars[0], (uint32_t)(C::QB + C::OB));
-#pragma unroll
-    for (int c = 0; c < D / 64; ++c) tma_load_3d(sQ + c * 128 * 128, &tmQ, &bars[0], c * 64, r0, hk);
-#pragma unroll
-    for (int c = 0; c < Dv / 64; ++c) tma_load_3d(sO + c * 128 * 128, &tmO, &bars[0], c * 64, r0, hk);
-  }
-  if (have_tiles) {
-    if (!mbar_wait_bounded(&bars[0], 0, kWaitLimitNs)) {
-      *s_abort = 1;
-      record_error(p.err, kErrTimeout);
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0 && p.raw_bulk) {
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
     }
-  }
-  __syncthreads();
-  if (*s_abort) have_tiles = false;
-
-  constexpr uint32_t ID_S = idesc_f16(128, BK, false, false);
-  constexpr uint32_t ID_DQ = idesc_f16(128, D, false, true);
-  uint32_t mma_phase = 0;
-  bool first = true;
-  const float* vshift = p.rmean + (size_t)hk * Dv;
-
-  for (int kt = kt_begin; have_tiles && kt < kt_end; ++kt) {
-    const int j0 = kt * BK;
-    decode_tile<D, BK, 128>(p.k, p.k_type, p.rbk, hk, p.Hkv, j0, p.M, sK, st.sK, nullptr);
-    decode_tile<Dv, BK, 128>(p.v, p.v_type, p.rbv, hk, p.Hkv, j0, p.M, sV, st.sV, vshift);
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t aq = smem_u32(sQ), ao = smem_u32(sO), bk = smem_u32(sK), bv = smem_u32(sV);
+    if (MODE == 1 && lane == 0 && ntiles > 0) {
+      mbar_arrive_expect_tx(&bar[B_Q_FULL], (uint32_t)C::QB);
 #pragma unroll
-      for (int k = 0; k < D / 16; ++k)
-        mma_f16(tS, sdesc_sw128(aq + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024),
-                sdesc_sw128(bk + (k / 4) * (BK * 128) + (k % 4) * 32, 16, 1024), ID_S, k > 0);
-#pragma unroll
-      for (int k = 0; k < Dv / 16; ++k)
-        mma_f16(tP, sdesc_sw128(ao + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024),
-                sdesc_sw128(bv + (k / 4) * (BK * 128) + (k % 4) * 32, 16, 1024), ID_S, k > 0);
-      mma_commit(&bars[1]);
+      for (int c = 0; c < D / 64; ++c) tma_load_3d(sQ + c * 128 * 128, &tmQ, &bar[B_Q_FULL], c * 64, r0, hk);
     }
-    if (!mbar_wait_bounded(&bars[1], mma_phase, kWaitLimitNs)) {
-      *s_abort = 1;
-      record_error(p.err, kErrTimeout);
-    }
-    mma_phase ^= 1;
-    tc_fence_after();
-
-#pragma unroll 1
-    for (int c32 = 0; c32 < BK / 32; ++c32) {
-      float s[32], dp[32];
-      tmem_ld32(tS + lane_off + c32 * 32, s);
-      tmem_ld32(tP + lane_off + c32 * 32, dp);
-      tmem_ld_wait();
-      const int jb = j0 + c32 * 32;
-      float t2[32];
-#pragma unroll
-      for (int n = 0; n < 32; ++n) {
-        const int j = jb + n;
-        bool ok = (long)j <= jlast;
-        float mv = 0.f;
-        if (ok && mrow) {
-          mv = h2f(__ldg(reinterpret_cast<const unsigned short*>(mrow) + j));
-          ok = !(mv == -CUDART_INF_F);
+    for (int t = 0; t < ntiles; ++t) {
+      const int j0 = (kt_begin + t) * BK;
+      for (int h = 0; h < EPT; ++h) {
+        const int e = t * EPT + h, slot = e % RD, use = e / RD;
+        if (!wait(&bar[B_RAW_EMPTY + slot], (use & 1) ^ 1)) break;
+        const int ja = j0 + h * KE;
+        const int nv = max(0, min(KE, p.M - ja));
+        uint8_t* dk = sRaw + slot * entry_bytes;
+        uint8_t* dv = dk + KE * p.rbk_pad;
+        if (p.raw_bulk) {
+          // one TMA box per tensor: KE rows of this KV head (dims: row bytes, head, key)
+          if (lane == 0) {
+            if (nv > 0) {
+              mbar_arrive_expect_tx(&bar[B_RAW_FULL + slot], (uint32_t)(KE * (p.rbk + p.rbv)));
+              tma_load_3d(dk, &tmK, &bar[B_RAW_FULL + slot], 0, hk, ja);
+              tma_load_3d(dv, &tmV, &bar[B_RAW_FULL + slot], 0, hk, ja);
+            } else {
+              mbar_arrive(&bar[B_RAW_FULL + slot]);
+            }
+          }
+        } else {
+          const int wk = p.rbk / 4, wv = p.rbv / 4;
+          for (int x = lane; x < nv * wk; x += 32) {
+            const int rr = x / wk, c = x % wk;
+            cp_async4(dk + rr * p.rbk_pad + 4 * c, p.k + ((size_t)(ja + rr) * p.Hkv + hk) * p.rbk + 4 * c);
+          }
+          for (int x = lane; x < nv * wv; x += 32) {
+            const int rr = x / wv, c = x % wv;
+            cp_async4(dv + rr * p.rbv_pad + 4 * c, p.v + ((size_t)(ja + rr) * p.Hkv + hk) * p.rbv + 4 * c);
+          }
+          cp_async_arrive(&bar[B_RAW_FULL + slot]);
         }
-        t2[n] = ok ? fmaf(s[n], st.c2, mv * kLog2e) : -CUDART_INF_F;
       }
-      if (MODE == 0) {
-        float cmax = -CUDART_INF_F;
+      if (*s_abort) break;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t ID_S = idesc_f16(128, BK, false, false);
+      constexpr uint32_t ID_DQ = idesc_f16(128, D, false, true);
+      const uint32_t tS = tbase + C::T_S, tP = tbase + C::T_P, tQ = tbase + C::T_Q, tO = tbase + C::T_O,
+                     tAcc = tbase + C::T_ACC;
+      bool ok = (MODE == 0 || wait(&bar[B_Q_FULL], 0)) && wait(&bar[B_OPS_READY], 0);
+      for (int t = 0; ok && t < ntiles; ++t) {
+        const int ks = t & 1, vs = MODE ? 0 : (t & 1);
+        if (!wait(&bar[B_KV_FULL + ks], (t >> 1) & 1) || !wait(&bar[B_S_FREE], (t & 1) ^ 1)) break;
+        tc_fence_after();
+        const uint32_t bk = smem_u32(sK + ks * C::KB), bv = smem_u32(sV + vs * C::VB);
 #pragma unroll
-        for (int n = 0; n < 32; ++n) cmax = fmaxf(cmax, t2[n]);
-        if (cmax > m2) {
-          const float f = exp2f(m2 - cmax);  // 0 when m2 = -inf
-          l *= f, lc *= f, sd *= f, sdc *= f;
-          m2 = cmax;
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t bd = sdesc_sw128(bk + (k / 4) * (BK * 128) + (k % 4) * 32, 16, 1024);
+          if (MODE == 1)
+            mma_f16(tS, sdesc_sw128(smem_u32(sQ) + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024), bd, ID_S, k > 0);
+          else
+            mma_f16_tmem_a(tS, tQ + k * 8, bd, ID_S, k > 0);
         }
-        if (cmax > -CUDART_INF_F) {
-          float cl = 0.f, cs = 0.f;
+#pragma unroll
+        for (int k = 0; k < Dv / 16; ++k)
+          mma_f16_tmem_a(tP, tO + k * 8, sdesc_sw128(bv + (k / 4) * (BK * 128) + (k % 4) * 32, 16, 1024), ID_S,
+                         k > 0);
+        mma_commit(&bar[B_S_FULL]);
+        mma_commit(&bar[B_V_EMPTY + vs]);
+        if (MODE == 0) mma_commit(&bar[B_K_EMPTY + ks]);
+        if (MODE == 1 && t >= 1) {
+          // dQ += dS(t-1) K'(t-1)
+          if (!wait(&bar[B_DS_FULL], (t - 1) & 1)) break;
+          tc_fence_after();
+          const uint32_t kp = smem_u32(sK + ((t - 1) & 1) * C::KB);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_f16(tAcc, sdesc_sw128(smem_u32(sS) + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024),
+                    sdesc_sw128(kp + k * 2048, BK * 128, 1024), ID_DQ, (t - 1 > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&bar[B_DS_EMPTY]);
+          mma_commit(&bar[B_K_EMPTY + ((t - 1) & 1)]);
+        }
+      }
+      if (MODE == 1 && !*s_abort) {
+        const int t = ntiles;
+        if (wait(&bar[B_DS_FULL], (t - 1) & 1)) {
+          tc_fence_after();
+          const uint32_t kp = smem_u32(sK + ((t - 1) & 1) * C::KB);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_f16(tAcc, sdesc_sw128(smem_u32(sS) + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024),
+                    sdesc_sw128(kp + k * 2048, BK * 128, 1024), ID_DQ, (t - 1 > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&bar[B_ACC_FULL]);
+        }
+      }
+    }
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------------ decoders
+    const int dt = tid - 12 * 32;
+    __half2 vsh[16];
+    load_group_shift<Dv, 128>(p.rsh + (size_t)hk * Dv, p.v_type, dt, vsh);
+    for (int t = 0; t < ntiles; ++t) {
+      const int ks = t & 1, vs = MODE ? 0 : (t & 1);
+      if (!wait(&bar[B_K_EMPTY + ks], ((t >> 1) & 1) ^ 1)) break;
+      if (!wait(&bar[B_V_EMPTY + vs], MODE ? ((t & 1) ^ 1) : (((t >> 1) & 1) ^ 1))) break;
+      const uint32_t kd = smem_u32(sK + ks * C::KB), vd = smem_u32(sV + vs * C::VB);
+      const int j0 = (kt_begin + t) * BK;
+      bool ok = true;
+      for (int h = 0; h < EPT; ++h) {
+        const int e = t * EPT + h, slot = e % RD, use = e / RD;
+        if (!wait(&bar[B_RAW_FULL + slot], use & 1)) {
+          ok = false;
+          break;
+        }
+        const uint32_t rk = smem_u32(sRaw) + slot * entry_bytes;
+        const uint32_t rv = rk + KE * p.rbk_pad;
+        const int nv = max(0, min(KE, p.M - (j0 + h * KE)));
+        decode_rows<D, BK, 128, false>(p.k_type, rk, p.rbk_pad, KE, nv, h * KE, kd, st.sK, vsh, dt);
+        decode_rows<Dv, BK, 128, true>(p.v_type, rv, p.rbv_pad, KE, nv, h * KE, vd, st.sV, vsh, dt);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[B_RAW_EMPTY + slot]);
+      }
+      if (!ok) break;
+      if (lane == 0) mbar_arrive(&bar[B_KV_FULL + ks]);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------------ softmax
+    const int q4 = warp & 3, ch = (warp - 4) >> 2;
+    const int row = q4 * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const int r = r0 + row;
+    const bool rvalid = r < R;
+    const int i = rvalid ? r / G : 0;
+    const int h = hk * G + (rvalid ? r % G : 0);
+    const long jlast = rvalid ? (p.causal ? min((long)p.M - 1, (long)p.M - p.N + i) : (long)p.M - 1) : -1;
+    const uint16_t* mrow = p.mask ? p.mask + ((size_t)(h % p.Hm) * p.N + i) * p.M : nullptr;
+    float lse2 = -CUDART_INF_F, dl = 0.f;
+    if (MODE == 1 && rvalid) {
+      lse2 = p.lse2[(size_t)hk * R + r];
+      dl = p.dlt[(size_t)hk * R + r];
+    }
+    const bool live = MODE == 1 ? (lse2 > -CUDART_INF_F) : rvalid;
+    const float nlse2 = live ? -lse2 : -CUDART_INF_F;  // exp2(t2 + nlse2) = p, and 0 on a dead row
+    const uint32_t sS_u = smem_u32(sS);
+    float m2 = -CUDART_INF_F, l = 0.f, lc = 0.f, sd = 0.f, sdc = 0.f;
+
+    if (ntiles > 0) {
+      // this thread's half of the row's A operands into tensor memory (binary16 pairs per column)
+      auto put_row = [&](const __half* src, int DD, uint32_t tcol) {
+        // DD/2 32-bit words per row; with 64 or more words the two halves split them, with 32
+        // the first half writes all of them (tensor-memory stores move 32 columns at a time)
+        const int wpr = DD / 2;
+        const int w0 = wpr >= 64 ? ch * (wpr / 2) : 0, nw = wpr >= 64 ? wpr / 2 : (ch == 0 ? wpr : 0);
+        const uint4* s4 = reinterpret_cast<const uint4*>(src) + w0 / 4;
+        for (int c = 0; c < nw; c += 32) {
+          uint32_t wv[32];
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            const uint4 u = rvalid ? __ldg(s4 + c / 4 + x) : make_uint4(0, 0, 0, 0);
+            wv[4 * x] = u.x, wv[4 * x + 1] = u.y, wv[4 * x + 2] = u.z, wv[4 * x + 3] = u.w;
+          }
+          tmem_st32(tbase + lane_off + tcol + w0 + c, wv);
+        }
+      };
+      const size_t rowq = (size_t)hk * R + (rvalid ? r : 0);
+      if (MODE == 0) put_row(p.q16 + rowq * D, D, C::T_Q);
+      put_row(p.do16 + rowq * Dv, Dv, C::T_O);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[B_OPS_READY]);
+    }
+
+    for (int t = 0; t < ntiles; ++t) {
+      const int j0 = (kt_begin + t) * BK;
+      if (!wait(&bar[B_S_FULL], t & 1)) break;
+      tc_fence_after();
+      bool stored_wait = false;
+#pragma unroll 1
+      for (int c = 0; c < C::HALF; c += 32) {
+        const int col0 = ch * C::HALF + c;
+        float s[32], dp[32];
+        tmem_ld32(tbase + C::T_S + lane_off + col0, s);
+        tmem_ld32(tbase + C::T_P + lane_off + col0, dp);
+        tmem_ld_wait();
+        if (c + 32 >= C::HALF) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar[B_S_FREE]);
+        }
+        // fully visible chunk without a mask: no per-key tests
+        const bool full = mrow == nullptr && (long)(j0 + col0 + 31) <= jlast;
+        float t2[32];
+        if (full) {
+#pragma unroll
+          for (int n = 0; n < 32; ++n) t2[n] = s[n] * st.c2;
+        } else {
 #pragma unroll
           for (int n = 0; n < 32; ++n) {
-            const float e = exp2f(t2[n] - m2);  // 0 for masked keys
-            cl += e;
-            cs = fmaf(e, dp[n], cs);
+            const int j = j0 + col0 + n;
+            bool ok = (long)j <= jlast;
+            float mv = 0.f;
+            if (ok && mrow) {
+              mv = h2f(__ldg(reinterpret_cast<const unsigned short*>(mrow) + j));
+              ok = !(mv == -CUDART_INF_F);
+            }
+            t2[n] = ok ? fmaf(s[n], st.c2, mv * kLog2e) : -CUDART_INF_F;
           }
-          // compensated accumulation of the chunk sums
-          float y = cl - lc, t = l + y;
-          lc = (t - l) - y, l = t;
-          y = cs - sdc, t = sd + y;
-          sdc = (t - sd) - y, sd = t;
         }
-      } else {
-        float ds[32];
+        if (MODE == 0) {
+          float cmax = -CUDART_INF_F;
 #pragma unroll
-        for (int n = 0; n < 32; ++n) {
-          const float pr = (live && t2[n] > -CUDART_INF_F) ? exp2f(t2[n] - lse2) : 0.f;
-          ds[n] = pr * (dp[n] - dl);
+          for (int n = 0; n < 32; ++n) cmax = fmaxf(cmax, t2[n]);
+          if (cmax > m2) {
+            const float f = exp2f(m2 - cmax);
+            l *= f, lc *= f, sd *= f, sdc *= f;
+            m2 = cmax;
+          }
+          if (cmax > -CUDART_INF_F) {
+            float cl = 0.f, cs = 0.f;
+#pragma unroll
+            for (int n = 0; n < 32; ++n) {
+              const float e = exp2f(t2[n] - m2);
+              cl += e;
+              cs = fmaf(e, dp[n], cs);
+            }
+            float y = cl - lc, tt = l + y;
+            lc = (tt - l) - y, l = tt;
+            y = cs - sdc, tt = sd + y;
+            sdc = (tt - sd) - y, sd = tt;
+          }
+        } else {
+          uint32_t pk[16];
+#pragma unroll
+          for (int n = 0; n < 32; n += 2) {
+            const float p0 = exp2f(t2[n] + nlse2), p1 = exp2f(t2[n + 1] + nlse2);  // 0 for masked keys, dead rows
+            pk[n / 2] = h2_as_u32(__floats2half2_rn(p0 * (dp[n] - dl) * st.lam, p1 * (dp[n + 1] - dl) * st.lam));
+          }
+          if (!stored_wait) {
+            if (!wait(&bar[B_DS_EMPTY], (t & 1) ^ 1)) break;
+            stored_wait = true;
+          }
+#pragma unroll
+          for (int x = 0; x < 4; ++x)
+            sts_v4(sS_u + panel_off_u(128, row, col0 + 8 * x), pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
         }
-        store_row32<BK>(sS, tid, c32 * 32, ds, st.lam);
+      }
+      if (*s_abort) break;
+      if (MODE == 1) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[B_DS_FULL]);
       }
     }
-    tc_fence_before();
-    if (MODE == 1) {
-      fence_proxy_async_smem();
-      __syncthreads();
-      if (tid == 0) {
-        tc_fence_after();
-        const uint32_t as = smem_u32(sS), bk = smem_u32(sK);
+
+    // epilogue
+    if (MODE == 0) {
+      if (ch == 1) s_merge[row * 3 + 0] = m2, s_merge[row * 3 + 1] = l, s_merge[row * 3 + 2] = sd;
+      named_bar_sync(1, 256);
+      if (ch == 0 && rvalid) {
+        const float m2b = s_merge[row * 3 + 0], lb = s_merge[row * 3 + 1], sdb = s_merge[row * 3 + 2];
+        const float mm = fmaxf(m2, m2b);
+        float L = 0.f, SD = 0.f;
+        if (mm > -CUDART_INF_F) {
+          const float fa = exp2f(m2 - mm), fb = exp2f(m2b - mm);
+          L = l * fa + lb * fb;
+          SD = sd * fa + sdb * fb;
+        }
+        float* o = p.part + (((size_t)split * p.Hkv + hk) * R + r) * 3;
+        o[0] = mm, o[1] = L, o[2] = SD;
+      }
+    } else {
+      float* out = !rvalid ? nullptr
+                   : p.nsplit == 1 ? p.dQ + ((size_t)i * p.H + h) * D
+                                   : p.dqpart + (((size_t)split * p.Hkv + hk) * R + r) * D;
+      const bool have = ntiles > 0 && wait(&bar[B_ACC_FULL], 0);
+      if (have) tc_fence_after();
+#pragma unroll 1
+      for (int c = ch * (D / 2); c < (ch + 1) * (D / 2); c += 32) {
+        float v[32];
+        if (have) {
+          tmem_ld32(tbase + C::T_ACC + lane_off + c, v);
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k)
-          mma_f16(tAcc, sdesc_sw128(as + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024),
-                  sdesc_sw128(bk + k * 2048, BK * 128, 1024), ID_DQ, (first && k == 0) ? 0u : 1u);
-        mma_commit(&bars[1]);
+          for (int e = 0; e < 32; ++e) v[e] = 0.f;
+        }
+        if (out) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(out + c + e) =
+                make_float4(v[e] * st.dq_fac, v[e + 1] * st.dq_fac, v[e + 2] * st.dq_fac, v[e + 3] * st.dq_fac);
+        }
       }
-      if (!mbar_wait_bounded(&bars[1], mma_phase, kWaitLimitNs)) {
-        *s_abort = 1;
-        record_error(p.err, kErrTimeout);
-      }
-      mma_phase ^= 1;
-      tc_fence_after();
-      first = false;
     }
-    __syncthreads();
-    if (*s_abort) break;
   }
 
-  // epilogue
-  if (MODE == 0) {
-    if (rvalid) {
-      float* o = p.part + (((size_t)split * p.Hkv + hk) * R + r) * 3;
-      o[0] = m2, o[1] = l, o[2] = sd;
-    }
-  } else {
-    // every lane takes part in the warp-wide TMEM loads; only valid rows store
-    float* out = !rvalid ? nullptr
-                 : p.nsplit == 1 ? p.dQ + ((size_t)i * p.H + h) * D
-                                 : p.dqpart + (((size_t)split * p.Hkv + hk) * R + r) * D;
-#pragma unroll 1
-    for (int c = 0; c < D; c += 32) {
-      float v[32];
-      if (!first) {
-        tmem_ld32(tAcc + lane_off + c, v);
-        tmem_ld_wait();
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = 0.f;
-      }
-      if (out) {
-#pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(out + c + e) =
-              make_float4(v[e] * st.dq_fac, v[e + 1] * st.dq_fac, v[e + 2] * st.dq_fac, v[e + 3] * st.dq_fac);
-      }
-    }
-  }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, C::TCOLS);
   }
@@ -652,228 +987,291 @@ __global__ void __launch_bounds__(256) k_dq_reduce(Params p) {
 
 // ------------------------------------------------------------------------------------------------
 // key-tile pass: dK and dV
+//
+// A CTA owns BK keys of one KV head: their K' and V' tiles are decoded once into shared memory,
+// then the CTA walks the 128-row query tiles that can see them.  Per query tile:
+//   S = Q K'^T, dP = dO V'^T              (M = 128 rows, N = BK keys)
+//   P, dS = P * (dP - delta)              (softmax warps, written as binary16 [row][key])
+//   dK^T += Q^T dS, dV^T += dO^T P        (M = 128 feature rows per half, N = BK keys, K = 128 rows)
+// Q and dO arrive as 64-column TMA panels with one full/empty barrier pair each; a panel is
+// released when the last product reading it completes, so the next tile's loads overlap this
+// tile's final products without a second buffer.
+// Warp roles (16 warps): 0 producer, 1 MMA issuer / tensor-memory owner, 4-11 softmax and
+// epilogue, every warp decodes K' and V' at the start.
 
 template <int D, int Dv, int BK>
-struct ColsCfg {
+struct Cols2Cfg {
+  static constexpr int NQP = D / 64, NOP = Dv / 64;  // panels of Q and dO
   static constexpr int KB = BK * D * 2, VB = BK * Dv * 2, QB = 128 * D * 2, OB = 128 * Dv * 2, PB = 128 * BK * 2;
   static constexpr int OFF_K = 0, OFF_V = KB, OFF_Q = KB + VB, OFF_O = OFF_Q + QB, OFF_P = OFF_O + OB,
                        OFF_S = OFF_P + PB, OFF_BAR = OFF_S + PB;
-  static constexpr int SMEM = OFF_BAR + 64 + 1024;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;
   static constexpr int NDH = D >= 128 ? D / 128 : 1, NVH = Dv >= 128 ? Dv / 128 : 1;
+  static constexpr int T_S = 0, T_P = BK, T_V = 2 * BK, T_K = 2 * BK + NVH * BK;
   static constexpr int TCOLS = pow2_at_least(2 * BK + (NDH + NVH) * BK);
+  static constexpr int HALF = BK / 2;
+};
+
+enum {
+  C_Q_FULL = 0,   // [4]
+  C_Q_EMPTY = 4,  // [4]
+  C_O_FULL = 8,   // [4]
+  C_O_EMPTY = 12, // [4]
+  C_S_FULL = 16,
+  C_DS_FULL,
+  C_DS_EMPTY,
+  C_DONE,
+  C_COUNT
 };
 
 template <int D, int Dv, int BK>
-__global__ void __launch_bounds__(128, 1)
-    k_cols(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO, Params p) {
-  using C = ColsCfg<D, Dv, BK>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+__global__ void __launch_bounds__(512, 1)
+    k_cols2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO, Params p) {
+  using C = Cols2Cfg<D, Dv, BK>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sK = sm + C::OFF_K;
   uint8_t* sV = sm + C::OFF_V;
   uint8_t* sQ = sm + C::OFF_Q;
   uint8_t* sO = sm + C::OFF_O;
   uint8_t* sP = sm + C::OFF_P;
   uint8_t* sS = sm + C::OFF_S;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 16);
-  int* s_abort = reinterpret_cast<int*>(sm + C::OFF_BAR + 20);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 8 * C_COUNT);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + C::OFF_BAR + 8 * C_COUNT + 4);
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kt = blockIdx.x, hk = blockIdx.y;
   const int j0 = kt * BK;
   const int R = p.R, G = p.G;
-
-  // first row tile that can see key j0 under the causal tail
   int qt_begin = 0;
   if (p.causal) {
-    const long imin = (long)j0 - ((long)p.M - p.N);
+    const long imin = (long)j0 - ((long)p.M - p.N);  // first query that sees key j0
     if (imin > 0) qt_begin = (int)min((long)p.nQT, (imin * G) / 128);
   }
-  bool have = qt_begin < p.nQT && R > 0;
+  const int nq = R > 0 ? max(0, p.nQT - qt_begin) : 0;
 
-  if (warp == 0) tmem_alloc(tslot, C::TCOLS);
+  if (warp == 1) tmem_alloc(tslot, C::TCOLS);
   if (tid == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
-    fence_mbar_init();
+    for (int c = 0; c < 4; ++c) {
+      mbar_init(&bar[C_Q_FULL + c], 1);
+      mbar_init(&bar[C_Q_EMPTY + c], 1);
+      mbar_init(&bar[C_O_FULL + c], 1);
+      mbar_init(&bar[C_O_EMPTY + c], 1);
+    }
+    mbar_init(&bar[C_S_FULL], 1);
+    mbar_init(&bar[C_DS_FULL], 8);
+    mbar_init(&bar[C_DS_EMPTY], 1);
+    mbar_init(&bar[C_DONE], 1);
     *s_abort = 0;
-    prefetch_tmap(&tmQ);
-    prefetch_tmap(&tmO);
+    fence_mbar_init();
+  }
+  const Stats st = *p.st;
+  if (nq > 0) {  // K' and V' once, by every thread
+    decode_tile<D, BK, 512>(p.k, p.k_type, p.rbk, hk, p.Hkv, j0, p.M, sK, st.sK, nullptr, tid);
+    decode_tile<Dv, BK, 512>(p.v, p.v_type, p.rbv, hk, p.Hkv, j0, p.M, sV, st.sV, p.rsh + (size_t)hk * Dv, tid);
+    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-  const uint32_t tS = tbase, tP = tbase + BK, tV = tbase + 2 * BK, tK = tbase + 2 * BK + C::NVH * BK;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-  const Stats st = *p.st;
+  const Waiter wait{s_abort, p.err};
 
-  if (have) {
-    decode_tile<D, BK, 128>(p.k, p.k_type, p.rbk, hk, p.Hkv, j0, p.M, sK, st.sK, nullptr);
-    decode_tile<Dv, BK, 128>(p.v, p.v_type, p.rbv, hk, p.Hkv, j0, p.M, sV, st.sV, p.rmean + (size_t)hk * Dv);
-    fence_proxy_async_smem();
-  }
-  __syncthreads();
-
-  constexpr uint32_t ID_S = idesc_f16(128, BK, false, false);
-  constexpr uint32_t ID_T = idesc_f16(128, BK, true, true);
-  constexpr uint32_t LBO_O = Dv >= 128 ? 128 * 128 : 0;  // second 64-row block of dO^T (duplicate if Dv = 64)
-  constexpr uint32_t LBO_Q = D >= 128 ? 128 * 128 : 0;
-  uint32_t tma_phase = 0, mma_phase = 0;
-  bool first = true;
-
-  for (int qt = qt_begin; have && qt < p.nQT; ++qt) {
-    const int r0 = qt * 128;
-    if (tid == 0) {
-      mbar_arrive_expect_tx(&bars[0], (uint32_t)(C::QB + C::OB));
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) tma_load_3d(sQ + c * 128 * 128, &tmQ, &bars[0], c * 64, r0, hk);
-#pragma unroll
-      for (int c = 0; c < Dv / 64; ++c) tma_load_3d(sO + c * 128 * 128, &tmO, &bars[0], c * 64, r0, hk);
-    }
-    const int r = r0 + tid;
-    const bool rvalid = r < R;
-    const int i = rvalid ? r / G : 0;
-    const int h = hk * G + (rvalid ? r % G : 0);
-    const float lse2 = rvalid ? p.lse2[(size_t)hk * R + r] : -CUDART_INF_F;
-    const float dl = rvalid ? p.dlt[(size_t)hk * R + r] : 0.f;
-    const bool live = lse2 > -CUDART_INF_F;
-    const long jlast = rvalid ? (p.causal ? min((long)p.M - 1, (long)p.M - p.N + i) : (long)p.M - 1) : -1;
-    const uint16_t* mrow = p.mask ? p.mask + ((size_t)(h % p.Hm) * p.N + i) * p.M : nullptr;
-
-    if (!mbar_wait_bounded(&bars[0], tma_phase, kWaitLimitNs)) {
-      *s_abort = 1;
-      record_error(p.err, kErrTimeout);
-    }
-    tma_phase ^= 1;
-    __syncthreads();
-    if (*s_abort) break;
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t aq = smem_u32(sQ), ao = smem_u32(sO), bk = smem_u32(sK), bv = smem_u32(sV);
-#pragma unroll
-      for (int k = 0; k < D / 16; ++k)
-        mma_f16(tS, sdesc_sw128(aq + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024),
-                sdesc_sw128(bk + (k / 4) * (BK * 128) + (k % 4) * 32, 16, 1024), ID_S, k > 0);
-#pragma unroll
-      for (int k = 0; k < Dv / 16; ++k)
-        mma_f16(tP, sdesc_sw128(ao + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024),
-                sdesc_sw128(bv + (k / 4) * (BK * 128) + (k % 4) * 32, 16, 1024), ID_S, k > 0);
-      mma_commit(&bars[1]);
-    }
-    if (!mbar_wait_bounded(&bars[1], mma_phase, kWaitLimitNs)) {
-      *s_abort = 1;
-      record_error(p.err, kErrTimeout);
-    }
-    mma_phase ^= 1;
-    tc_fence_after();
-
-#pragma unroll 1
-    for (int c32 = 0; c32 < BK / 32; ++c32) {
-      float s[32], dp[32];
-      tmem_ld32(tS + lane_off + c32 * 32, s);
-      tmem_ld32(tP + lane_off + c32 * 32, dp);
-      tmem_ld_wait();
-      const int jb = j0 + c32 * 32;
-#pragma unroll
-      for (int n = 0; n < 32; ++n) {
-        const int j = jb + n;
-        bool ok = live && (long)j <= jlast;
-        float mv = 0.f;
-        if (ok && mrow) {
-          mv = h2f(__ldg(reinterpret_cast<const unsigned short*>(mrow) + j));
-          ok = !(mv == -CUDART_INF_F);
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmO);
+      for (int t = 0; t < nq; ++t) {
+        const int r0 = (qt_begin + t) * 128;
+        bool ok = true;
+        for (int c = 0; ok && c < C::NQP; ++c) {
+          if (!(ok = wait(&bar[C_Q_EMPTY + c], (t & 1) ^ 1))) break;
+          mbar_arrive_expect_tx(&bar[C_Q_FULL + c], 128 * 128);
+          tma_load_3d(sQ + c * 128 * 128, &tmQ, &bar[C_Q_FULL + c], c * 64, r0, hk);
         }
-        const float pr = ok ? exp2f(fmaf(s[n], st.c2, mv * kLog2e) - lse2) : 0.f;
-        s[n] = pr;
-        dp[n] = pr * (dp[n] - dl);
+        for (int c = 0; ok && c < C::NOP; ++c) {
+          if (!(ok = wait(&bar[C_O_EMPTY + c], (t & 1) ^ 1))) break;
+          mbar_arrive_expect_tx(&bar[C_O_FULL + c], 128 * 128);
+          tma_load_3d(sO + c * 128 * 128, &tmO, &bar[C_O_FULL + c], c * 64, r0, hk);
+        }
+        if (!ok) break;
       }
-      store_row32<BK>(sP, tid, c32 * 32, s, st.sP);
-      store_row32<BK>(sS, tid, c32 * 32, dp, st.lam);
     }
-    tc_fence_before();
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nq > 0) {
+      constexpr uint32_t ID_S = idesc_f16(128, BK, false, false);
+      constexpr uint32_t ID_T = idesc_f16(128, BK, true, true);
+      constexpr uint32_t LBO_O = Dv >= 128 ? 128 * 128 : 0;  // second 64-row block of dO^T (repeat if Dv = 64)
+      constexpr uint32_t LBO_Q = D >= 128 ? 128 * 128 : 0;
+      const uint32_t tS = tbase + C::T_S, tP = tbase + C::T_P, tV = tbase + C::T_V, tK = tbase + C::T_K;
+      const uint32_t aq = smem_u32(sQ), ao = smem_u32(sO), bk = smem_u32(sK), bv = smem_u32(sV),
+                     bp = smem_u32(sP), bs = smem_u32(sS);
+      for (int t = 0; t < nq; ++t) {
+        bool ok = true;
+        for (int c = 0; ok && c < C::NQP; ++c) {
+          if (!(ok = wait(&bar[C_Q_FULL + c], t & 1))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f16(tS, sdesc_sw128(aq + c * (128 * 128) + k * 32, 16, 1024),
+                    sdesc_sw128(bk + c * (BK * 128) + k * 32, 16, 1024), ID_S, (c > 0 || k > 0) ? 1u : 0u);
+        }
+        for (int c = 0; ok && c < C::NOP; ++c) {
+          if (!(ok = wait(&bar[C_O_FULL + c], t & 1))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f16(tP, sdesc_sw128(ao + c * (128 * 128) + k * 32, 16, 1024),
+                    sdesc_sw128(bv + c * (BK * 128) + k * 32, 16, 1024), ID_S, (c > 0 || k > 0) ? 1u : 0u);
+        }
+        if (!ok) break;
+        mma_commit(&bar[C_S_FULL]);
+        if (!wait(&bar[C_DS_FULL], t & 1)) break;
+        tc_fence_after();
+        const uint32_t acc0 = t > 0 ? 1u : 0u;
+#pragma unroll
+        for (int hh = 0; hh < C::NDH; ++hh) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_f16(tK + hh * BK, sdesc_sw128(aq + hh * 2 * (128 * 128) + k * 2048, LBO_Q, 1024),
+                    sdesc_sw128(bs + k * 2048, 128 * 128, 1024), ID_T, (acc0 || k > 0) ? 1u : 0u);
+          mma_commit(&bar[C_Q_EMPTY + 2 * hh]);
+          if (2 * hh + 1 < C::NQP) mma_commit(&bar[C_Q_EMPTY + 2 * hh + 1]);
+        }
+#pragma unroll
+        for (int hh = 0; hh < C::NVH; ++hh) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_f16(tV + hh * BK, sdesc_sw128(ao + hh * 2 * (128 * 128) + k * 2048, LBO_O, 1024),
+                    sdesc_sw128(bp + k * 2048, 128 * 128, 1024), ID_T, (acc0 || k > 0) ? 1u : 0u);
+          mma_commit(&bar[C_O_EMPTY + 2 * hh]);
+          if (2 * hh + 1 < C::NOP) mma_commit(&bar[C_O_EMPTY + 2 * hh + 1]);
+        }
+        mma_commit(&bar[C_DS_EMPTY]);
+      }
+      mma_commit(&bar[C_DONE]);
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------------------------ softmax, then epilogue
+    const int q4 = warp & 3, ch = (warp - 4) >> 2;
+    const int row = q4 * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    auto row_stats = [&](int t, float& lse2, float& dl, long& jlast, const uint16_t*& mrow) {
+      const int r = (qt_begin + t) * 128 + row;
+      const bool rvalid = r < R;
+      const int i = rvalid ? r / G : 0;
+      const int h = hk * G + (rvalid ? r % G : 0);
+      lse2 = rvalid ? p.lse2[(size_t)hk * R + r] : -CUDART_INF_F;
+      dl = rvalid ? p.dlt[(size_t)hk * R + r] : 0.f;
+      jlast = rvalid ? (p.causal ? min((long)p.M - 1, (long)p.M - p.N + i) : (long)p.M - 1) : -1;
+      mrow = p.mask ? p.mask + ((size_t)(h % p.Hm) * p.N + i) * p.M : nullptr;
+    };
+    float lse2 = 0.f, dl = 0.f;
+    long jlast = -1;
+    const uint16_t* mrow = nullptr;
+    const uint32_t sP_u = smem_u32(sP), sS_u = smem_u32(sS);
+    if (nq > 0) row_stats(0, lse2, dl, jlast, mrow);
+    for (int t = 0; t < nq; ++t) {
+      float nlse2 = 0.f, ndl = 0.f;  // next tile's row values, fetched ahead
+      long njlast = -1;
+      const uint16_t* nmrow = nullptr;
+      if (t + 1 < nq) row_stats(t + 1, nlse2, ndl, njlast, nmrow);
+      const bool live = lse2 > -CUDART_INF_F;
+      if (!wait(&bar[C_S_FULL], t & 1)) break;
       tc_fence_after();
-      const uint32_t ao = smem_u32(sO), aq = smem_u32(sQ), bp = smem_u32(sP), bs = smem_u32(sS);
-#pragma unroll
-      for (int hh = 0; hh < C::NVH; ++hh)
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_f16(tV + hh * BK, sdesc_sw128(ao + hh * 2 * (128 * 128) + k * 2048, LBO_O, 1024),
-                  sdesc_sw128(bp + k * 2048, 128 * 128, 1024), ID_T, (first && k == 0) ? 0u : 1u);
-#pragma unroll
-      for (int hh = 0; hh < C::NDH; ++hh)
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_f16(tK + hh * BK, sdesc_sw128(aq + hh * 2 * (128 * 128) + k * 2048, LBO_Q, 1024),
-                  sdesc_sw128(bs + k * 2048, 128 * 128, 1024), ID_T, (first && k == 0) ? 0u : 1u);
-      mma_commit(&bars[1]);
-    }
-    if (!mbar_wait_bounded(&bars[1], mma_phase, kWaitLimitNs)) {
-      *s_abort = 1;
-      record_error(p.err, kErrTimeout);
-    }
-    mma_phase ^= 1;
-    tc_fence_after();
-    first = false;
-    __syncthreads();
-    if (*s_abort) break;
-  }
-
-  // epilogue: lane = feature row (dv or d), columns = keys
-  {
-    const int lrow = warp * 32 + (tid & 31);
+      bool waited = false;
 #pragma unroll 1
-    for (int hh = 0; hh < C::NVH; ++hh) {
-      const int dv = hh * 128 + lrow;
+      for (int c = 0; c < C::HALF; c += 32) {
+        const int col0 = ch * C::HALF + c;
+        float s[32], dp[32];
+        tmem_ld32(tbase + C::T_S + lane_off + col0, s);
+        tmem_ld32(tbase + C::T_P + lane_off + col0, dp);
+        tmem_ld_wait();
+        uint32_t pp[16], pd[16];
+        const bool full = mrow == nullptr && (long)(j0 + col0 + 31) <= jlast;
+        const float nl = live ? -lse2 : -CUDART_INF_F;
+#pragma unroll
+        for (int n = 0; n < 32; n += 2) {
+          float pr[2], ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float t2;
+            if (full) {
+              t2 = fmaf(s[n + e], st.c2, nl);
+            } else {
+              const int j = j0 + col0 + n + e;
+              bool ok = (long)j <= jlast;
+              float mv = 0.f;
+              if (ok && mrow) {
+                mv = h2f(__ldg(reinterpret_cast<const unsigned short*>(mrow) + j));
+                ok = !(mv == -CUDART_INF_F);
+              }
+              t2 = ok ? fmaf(s[n + e], st.c2, mv * kLog2e) + nl : -CUDART_INF_F;
+            }
+            pr[e] = exp2f(t2);
+            ds[e] = pr[e] * (dp[n + e] - dl);
+          }
+          pp[n / 2] = h2_as_u32(__floats2half2_rn(pr[0] * st.sP, pr[1] * st.sP));
+          pd[n / 2] = h2_as_u32(__floats2half2_rn(ds[0] * st.lam, ds[1] * st.lam));
+        }
+        if (!waited) {
+          if (!wait(&bar[C_DS_EMPTY], (t & 1) ^ 1)) break;
+          waited = true;
+        }
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const uint32_t off = panel_off_u(128, row, col0 + 8 * x);
+          sts_v4(sP_u + off, pp[4 * x], pp[4 * x + 1], pp[4 * x + 2], pp[4 * x + 3]);
+          sts_v4(sS_u + off, pd[4 * x], pd[4 * x + 1], pd[4 * x + 2], pd[4 * x + 3]);
+        }
+      }
+      if (*s_abort) break;
+      tc_fence_before();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[C_DS_FULL]);
+      lse2 = nlse2, dl = ndl, jlast = njlast, mrow = nmrow;
+    }
+    // epilogue: lane = feature row of a half, columns = keys; this warp takes half the keys
+    const bool have = nq > 0 && wait(&bar[C_DONE], 0);
+    if (have) tc_fence_after();
+    const int lrow = q4 * 32 + lane;
 #pragma unroll 1
-      for (int c = 0; c < BK; c += 32) {
+    for (int hh = 0; hh < C::NVH + C::NDH; ++hh) {
+      const bool isv = hh < C::NVH;
+      const int half = isv ? hh : hh - C::NVH;
+      const int DD = isv ? Dv : D;
+      const int d = half * 128 + lrow;
+      float* out = isv ? p.dV : p.dK;
+      const float fac = isv ? st.dv_fac : st.dk_fac;
+      const uint32_t tcol = isv ? C::T_V + half * BK : C::T_K + half * BK;
+#pragma unroll 1
+      for (int c = ch * C::HALF; c < (ch + 1) * C::HALF; c += 32) {
         float v[32];
-        if (!first) {
-          tmem_ld32(tV + hh * BK + lane_off + c, v);
+        if (have) {
+          tmem_ld32(tbase + tcol + lane_off + c, v);
           tmem_ld_wait();
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = 0.f;
         }
-        if (dv < Dv) {
+        if (d < DD) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int j = j0 + c + e;
-            if (j < p.M) p.dV[((size_t)j * p.Hkv + hk) * Dv + dv] = v[e] * st.dv_fac;
-          }
-        }
-      }
-    }
-#pragma unroll 1
-    for (int hh = 0; hh < C::NDH; ++hh) {
-      const int d = hh * 128 + lrow;
-#pragma unroll 1
-      for (int c = 0; c < BK; c += 32) {
-        float v[32];
-        if (!first) {
-          tmem_ld32(tK + hh * BK + lane_off + c, v);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = 0.f;
-        }
-        if (d < D) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int j = j0 + c + e;
-            if (j < p.M) p.dK[((size_t)j * p.Hkv + hk) * D + d] = v[e] * st.dk_fac;
+            if (j < p.M) out[((size_t)j * p.Hkv + hk) * DD + d] = v[e] * fac;
           }
         }
       }
     }
   }
+
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, C::TCOLS);
   }
