@@ -237,7 +237,7 @@ static cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& 
     rec.mark(KS_DQ_REDUCE);
   }
   if (P.nKT > 0) {
-    k_cols2<D, Dv, BK><<<dim3(P.nKT, p.Hkv), 512, CC::SMEM, s>>>(tmQ, tmO, p);
+    k_cols2<D, Dv, BK><<<dim3(P.nKT, p.Hkv), 384, CC::SMEM, s>>>(tmQ, tmO, p);
     rec.mark(KS_COLS);
   }
   return cudaGetLastError();

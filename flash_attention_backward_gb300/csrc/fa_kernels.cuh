@@ -173,13 +173,30 @@ __device__ __forceinline__ uint4 decode8_h(const uint8_t* row, int type, int c0,
 // ---- decoders of the row passes: raw rows staged in shared memory -> binary16 operand tiles
 //
 // A decoder thread owns one column group of every row it handles: a whole 32-value block for
-// q8_0 / q4_0 (one scale load, the codes read as aligned 32-bit words and realigned with funnel
-// shifts), 8 values for f16 / f32.  Its V shifts are therefore fixed and held in registers.
+// q8_0 / q4_0 (one scale load, the codes read as aligned 32-bit words), 8 values for f16 / f32.
+// Its V shifts are therefore fixed and held in registers.
 __device__ __forceinline__ int group_cols(int type) { return (type == kTypeQ8 || type == kTypeQ4) ? 32 : 8; }
+
+// Decoder thread -> (group, first row, row step).  For q8_0/q4_0 the 8 lanes of a quarter-warp
+// take one column group of 8 consecutive rows, so their 16-byte stores hit 8 distinct bank
+// groups of the swizzled tile; for f16/f32 they take 8 consecutive groups of one row.
+__device__ __forceinline__ void decoder_map(int type, int DD, int NT, int dt, int& g, int& r0, int& rs) {
+  const int ng = DD / group_cols(type);
+  if (type == kTypeQ8 || type == kTypeQ4) {
+    g = (dt >> 3) % ng;
+    r0 = (dt & 7) + 8 * (dt / (8 * ng));
+  } else {
+    g = dt % ng;
+    r0 = dt / ng;
+  }
+  rs = NT / ng;
+}
 
 template <int DD, int NT>
 __device__ __forceinline__ void load_group_shift(const float* shift, int type, int dt, __half2* sh) {
-  const int cg = group_cols(type), g = dt % (DD / cg);
+  int g, r0, rs;
+  decoder_map(type, DD, NT, dt, g, r0, rs);
+  const int cg = group_cols(type);
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
     const int c = g * cg + 2 * e;
@@ -187,41 +204,46 @@ __device__ __forceinline__ void load_group_shift(const float* shift, int type, i
   }
 }
 
-// Four packed binary16 pairs from four bytes holding values v+1024 after the exponent trick.
-__device__ __forceinline__ void four_codes(uint32_t c, __half2 bias, __half2 ds, __half2 s0, __half2 s1, uint32_t& o0,
-                                           uint32_t& o1) {
-  const __half2 lo = u32_as_h2(__byte_perm(c, 0x64646464u, 0x5140));  // bytes 0, 1
-  const __half2 hi = u32_as_h2(__byte_perm(c, 0x64646464u, 0x7362));  // bytes 2, 3
-  o0 = h2_as_u32(__hfma2(__hsub2(lo, bias), ds, s0));
-  o1 = h2_as_u32(__hfma2(__hsub2(hi, bias), ds, s1));
-}
-
 // Decode raw rows 0..nrows-1 of one staged entry (shared address raw0, stride rb_pad) into
 // rows prow0.. of a tile of DD/64 panels of [BKR][64]; rows >= nvalid become zero.
+//
+// q8_0 / q4_0: the codes of a block start 2 bytes in, so they are 4-byte aligned for every
+// other block; either way each pair of codes sits inside one aligned 32-bit word (aligned codes:
+// bytes (0,1) and (2,3) of word k; otherwise bytes (2,3) of word k and (0,1) of word k+1).  One
+// byte permute per pair puts the two biased codes under the binary16 exponent byte 0x64 (value
+// 1024 + byte), one subtraction removes the bias exactly, and one fused multiply-add applies
+// d * sigma and the shift with a single rounding.
 template <int DD, int BKR, int NT, bool SHIFT>
 __device__ __forceinline__ void decode_rows(int type, uint32_t raw0, int rb_pad, int nrows, int nvalid, int prow0,
                                             uint32_t panels, float sig, const __half2* sh, int dt) {
-  const int cg = group_cols(type), ng = DD / cg, g = dt % ng, rs = NT / ng;
+  int g, rfirst, rs;
+  decoder_map(type, DD, NT, dt, g, rfirst, rs);
   const __half2 z = __float2half2_rn(0.f);
   if (type == kTypeQ8 || type == kTypeQ4) {
     const bool q8 = type == kTypeQ8;
     const int bbytes = q8 ? 34 : 18;
     const __half2 bias = q8 ? __float2half2_rn(1152.f) : __float2half2_rn(1032.f);
-    for (int rr = dt / ng; rr < nrows; rr += rs) {
+    const __half2 sig2 = __float2half2_rn(sig);
+    for (int rr = rfirst; rr < nrows; rr += rs) {
       uint32_t o[16];
       if (rr < nvalid) {
         const uint32_t blk = raw0 + rr * rb_pad + g * bbytes;
-        const float d = __half2float(__ushort_as_half((unsigned short)lds_u16(blk)));
-        const __half2 ds = __float2half2_rn(d * sig);
-        const uint32_t cs = blk + 2, cb = cs & ~3u, shf = (cs & 3u) * 8;
+        const uint32_t dd = lds_u16(blk);
+        const __half2 ds = __hmul2(u32_as_h2(dd | (dd << 16)), sig2);  // exact: power-of-two scale
+        const uint32_t cs = blk + 2, cb = cs & ~3u;
+        const bool al = (cs & 3u) == 0;
+        const uint32_t sa = al ? 0x5140u : 0x7362u, sb = al ? 0x7362u : 0x5140u;
         if (q8) {
           uint32_t w[9];
 #pragma unroll
-          for (int k = 0; k < 9; ++k) w[k] = lds_u32(cb + 4 * k);
+          for (int k = 0; k < 9; ++k) w[k] = lds_u32(cb + 4 * k) ^ 0x80808080u;  // codes + 128
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const uint32_t c = __funnelshift_r(w[k], w[k + 1], shf) ^ 0x80808080u;  // codes + 128
-            four_codes(c, bias, ds, SHIFT ? sh[2 * k] : z, SHIFT ? sh[2 * k + 1] : z, o[2 * k], o[2 * k + 1]);
+            const uint32_t wa = w[k], wb = al ? w[k] : w[k + 1];
+            const __half2 c0 = __hsub2(u32_as_h2(__byte_perm(wa, 0x64646464u, sa)), bias);
+            const __half2 c1 = __hsub2(u32_as_h2(__byte_perm(wb, 0x64646464u, sb)), bias);
+            o[2 * k] = h2_as_u32(__hfma2(c0, ds, SHIFT ? sh[2 * k] : z));
+            o[2 * k + 1] = h2_as_u32(__hfma2(c1, ds, SHIFT ? sh[2 * k + 1] : z));
           }
         } else {
           uint32_t w[5];
@@ -229,11 +251,17 @@ __device__ __forceinline__ void decode_rows(int type, uint32_t raw0, int rb_pad,
           for (int k = 0; k < 5; ++k) w[k] = lds_u32(cb + 4 * k);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint32_t c = __funnelshift_r(w[k], w[k + 1], shf);  // bytes 4k..4k+3
-            four_codes(c & 0x0f0f0f0fu, bias, ds, SHIFT ? sh[2 * k] : z, SHIFT ? sh[2 * k + 1] : z, o[2 * k],
-                       o[2 * k + 1]);  // values 4k..4k+3 (low nibbles)
-            four_codes((c >> 4) & 0x0f0f0f0fu, bias, ds, SHIFT ? sh[8 + 2 * k] : z, SHIFT ? sh[8 + 2 * k + 1] : z,
-                       o[8 + 2 * k], o[8 + 2 * k + 1]);  // values 16+4k.. (high nibbles)
+            const uint32_t wa = w[k], wb = al ? w[k] : w[k + 1];
+            const uint32_t la = wa & 0x0f0f0f0fu, lb = wb & 0x0f0f0f0fu;                // values 4k.. (low nibbles)
+            const uint32_t ha = (wa >> 4) & 0x0f0f0f0fu, hb = (wb >> 4) & 0x0f0f0f0fu;  // values 16+4k.. (high)
+            const __half2 c0 = __hsub2(u32_as_h2(__byte_perm(la, 0x64646464u, sa)), bias);
+            const __half2 c1 = __hsub2(u32_as_h2(__byte_perm(lb, 0x64646464u, sb)), bias);
+            const __half2 c2 = __hsub2(u32_as_h2(__byte_perm(ha, 0x64646464u, sa)), bias);
+            const __half2 c3 = __hsub2(u32_as_h2(__byte_perm(hb, 0x64646464u, sb)), bias);
+            o[2 * k] = h2_as_u32(__hfma2(c0, ds, SHIFT ? sh[2 * k] : z));
+            o[2 * k + 1] = h2_as_u32(__hfma2(c1, ds, SHIFT ? sh[2 * k + 1] : z));
+            o[8 + 2 * k] = h2_as_u32(__hfma2(c2, ds, SHIFT ? sh[8 + 2 * k] : z));
+            o[8 + 2 * k + 1] = h2_as_u32(__hfma2(c3, ds, SHIFT ? sh[8 + 2 * k + 1] : z));
           }
         }
       } else {
@@ -248,7 +276,7 @@ __device__ __forceinline__ void decode_rows(int type, uint32_t raw0, int rb_pad,
   } else {
     const bool f16 = type == kTypeF16;
     const __half2 s2 = __float2half2_rn(sig);
-    for (int rr = dt / ng; rr < nrows; rr += rs) {
+    for (int rr = rfirst; rr < nrows; rr += rs) {
       uint32_t o[4] = {0u, 0u, 0u, 0u};
       if (rr < nvalid) {
         const uint32_t a = raw0 + rr * rb_pad + g * (f16 ? 16 : 32);
@@ -524,14 +552,20 @@ struct Rows2Cfg {
   static constexpr int OFF_RAW = OFF_BAR + BAR_BYTES;
   static constexpr int SMEM_MAX = 232448;
   static constexpr int RAW_BUDGET = SMEM_MAX - 1024 - 64 - OFF_RAW;  // bytes for the raw ring
-  // tensor-memory columns
+  // tensor-memory columns; slot s holds S at T_S + 2*BK*s and dP BK columns later
   static constexpr int T_Q = 0;
   static constexpr int T_O = MODE ? 0 : D / 2;
   static constexpr int T_S = T_O + Dv / 2;
-  static constexpr int T_P = T_S + BK;
-  static constexpr int T_ACC = T_P + BK;
-  static constexpr int TCOLS = pow2_at_least(MODE ? T_ACC + D : T_P + BK);
-  static constexpr int HALF = BK / 2;  // columns per softmax thread
+  static constexpr int NSLOT = (MODE == 0 && T_S + 4 * BK <= 512) ? 2 : 1;
+  static constexpr int T_ACC = T_S + 2 * BK;
+  static constexpr int TCOLS = pow2_at_least(MODE ? T_ACC + D : T_S + 2 * BK * NSLOT);
+  // softmax warps 4 .. 4+NSOFT-1 (NCH of them per tensor-memory lane quarter, splitting the
+  // columns); decoder warps 2, 3 and 4+NSOFT .. 15.  The LSE pass has two S/dP slots, so one
+  // softmax thread per row suffices and more warps decode.
+  static constexpr int NSOFT = MODE ? 8 : 4;
+  static constexpr int NCH = NSOFT / 4;
+  static constexpr int HALF = BK / NCH;  // columns per softmax thread
+  static constexpr int NDEC = 16 - 2 - NSOFT;
 };
 
 // barrier indices
@@ -541,9 +575,9 @@ enum {
   B_KV_FULL = 8,    // [2]
   B_K_EMPTY = 10,   // [2]
   B_V_EMPTY = 12,   // [2]
-  B_S_FULL = 14,
-  B_S_FREE,
-  B_DS_FULL,
+  B_S_FULL = 14,    // [2]
+  B_S_FREE = 16,    // [2]
+  B_DS_FULL = 18,
   B_DS_EMPTY,
   B_ACC_FULL,
   B_Q_FULL,
@@ -600,20 +634,20 @@ __global__ void __launch_bounds__(512, 1)
   if (tid == 0) {
     for (int s = 0; s < 4; ++s) {
       mbar_init(&bar[B_RAW_FULL + s], p.raw_bulk ? 1 : 32);
-      mbar_init(&bar[B_RAW_EMPTY + s], 4);
+      mbar_init(&bar[B_RAW_EMPTY + s], C::NDEC);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar[B_KV_FULL + s], 4);
+      mbar_init(&bar[B_KV_FULL + s], C::NDEC);
       mbar_init(&bar[B_K_EMPTY + s], 1);
       mbar_init(&bar[B_V_EMPTY + s], 1);
+      mbar_init(&bar[B_S_FULL + s], 1);
+      mbar_init(&bar[B_S_FREE + s], C::NSOFT);
     }
-    mbar_init(&bar[B_S_FULL], 1);
-    mbar_init(&bar[B_S_FREE], 8);
-    mbar_init(&bar[B_DS_FULL], 8);
+    mbar_init(&bar[B_DS_FULL], C::NSOFT);
     mbar_init(&bar[B_DS_EMPTY], 1);
     mbar_init(&bar[B_ACC_FULL], 1);
     mbar_init(&bar[B_Q_FULL], 1);
-    mbar_init(&bar[B_OPS_READY], 8);
+    mbar_init(&bar[B_OPS_READY], C::NSOFT);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -675,12 +709,12 @@ __global__ void __launch_bounds__(512, 1)
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t ID_S = idesc_f16(128, BK, false, false);
       constexpr uint32_t ID_DQ = idesc_f16(128, D, false, true);
-      const uint32_t tS = tbase + C::T_S, tP = tbase + C::T_P, tQ = tbase + C::T_Q, tO = tbase + C::T_O,
-                     tAcc = tbase + C::T_ACC;
-      bool ok = (MODE == 0 || wait(&bar[B_Q_FULL], 0)) && wait(&bar[B_OPS_READY], 0);
-      for (int t = 0; ok && t < ntiles; ++t) {
-        const int ks = t & 1, vs = MODE ? 0 : (t & 1);
-        if (!wait(&bar[B_KV_FULL + ks], (t >> 1) & 1) || !wait(&bar[B_S_FREE], (t & 1) ^ 1)) break;
+      const uint32_t tQ = tbase + C::T_Q, tO = tbase + C::T_O, tAcc = tbase + C::T_ACC;
+      const bool ok = (MODE == 0 || wait(&bar[B_Q_FULL], 0)) && wait(&bar[B_OPS_READY], 0);
+      // S(t) = Q K'^T and dP(t) = dO V'^T into the tensor-memory slot of tile t
+      auto issue_sdp = [&](int t) {
+        const int ks = t & 1, vs = MODE ? 0 : (t & 1), sl = t % C::NSLOT;
+        const uint32_t tS = tbase + C::T_S + 2 * BK * sl, tP = tS + BK;
         tc_fence_after();
         const uint32_t bk = smem_u32(sK + ks * C::KB), bv = smem_u32(sV + vs * C::VB);
 #pragma unroll
@@ -695,40 +729,63 @@ __global__ void __launch_bounds__(512, 1)
         for (int k = 0; k < Dv / 16; ++k)
           mma_f16_tmem_a(tP, tO + k * 8, sdesc_sw128(bv + (k / 4) * (BK * 128) + (k % 4) * 32, 16, 1024), ID_S,
                          k > 0);
-        mma_commit(&bar[B_S_FULL]);
+        mma_commit(&bar[B_S_FULL + sl]);
         mma_commit(&bar[B_V_EMPTY + vs]);
         if (MODE == 0) mma_commit(&bar[B_K_EMPTY + ks]);
-        if (MODE == 1 && t >= 1) {
-          // dQ += dS(t-1) K'(t-1)
-          if (!wait(&bar[B_DS_FULL], (t - 1) & 1)) break;
-          tc_fence_after();
-          const uint32_t kp = smem_u32(sK + ((t - 1) & 1) * C::KB);
+      };
+      // dQ += dS(t) K'(t)
+      auto issue_dq = [&](int t) {
+        tc_fence_after();
+        const uint32_t kp = smem_u32(sK + (t & 1) * C::KB);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            mma_f16(tAcc, sdesc_sw128(smem_u32(sS) + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024),
-                    sdesc_sw128(kp + k * 2048, BK * 128, 1024), ID_DQ, (t - 1 > 0 || k > 0) ? 1u : 0u);
-          mma_commit(&bar[B_DS_EMPTY]);
-          mma_commit(&bar[B_K_EMPTY + ((t - 1) & 1)]);
-        }
-      }
-      if (MODE == 1 && !*s_abort) {
-        const int t = ntiles;
-        if (wait(&bar[B_DS_FULL], (t - 1) & 1)) {
-          tc_fence_after();
-          const uint32_t kp = smem_u32(sK + ((t - 1) & 1) * C::KB);
-#pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            mma_f16(tAcc, sdesc_sw128(smem_u32(sS) + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024),
-                    sdesc_sw128(kp + k * 2048, BK * 128, 1024), ID_DQ, (t - 1 > 0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < BK / 16; ++k)
+          mma_f16(tAcc, sdesc_sw128(smem_u32(sS) + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024),
+                  sdesc_sw128(kp + k * 2048, BK * 128, 1024), ID_DQ, (t > 0 || k > 0) ? 1u : 0u);
+        if (t == ntiles - 1) {
           mma_commit(&bar[B_ACC_FULL]);
+        } else {
+          mma_commit(&bar[B_DS_EMPTY]);
+          mma_commit(&bar[B_K_EMPTY + (t & 1)]);
+        }
+      };
+      if (MODE == 0) {
+        for (int t = 0; ok && t < ntiles; ++t) {
+          const int sl = t % C::NSLOT, su = t / C::NSLOT;
+          if (!wait(&bar[B_KV_FULL + (t & 1)], (t >> 1) & 1) || !wait(&bar[B_S_FREE + sl], (su & 1) ^ 1)) break;
+          issue_sdp(t);
+        }
+      } else if (ok) {
+        // Issue whichever product is ready, dQ first: it frees the K' stage the decoders need next.
+        int ns = 0, nd = 0;
+        uint64_t t0 = globaltimer_ns();
+        while (nd < ntiles) {
+          if (nd < ns && mbar_try_wait(&bar[B_DS_FULL], nd & 1)) {
+            issue_dq(nd++);
+            t0 = globaltimer_ns();
+            continue;
+          }
+          if (ns < ntiles && mbar_try_wait(&bar[B_KV_FULL + (ns & 1)], (ns >> 1) & 1) &&
+              mbar_try_wait(&bar[B_S_FREE], (ns & 1) ^ 1)) {
+            issue_sdp(ns++);
+            t0 = globaltimer_ns();
+            continue;
+          }
+          if (*s_abort) break;
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *s_abort = 1;
+            record_error(p.err, kErrTimeout);
+            break;
+          }
         }
       }
     }
-  } else if (warp >= 12) {
+  } else if (warp >= 4 + C::NSOFT || warp == 2 || warp == 3) {
     // ------------------------------------------------------------------ decoders
-    const int dt = tid - 12 * 32;
+    constexpr int NDT = C::NDEC * 32;
+    static_assert(NDT % 64 == 0, "decoder_map needs a multiple of 8 column groups of 8 lanes");
+    const int dt = (warp < 4 ? warp - 2 : warp - (4 + C::NSOFT) + 2) * 32 + lane;
     __half2 vsh[16];
-    load_group_shift<Dv, 128>(p.rsh + (size_t)hk * Dv, p.v_type, dt, vsh);
+    load_group_shift<Dv, NDT>(p.rsh + (size_t)hk * Dv, p.v_type, dt, vsh);
     for (int t = 0; t < ntiles; ++t) {
       const int ks = t & 1, vs = MODE ? 0 : (t & 1);
       if (!wait(&bar[B_K_EMPTY + ks], ((t >> 1) & 1) ^ 1)) break;
@@ -745,18 +802,19 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t rk = smem_u32(sRaw) + slot * entry_bytes;
         const uint32_t rv = rk + KE * p.rbk_pad;
         const int nv = max(0, min(KE, p.M - (j0 + h * KE)));
-        decode_rows<D, BK, 128, false>(p.k_type, rk, p.rbk_pad, KE, nv, h * KE, kd, st.sK, vsh, dt);
-        decode_rows<Dv, BK, 128, true>(p.v_type, rv, p.rbv_pad, KE, nv, h * KE, vd, st.sV, vsh, dt);
-        fence_proxy_async_smem();
+        decode_rows<D, BK, NDT, false>(p.k_type, rk, p.rbk_pad, KE, nv, h * KE, kd, st.sK, vsh, dt);
+        decode_rows<Dv, BK, NDT, true>(p.v_type, rv, p.rbv_pad, KE, nv, h * KE, vd, st.sV, vsh, dt);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[B_RAW_EMPTY + slot]);
+        if (lane == 0) mbar_arrive(&bar[B_RAW_EMPTY + slot]);  // raw entry consumed
       }
       if (!ok) break;
+      fence_proxy_async_smem();  // the tile's binary16 stores, visible to the tensor cores
+      __syncwarp();
       if (lane == 0) mbar_arrive(&bar[B_KV_FULL + ks]);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax
-    const int q4 = warp & 3, ch = (warp - 4) >> 2;
+    const int q4 = warp & 3, ch = (warp - 4) >> 2;  // ch < C::NCH
     const int row = q4 * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const int r = r0 + row;
@@ -771,17 +829,19 @@ __global__ void __launch_bounds__(512, 1)
       dl = p.dlt[(size_t)hk * R + r];
     }
     const bool live = MODE == 1 ? (lse2 > -CUDART_INF_F) : rvalid;
-    const float nlse2 = live ? -lse2 : -CUDART_INF_F;  // exp2(t2 + nlse2) = p, and 0 on a dead row
+    const float nlse2 = live ? -lse2 : -CUDART_INF_F;  // 2^(t2 + nlse2) = p, and 0 on a dead row
+    const float c2 = st.c2, lam = st.lam, dq_fac = st.dq_fac;
     const uint32_t sS_u = smem_u32(sS);
     float m2 = -CUDART_INF_F, l = 0.f, lc = 0.f, sd = 0.f, sdc = 0.f;
 
     if (ntiles > 0) {
-      // this thread's half of the row's A operands into tensor memory (binary16 pairs per column)
+      // this thread's share of the row's A operands into tensor memory (binary16 pairs per column)
       auto put_row = [&](const __half* src, int DD, uint32_t tcol) {
-        // DD/2 32-bit words per row; with 64 or more words the two halves split them, with 32
-        // the first half writes all of them (tensor-memory stores move 32 columns at a time)
+        // DD/2 32-bit words per row, split between the NCH threads of the row; a share under
+        // 32 words goes whole to the first (tensor-memory stores move 32 columns at a time)
         const int wpr = DD / 2;
-        const int w0 = wpr >= 64 ? ch * (wpr / 2) : 0, nw = wpr >= 64 ? wpr / 2 : (ch == 0 ? wpr : 0);
+        const int per = wpr / C::NCH;
+        const int w0 = per >= 32 ? ch * per : 0, nw = per >= 32 ? per : (ch == 0 ? wpr : 0);
         const uint4* s4 = reinterpret_cast<const uint4*>(src) + w0 / 4;
         for (int c = 0; c < nw; c += 32) {
           uint32_t wv[32];
@@ -804,27 +864,29 @@ __global__ void __launch_bounds__(512, 1)
 
     for (int t = 0; t < ntiles; ++t) {
       const int j0 = (kt_begin + t) * BK;
-      if (!wait(&bar[B_S_FULL], t & 1)) break;
+      const int sl = t % C::NSLOT, su = t / C::NSLOT;
+      if (!wait(&bar[B_S_FULL + sl], su & 1)) break;
       tc_fence_after();
       bool stored_wait = false;
+      const uint32_t tS = tbase + C::T_S + 2 * BK * sl;
 #pragma unroll 1
       for (int c = 0; c < C::HALF; c += 32) {
         const int col0 = ch * C::HALF + c;
         float s[32], dp[32];
-        tmem_ld32(tbase + C::T_S + lane_off + col0, s);
-        tmem_ld32(tbase + C::T_P + lane_off + col0, dp);
+        tmem_ld32(tS + lane_off + col0, s);
+        tmem_ld32(tS + BK + lane_off + col0, dp);
         tmem_ld_wait();
-        if (c + 32 >= C::HALF) {
+        if (c + 32 >= C::HALF) {  // the slot is free once its last columns are in registers
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bar[B_S_FREE]);
+          if (lane == 0) mbar_arrive(&bar[B_S_FREE + sl]);
         }
         // fully visible chunk without a mask: no per-key tests
         const bool full = mrow == nullptr && (long)(j0 + col0 + 31) <= jlast;
         float t2[32];
         if (full) {
 #pragma unroll
-          for (int n = 0; n < 32; ++n) t2[n] = s[n] * st.c2;
+          for (int n = 0; n < 32; ++n) t2[n] = s[n] * c2;
         } else {
 #pragma unroll
           for (int n = 0; n < 32; ++n) {
@@ -835,7 +897,7 @@ __global__ void __launch_bounds__(512, 1)
               mv = h2f(__ldg(reinterpret_cast<const unsigned short*>(mrow) + j));
               ok = !(mv == -CUDART_INF_F);
             }
-            t2[n] = ok ? fmaf(s[n], st.c2, mv * kLog2e) : -CUDART_INF_F;
+            t2[n] = ok ? fmaf(s[n], c2, mv * kLog2e) : -CUDART_INF_F;
           }
         }
         if (MODE == 0) {
@@ -843,7 +905,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int n = 0; n < 32; ++n) cmax = fmaxf(cmax, t2[n]);
           if (cmax > m2) {
-            const float f = exp2f(m2 - cmax);
+            const float f = ex2(m2 - cmax);  // 0 while m2 = -inf
             l *= f, lc *= f, sd *= f, sdc *= f;
             m2 = cmax;
           }
@@ -851,10 +913,11 @@ __global__ void __launch_bounds__(512, 1)
             float cl = 0.f, cs = 0.f;
 #pragma unroll
             for (int n = 0; n < 32; ++n) {
-              const float e = exp2f(t2[n] - m2);
+              const float e = ex2(t2[n] - m2);
               cl += e;
               cs = fmaf(e, dp[n], cs);
             }
+            // compensated accumulation of the chunk sums
             float y = cl - lc, tt = l + y;
             lc = (tt - l) - y, l = tt;
             y = cs - sdc, tt = sd + y;
@@ -864,8 +927,8 @@ __global__ void __launch_bounds__(512, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int n = 0; n < 32; n += 2) {
-            const float p0 = exp2f(t2[n] + nlse2), p1 = exp2f(t2[n + 1] + nlse2);  // 0 for masked keys, dead rows
-            pk[n / 2] = h2_as_u32(__floats2half2_rn(p0 * (dp[n] - dl) * st.lam, p1 * (dp[n + 1] - dl) * st.lam));
+            const float p0 = ex2(t2[n] + nlse2), p1 = ex2(t2[n + 1] + nlse2);  // 0 for masked keys, dead rows
+            pk[n / 2] = h2_as_u32(__floats2half2_rn(p0 * (dp[n] - dl) * lam, p1 * (dp[n + 1] - dl) * lam));
           }
           if (!stored_wait) {
             if (!wait(&bar[B_DS_EMPTY], (t & 1) ^ 1)) break;
@@ -886,14 +949,17 @@ __global__ void __launch_bounds__(512, 1)
 
     // epilogue
     if (MODE == 0) {
-      if (ch == 1) s_merge[row * 3 + 0] = m2, s_merge[row * 3 + 1] = l, s_merge[row * 3 + 2] = sd;
-      named_bar_sync(1, 256);
+      if (C::NCH == 2) {
+        if (ch == 1) s_merge[row * 3 + 0] = m2, s_merge[row * 3 + 1] = l, s_merge[row * 3 + 2] = sd;
+        named_bar_sync(1, 32 * C::NSOFT);
+      }
       if (ch == 0 && rvalid) {
-        const float m2b = s_merge[row * 3 + 0], lb = s_merge[row * 3 + 1], sdb = s_merge[row * 3 + 2];
+        float m2b = -CUDART_INF_F, lb = 0.f, sdb = 0.f;
+        if (C::NCH == 2) m2b = s_merge[row * 3 + 0], lb = s_merge[row * 3 + 1], sdb = s_merge[row * 3 + 2];
         const float mm = fmaxf(m2, m2b);
         float L = 0.f, SD = 0.f;
         if (mm > -CUDART_INF_F) {
-          const float fa = exp2f(m2 - mm), fb = exp2f(m2b - mm);
+          const float fa = ex2(m2 - mm), fb = ex2(m2b - mm);
           L = l * fa + lb * fb;
           SD = sd * fa + sdb * fb;
         }
@@ -907,7 +973,7 @@ __global__ void __launch_bounds__(512, 1)
       const bool have = ntiles > 0 && wait(&bar[B_ACC_FULL], 0);
       if (have) tc_fence_after();
 #pragma unroll 1
-      for (int c = ch * (D / 2); c < (ch + 1) * (D / 2); c += 32) {
+      for (int c = ch * (D / C::NCH); c < (ch + 1) * (D / C::NCH); c += 32) {
         float v[32];
         if (have) {
           tmem_ld32(tbase + C::T_ACC + lane_off + c, v);
@@ -920,7 +986,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4*>(out + c + e) =
-                make_float4(v[e] * st.dq_fac, v[e + 1] * st.dq_fac, v[e + 2] * st.dq_fac, v[e + 3] * st.dq_fac);
+                make_float4(v[e] * dq_fac, v[e + 1] * dq_fac, v[e + 2] * dq_fac, v[e + 3] * dq_fac);
         }
       }
     }
@@ -1025,7 +1091,7 @@ enum {
 };
 
 template <int D, int Dv, int BK>
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(384, 1)
     k_cols2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO, Params p) {
   using C = Cols2Cfg<D, Dv, BK>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1068,8 +1134,8 @@ __global__ void __launch_bounds__(512, 1)
   }
   const Stats st = *p.st;
   if (nq > 0) {  // K' and V' once, by every thread
-    decode_tile<D, BK, 512>(p.k, p.k_type, p.rbk, hk, p.Hkv, j0, p.M, sK, st.sK, nullptr, tid);
-    decode_tile<Dv, BK, 512>(p.v, p.v_type, p.rbv, hk, p.Hkv, j0, p.M, sV, st.sV, p.rsh + (size_t)hk * Dv, tid);
+    decode_tile<D, BK, 384>(p.k, p.k_type, p.rbk, hk, p.Hkv, j0, p.M, sK, st.sK, nullptr, tid);
+    decode_tile<Dv, BK, 384>(p.v, p.v_type, p.rbv, hk, p.Hkv, j0, p.M, sV, st.sV, p.rsh + (size_t)hk * Dv, tid);
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -1154,7 +1220,7 @@ __global__ void __launch_bounds__(512, 1)
       }
       mma_commit(&bar[C_DONE]);
     }
-  } else if (warp >= 4 && warp < 12) {
+  } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax, then epilogue
     const int q4 = warp & 3, ch = (warp - 4) >> 2;
     const int row = q4 * 32 + lane;
@@ -1173,16 +1239,18 @@ __global__ void __launch_bounds__(512, 1)
     long jlast = -1;
     const uint16_t* mrow = nullptr;
     const uint32_t sP_u = smem_u32(sP), sS_u = smem_u32(sS);
+    const float c2 = st.c2, pmul = st.sP, lam = st.lam;
     if (nq > 0) row_stats(0, lse2, dl, jlast, mrow);
     for (int t = 0; t < nq; ++t) {
       float nlse2 = 0.f, ndl = 0.f;  // next tile's row values, fetched ahead
       long njlast = -1;
       const uint16_t* nmrow = nullptr;
       if (t + 1 < nq) row_stats(t + 1, nlse2, ndl, njlast, nmrow);
-      const bool live = lse2 > -CUDART_INF_F;
+      const float nl = lse2 > -CUDART_INF_F ? -lse2 : -CUDART_INF_F;  // p = 2^(t2 + nl); 0 on a dead row
       if (!wait(&bar[C_S_FULL], t & 1)) break;
+      // the previous tile's P and dS panels are free once its gradient products completed
+      if (!wait(&bar[C_DS_EMPTY], (t & 1) ^ 1)) break;
       tc_fence_after();
-      bool waited = false;
 #pragma unroll 1
       for (int c = 0; c < C::HALF; c += 32) {
         const int col0 = ch * C::HALF + c;
@@ -1190,42 +1258,38 @@ __global__ void __launch_bounds__(512, 1)
         tmem_ld32(tbase + C::T_S + lane_off + col0, s);
         tmem_ld32(tbase + C::T_P + lane_off + col0, dp);
         tmem_ld_wait();
-        uint32_t pp[16], pd[16];
         const bool full = mrow == nullptr && (long)(j0 + col0 + 31) <= jlast;
-        const float nl = live ? -lse2 : -CUDART_INF_F;
 #pragma unroll
-        for (int n = 0; n < 32; n += 2) {
-          float pr[2], ds[2];
+        for (int g = 0; g < 32; g += 8) {
+          uint32_t pp[4], pd[4];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float t2;
-            if (full) {
-              t2 = fmaf(s[n + e], st.c2, nl);
-            } else {
-              const int j = j0 + col0 + n + e;
-              bool ok = (long)j <= jlast;
-              float mv = 0.f;
-              if (ok && mrow) {
-                mv = h2f(__ldg(reinterpret_cast<const unsigned short*>(mrow) + j));
-                ok = !(mv == -CUDART_INF_F);
+          for (int n = 0; n < 8; n += 2) {
+            float pr[2], ds[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int x = g + n + e;
+              float t2;
+              if (full) {
+                t2 = fmaf(s[x], c2, nl);
+              } else {
+                const int j = j0 + col0 + x;
+                bool ok = (long)j <= jlast;
+                float mv = 0.f;
+                if (ok && mrow) {
+                  mv = h2f(__ldg(reinterpret_cast<const unsigned short*>(mrow) + j));
+                  ok = !(mv == -CUDART_INF_F);
+                }
+                t2 = ok ? fmaf(s[x], c2, mv * kLog2e) + nl : -CUDART_INF_F;
               }
-              t2 = ok ? fmaf(s[n + e], st.c2, mv * kLog2e) + nl : -CUDART_INF_F;
+              pr[e] = ex2(t2);
+              ds[e] = pr[e] * (dp[x] - dl);
             }
-            pr[e] = exp2f(t2);
-            ds[e] = pr[e] * (dp[n + e] - dl);
+            pp[n / 2] = h2_as_u32(__floats2half2_rn(pr[0] * pmul, pr[1] * pmul));
+            pd[n / 2] = h2_as_u32(__floats2half2_rn(ds[0] * lam, ds[1] * lam));
           }
-          pp[n / 2] = h2_as_u32(__floats2half2_rn(pr[0] * st.sP, pr[1] * st.sP));
-          pd[n / 2] = h2_as_u32(__floats2half2_rn(ds[0] * st.lam, ds[1] * st.lam));
-        }
-        if (!waited) {
-          if (!wait(&bar[C_DS_EMPTY], (t & 1) ^ 1)) break;
-          waited = true;
-        }
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const uint32_t off = panel_off_u(128, row, col0 + 8 * x);
-          sts_v4(sP_u + off, pp[4 * x], pp[4 * x + 1], pp[4 * x + 2], pp[4 * x + 3]);
-          sts_v4(sS_u + off, pd[4 * x], pd[4 * x + 1], pd[4 * x + 2], pd[4 * x + 3]);
+          const uint32_t off = panel_off_u(128, row, col0 + g);
+          sts_v4(sP_u + off, pp[0], pp[1], pp[2], pp[3]);
+          sts_v4(sS_u + off, pd[0], pd[1], pd[2], pd[3]);
         }
       }
       if (*s_abort) break;

@@ -48,6 +48,14 @@ __device__ __forceinline__ void sts_v4(uint32_t a, uint32_t x, uint32_t y, uint3
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
 }
 
+// 2^x by the hardware approximation (PTX ex2.approx.ftz.f32: relative error about 2^-22;
+// results below 2^-126 flush to zero; 2^-inf = +0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------------------------------------------------------------
 // mbarrier
 
