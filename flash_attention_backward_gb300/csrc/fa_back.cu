@@ -49,10 +49,16 @@ static Plan make_plan(int N, int M, int H, int Hkv, int D, int Dv, int nsm) {
   P.nQT = (P.R + 127) / 128;
   P.BK = block_keys(D, Dv);
   P.nKT = (M + P.BK - 1) / P.BK;
-  // split the keys of each row tile so the row passes fill the GPU about twice
+  // Split the keys of each row tile: pick the split count whose last wave of CTAs (one per SM)
+  // wastes least, counting a small cost per split for the partial merges.
   const int base = std::max(1, P.nQT * Hkv);
-  int ns = (2 * nsm + base - 1) / base;
-  ns = std::max(1, std::min(ns, std::max(1, P.nKT)));
+  int ns = 1;
+  double best = 1e30;
+  for (int c = 1; c <= std::min(64, std::max(1, P.nKT)); ++c) {
+    const double waves = (double)(((long)base * c + nsm - 1) / nsm);
+    const double cost = waves / c * (1.0 + 0.01 * c);
+    if (cost < best - 1e-12) best = cost, ns = c;
+  }
   P.kt_per_split = P.nKT > 0 ? (P.nKT + ns - 1) / ns : 1;
   P.nsplit = P.nKT > 0 ? (P.nKT + P.kt_per_split - 1) / P.kt_per_split : 1;
   P.nsplit_dq = P.nsplit;
@@ -191,7 +197,7 @@ static void pick_raw(Params& q, int budget, int BK) {
   int ke = std::min(32, BK);
   while (ke > 1 && 2 * ke * pair > budget) ke >>= 1;
   q.ke = ke;
-  q.raw_depth = std::max(2, std::min(4, budget / std::max(1, ke * pair)));
+  q.raw_depth = std::max(2, std::min(kMaxRawDepth, budget / std::max(1, ke * pair)));
 }
 
 template <int D, int Dv>

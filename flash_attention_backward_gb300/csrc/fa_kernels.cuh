@@ -569,15 +569,16 @@ struct Rows2Cfg {
 };
 
 // barrier indices
+constexpr int kMaxRawDepth = 8;  // raw staging entries
 enum {
-  B_RAW_FULL = 0,   // [4]
-  B_RAW_EMPTY = 4,  // [4]
-  B_KV_FULL = 8,    // [2]
-  B_K_EMPTY = 10,   // [2]
-  B_V_EMPTY = 12,   // [2]
-  B_S_FULL = 14,    // [2]
-  B_S_FREE = 16,    // [2]
-  B_DS_FULL = 18,
+  B_RAW_FULL = 0,                           // [kMaxRawDepth]
+  B_RAW_EMPTY = B_RAW_FULL + kMaxRawDepth,  // [kMaxRawDepth]
+  B_KV_FULL = B_RAW_EMPTY + kMaxRawDepth,   // [2]
+  B_K_EMPTY = B_KV_FULL + 2,                // [2]
+  B_V_EMPTY = B_K_EMPTY + 2,                // [2]
+  B_S_FULL = B_V_EMPTY + 2,                 // [2]
+  B_S_FREE = B_S_FULL + 2,                  // [2]
+  B_DS_FULL = B_S_FREE + 2,
   B_DS_EMPTY,
   B_ACC_FULL,
   B_Q_FULL,
@@ -589,6 +590,7 @@ struct Waiter {
   volatile int* abort;
   int* err;
   __device__ __forceinline__ bool operator()(uint64_t* bar, uint32_t parity) const {
+    if (mbar_try_wait(bar, parity)) return true;  // fast path: the phase is already complete
     if (*abort) return false;
     if (mbar_wait_bounded(bar, parity, kWaitLimitNs)) return true;
     *abort = 1;
@@ -632,7 +634,7 @@ __global__ void __launch_bounds__(512, 1)
 
   if (warp == 1) tmem_alloc(tslot, C::TCOLS);
   if (tid == 0) {
-    for (int s = 0; s < 4; ++s) {
+    for (int s = 0; s < kMaxRawDepth; ++s) {
       mbar_init(&bar[B_RAW_FULL + s], p.raw_bulk ? 1 : 32);
       mbar_init(&bar[B_RAW_EMPTY + s], C::NDEC);
     }
@@ -669,10 +671,10 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) tma_load_3d(sQ + c * 128 * 128, &tmQ, &bar[B_Q_FULL], c * 64, r0, hk);
     }
+    int slot = 0, use = 0;  // raw ring position of entry t * EPT + h
     for (int t = 0; t < ntiles; ++t) {
       const int j0 = (kt_begin + t) * BK;
-      for (int h = 0; h < EPT; ++h) {
-        const int e = t * EPT + h, slot = e % RD, use = e / RD;
+      for (int h = 0; h < EPT; ++h, slot = (slot + 1 == RD) ? 0 : slot + 1, use += (slot == 0)) {
         if (!wait(&bar[B_RAW_EMPTY + slot], (use & 1) ^ 1)) break;
         const int ja = j0 + h * KE;
         const int nv = max(0, min(KE, p.M - ja));
@@ -786,6 +788,7 @@ __global__ void __launch_bounds__(512, 1)
     const int dt = (warp < 4 ? warp - 2 : warp - (4 + C::NSOFT) + 2) * 32 + lane;
     __half2 vsh[16];
     load_group_shift<Dv, NDT>(p.rsh + (size_t)hk * Dv, p.v_type, dt, vsh);
+    int slot = 0, use = 0;  // raw ring position of entry t * EPT + h
     for (int t = 0; t < ntiles; ++t) {
       const int ks = t & 1, vs = MODE ? 0 : (t & 1);
       if (!wait(&bar[B_K_EMPTY + ks], ((t >> 1) & 1) ^ 1)) break;
@@ -793,8 +796,7 @@ __global__ void __launch_bounds__(512, 1)
       const uint32_t kd = smem_u32(sK + ks * C::KB), vd = smem_u32(sV + vs * C::VB);
       const int j0 = (kt_begin + t) * BK;
       bool ok = true;
-      for (int h = 0; h < EPT; ++h) {
-        const int e = t * EPT + h, slot = e % RD, use = e / RD;
+      for (int h = 0; h < EPT; ++h, slot = (slot + 1 == RD) ? 0 : slot + 1, use += (slot == 0)) {
         if (!wait(&bar[B_RAW_FULL + slot], use & 1)) {
           ok = false;
           break;
