@@ -560,9 +560,9 @@ struct Rows2Cfg {
   static constexpr int T_ACC = T_S + 2 * BK;
   static constexpr int TCOLS = pow2_at_least(MODE ? T_ACC + D : T_S + 2 * BK * NSLOT);
   // softmax warps 4 .. 4+NSOFT-1 (NCH of them per tensor-memory lane quarter, splitting the
-  // columns); decoder warps 2, 3 and 4+NSOFT .. 15.  The LSE pass has two S/dP slots, so one
-  // softmax thread per row suffices and more warps decode.
-  static constexpr int NSOFT = MODE ? 8 : 4;
+  // columns); decoder warps 2, 3 and 4+NSOFT .. 15.  Decoding is the longer of the two per key
+  // tile, so one softmax thread per row suffices and ten warps decode.
+  static constexpr int NSOFT = 4;
   static constexpr int NCH = NSOFT / 4;
   static constexpr int HALF = BK / NCH;  // columns per softmax thread
   static constexpr int NDEC = 16 - 2 - NSOFT;
