@@ -1260,34 +1260,33 @@ __global__ void __launch_bounds__(384, 1)
         tmem_ld32(tbase + C::T_S + lane_off + col0, s);
         tmem_ld32(tbase + C::T_P + lane_off + col0, dp);
         tmem_ld_wait();
-        const bool full = mrow == nullptr && (long)(j0 + col0 + 31) <= jlast;
+        // log2-domain exponents; a fully visible chunk without a mask takes no per-key tests
+        float t2[32];
+        if (mrow == nullptr && (long)(j0 + col0 + 31) <= jlast) {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) t2[x] = fmaf(s[x], c2, nl);
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            const int j = j0 + col0 + x;
+            bool ok = (long)j <= jlast;
+            float mv = 0.f;
+            if (ok && mrow) {
+              mv = h2f(__ldg(reinterpret_cast<const unsigned short*>(mrow) + j));
+              ok = !(mv == -CUDART_INF_F);
+            }
+            t2[x] = ok ? fmaf(s[x], c2, mv * kLog2e) + nl : -CUDART_INF_F;
+          }
+        }
 #pragma unroll
         for (int g = 0; g < 32; g += 8) {
           uint32_t pp[4], pd[4];
 #pragma unroll
           for (int n = 0; n < 8; n += 2) {
-            float pr[2], ds[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int x = g + n + e;
-              float t2;
-              if (full) {
-                t2 = fmaf(s[x], c2, nl);
-              } else {
-                const int j = j0 + col0 + x;
-                bool ok = (long)j <= jlast;
-                float mv = 0.f;
-                if (ok && mrow) {
-                  mv = h2f(__ldg(reinterpret_cast<const unsigned short*>(mrow) + j));
-                  ok = !(mv == -CUDART_INF_F);
-                }
-                t2 = ok ? fmaf(s[x], c2, mv * kLog2e) + nl : -CUDART_INF_F;
-              }
-              pr[e] = ex2(t2);
-              ds[e] = pr[e] * (dp[x] - dl);
-            }
-            pp[n / 2] = h2_as_u32(__floats2half2_rn(pr[0] * pmul, pr[1] * pmul));
-            pd[n / 2] = h2_as_u32(__floats2half2_rn(ds[0] * lam, ds[1] * lam));
+            const int x = g + n;
+            const float p0 = ex2(t2[x]), p1 = ex2(t2[x + 1]);  // 0 for masked keys and dead rows
+            pp[n / 2] = h2_as_u32(__floats2half2_rn(p0 * pmul, p1 * pmul));
+            pd[n / 2] = h2_as_u32(__floats2half2_rn(p0 * (dp[x] - dl) * lam, p1 * (dp[x + 1] - dl) * lam));
           }
           const uint32_t off = panel_off_u(128, row, col0 + g);
           sts_v4(sP_u + off, pp[0], pp[1], pp[2], pp[3]);
