@@ -24,6 +24,7 @@
 #include <mutex>
 
 #include "../../include/fa_back.h"
+#include "fa_internal.h"
 #include "fa_kernels.cuh"
 
 namespace fab {
@@ -41,30 +42,8 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 static int block_keys(int D, int Dv) { return (D + Dv <= 256) ? 128 : 64; }
 
-static Plan make_plan(int N, int M, int H, int Hkv, int D, int Dv, int nsm) {
-  Plan P;
-  std::memset(&P, 0, sizeof(P));
-  P.G = H / Hkv;
-  P.R = N * P.G;
-  P.nQT = (P.R + 127) / 128;
-  P.BK = block_keys(D, Dv);
-  P.nKT = (M + P.BK - 1) / P.BK;
-  // Split the keys of each row tile: pick the split count whose last wave of CTAs (one per SM)
-  // wastes least, counting a small cost per split for the partial merges.
-  const int base = std::max(1, P.nQT * Hkv);
-  int ns = 1;
-  double best = 1e30;
-  for (int c = 1; c <= std::min(64, std::max(1, P.nKT)); ++c) {
-    const double waves = (double)(((long)base * c + nsm - 1) / nsm);
-    const double cost = waves / c * (1.0 + 0.01 * c);
-    if (cost < best - 1e-12) best = cost, ns = c;
-  }
-  P.kt_per_split = P.nKT > 0 ? (P.nKT + ns - 1) / ns : 1;
-  P.nsplit = P.nKT > 0 ? (P.nKT + P.kt_per_split - 1) / P.kt_per_split : 1;
-  P.nsplit_dq = P.nsplit;
-  const long rows = 2L * N * H + 2L * M * Hkv;
-  P.nblk_stats = (int)std::max(1L, std::min(4L * nsm, (rows + 7) / 8));
-  P.nbv = std::max(1, std::min(256, (M + 255) / 256));
+// Workspace offsets of a plan whose split counts are set.
+static void layout(Plan& P, int Hkv, int D, int Dv) {
   size_t o = 0;
   P.off_stats = o; o = align256(o + sizeof(Stats));
   P.off_rmean = o; o = align256(o + sizeof(float) * (size_t)Hkv * Dv);
@@ -79,6 +58,40 @@ static Plan make_plan(int N, int M, int H, int Hkv, int D, int Dv, int nsm) {
   P.off_bstat = o; o = align256(o + sizeof(float) * 8 * (size_t)P.nblk_stats);
   P.off_vsum = o; o = align256(o + sizeof(float) * (size_t)P.nbv * Hkv * Dv);
   P.total = o;
+}
+
+// Launch plan and workspace layout.  The keys of each row tile are split so that the last wave
+// of CTAs (one per SM) wastes least, counting a small cost per split for the partial merges;
+// among split counts whose workspace fits `ws_cap`, the cheapest is taken (1 if none fits).
+static Plan make_plan(int N, int M, int H, int Hkv, int D, int Dv, int nsm, size_t ws_cap = SIZE_MAX) {
+  Plan P;
+  std::memset(&P, 0, sizeof(P));
+  P.G = H / Hkv;
+  P.R = N * P.G;
+  P.nQT = (P.R + 127) / 128;
+  P.BK = block_keys(D, Dv);
+  P.nKT = (M + P.BK - 1) / P.BK;
+  const long rows = 2L * N * H + 2L * M * Hkv;
+  P.nblk_stats = (int)std::max(1L, std::min(4L * nsm, (rows + 7) / 8));
+  P.nbv = std::max(1, std::min(256, (M + 255) / 256));
+  auto set_split = [&](int ns) {
+    P.kt_per_split = P.nKT > 0 ? (P.nKT + ns - 1) / ns : 1;
+    P.nsplit = P.nKT > 0 ? (P.nKT + P.kt_per_split - 1) / P.kt_per_split : 1;
+    P.nsplit_dq = P.nsplit;
+    layout(P, Hkv, D, Dv);
+  };
+  const int base = std::max(1, P.nQT * Hkv);
+  int ns = 1;
+  double best = 1e30;
+  for (int c = 1; c <= std::min(64, std::max(1, P.nKT)); ++c) {
+    const double waves = (double)(((long)base * c + nsm - 1) / nsm);
+    const double cost = waves / c * (1.0 + 0.01 * c);
+    if (cost < best - 1e-12) {
+      set_split(c);
+      if (c == 1 || P.total <= ws_cap) best = cost, ns = c;
+    }
+  }
+  set_split(ns);
   return P;
 }
 
@@ -285,17 +298,30 @@ extern "C" long fa_row_bytes(int type, int D) {
   return -1;
 }
 
-extern "C" size_t fa_back_workspace_size(int N, int M, int H, int Hkv, int D, int Dv) {
+extern "C" size_t fab_workspace_size_capped(int N, int M, int H, int Hkv, int D, int Dv, size_t ws_cap) {
   if (N < 0 || M < 0 || H <= 0 || Hkv <= 0 || H % Hkv) return 0;
   int nsm = device_sms(nullptr, nullptr);
   if (nsm <= 0) nsm = 152;
-  return make_plan(N, M, H, Hkv, D, Dv, nsm).total;
+  return make_plan(N, M, H, Hkv, D, Dv, nsm, ws_cap).total;
+}
+
+extern "C" size_t fa_back_workspace_size(int N, int M, int H, int Hkv, int D, int Dv) {
+  return fab_workspace_size_capped(N, M, H, Hkv, D, Dv, SIZE_MAX);
 }
 
 extern "C" fa_status fa_back(const float* q, const void* k, int k_type, const void* v, int v_type,
                              const uint16_t* mask, int mask_heads, const float* dO, float scale, int N, int M,
                              int H, int Hkv, int D, int Dv, int causal, float* dQ, float* dK, float* dV,
                              float* lse, float* delta, void* workspace, size_t workspace_bytes, void* stream) {
+  return fab_back_capped(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal, dQ,
+                         dK, dV, lse, delta, workspace, workspace_bytes, stream, SIZE_MAX);
+}
+
+extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, const void* v, int v_type,
+                                     const uint16_t* mask, int mask_heads, const float* dO, float scale, int N,
+                                     int M, int H, int Hkv, int D, int Dv, int causal, float* dQ, float* dK,
+                                     float* dV, float* lse, float* delta, void* workspace, size_t workspace_bytes,
+                                     void* stream, size_t ws_cap) {
   // ---- argument checks (nothing is enqueued on failure)
   if (k_type < FA_F32 || k_type > FA_Q4_0 || v_type < FA_F32 || v_type > FA_Q4_0) return FA_ERR_TYPE;
   if (N < 0 || M < 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || Hkv > 256) return FA_ERR_SHAPE;
@@ -313,7 +339,7 @@ extern "C" fa_status fa_back(const float* q, const void* k, int k_type, const vo
   const int nsm = device_sms(&major, &minor);
   if (nsm <= 0) return FA_ERR_CUDA;
   if (major != 10 || minor != 3) return FA_ERR_DEVICE;
-  const Plan P = make_plan(N, M, H, Hkv, D, Dv, nsm);
+  const Plan P = make_plan(N, M, H, Hkv, D, Dv, nsm, ws_cap);
   if (!workspace || workspace_bytes < P.total) return FA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return FA_ERR_ALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

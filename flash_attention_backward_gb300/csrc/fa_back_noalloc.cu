@@ -10,7 +10,7 @@
 
 #include <mutex>
 
-#include "../../include/fa_back.h"
+#include "fa_internal.h"
 
 namespace {
 
@@ -44,11 +44,12 @@ extern "C" fa_status fa_back_noalloc(const float* q, const void* k, int k_type, 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_DEVICE;
-  const size_t need = fa_back_workspace_size(N, M, H, Hkv, D, Dv);
+  // the plan takes fewer key splits where that keeps the workspace within the scratch
+  const size_t need = fab_workspace_size_capped(N, M, H, Hkv, D, Dv, kScratchBytes);
   if (need > kScratchBytes) return FA_ERR_WORKSPACE;  // larger than the static scratch
   cudaError_t err = cudaSuccess;
   void* scratch = scratch_on(dev, &err);
   if (!scratch) return FA_ERR_CUDA;
-  return fa_back(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal, dQ, dK, dV,
-                 lse, delta, scratch, kScratchBytes, stream);
+  return fab_back_capped(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal, dQ, dK,
+                         dV, lse, delta, scratch, kScratchBytes, stream, kScratchBytes);
 }

@@ -1,0 +1,26 @@
+// Library-internal entry points shared by the translation units of libfa_back.so (hidden: not
+// part of the C ABI in fa_back.h).
+#pragma once
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/fa_back.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+// fa_back_workspace_size() for a plan restricted to at most ws_cap bytes of workspace where a
+// cheaper key split would need more (the plan falls back to fewer key splits).
+__attribute__((visibility("hidden"))) size_t fab_workspace_size_capped(int N, int M, int H, int Hkv, int D, int Dv,
+                                                                       size_t ws_cap);
+
+// fa_back() with the same restriction on the plan.
+__attribute__((visibility("hidden"))) fa_status fab_back_capped(
+    const float* q, const void* k, int k_type, const void* v, int v_type, const uint16_t* mask, int mask_heads,
+    const float* dO, float scale, int N, int M, int H, int Hkv, int D, int Dv, int causal, float* dQ, float* dK,
+    float* dV, float* lse, float* delta, void* workspace, size_t workspace_bytes, void* stream, size_t ws_cap);
+
+#ifdef __cplusplus
+}
+#endif

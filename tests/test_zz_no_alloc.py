@@ -66,3 +66,15 @@ def test_noalloc_rejects_problems_beyond_its_scratch(fb):
     rc = fb.fa_back_noalloc(0x1000, 0x2000, 2, 0x3000, 2, None, 0, 0x4000, 0.0625, N, M, H, Hkv, D, D, 1,
                             0x5000, 0x6000, 0x7000, 0x8000, 0x9000, None)
     assert fb.STATUS[rc] == "FA_ERR_WORKSPACE"
+
+
+@pytest.mark.slow
+def test_noalloc_long_context_within_the_scratch(fb):
+    """The long-context shape: the plan takes fewer key splits so its workspace fits the
+    64 MiB scratch; results agree with fa_back() (whose plan splits more) within tolerance."""
+    p = synth.from_config("4")
+    assert fb.fa_back_workspace_size(p.N, p.M, p.H, p.Hkv, p.D, p.Dv) > (64 << 20)
+    t = synth.device.to_torch(p, "cuda")
+    ref = _with_workspace(fb, p, t)
+    got = _noalloc(fb, p, t)
+    check_components(got, ref, NMSE_TOL)
