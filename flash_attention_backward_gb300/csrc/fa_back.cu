@@ -204,14 +204,23 @@ static cudaError_t set_smem(K kernel, int bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-// Raw K/V staging of the row passes: entry size (keys) and ring depth that fit the budget.
+// Raw K/V staging of the row passes: entry size (keys) and the depths of the K and V rings
+// that fit the budget.  Both rings get the same depth, and bytes left over go to extra K
+// entries (the K rows of the next tile are what the decoders need first).
 static void pick_raw(Params& q, int budget, int BK) {
   const int pair = q.rbk_pad + q.rbv_pad;
-  int ke = std::min(32, BK);
+  // one entry per key tile (fewest waits) when two tiles of both tensors and a third K tile
+  // fit, else 32 keys
+  int ke = (2 * BK * pair + BK * q.rbk_pad <= budget) ? BK : std::min(32, BK);
   while (ke > 1 && 2 * ke * pair > budget) ke >>= 1;
   q.ke = ke;
-  q.raw_depth = std::max(2, std::min(kMaxRawDepth, budget / std::max(1, ke * pair)));
+  int d = std::max(1, std::min(kMaxRawDepth, budget / std::max(1, ke * pair)));
+  q.raw_depth = q.raw_depth_v = d;
+  while (q.raw_depth < kMaxRawDepth && (q.raw_depth + 1) * ke * q.rbk_pad + d * ke * q.rbv_pad <= budget)
+    ++q.raw_depth;
 }
+
+static int raw_bytes(const Params& q) { return q.ke * (q.raw_depth * q.rbk_pad + q.raw_depth_v * q.rbv_pad); }
 
 template <int D, int Dv>
 static cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& tmQ, const CUtensorMap& tmO,
@@ -228,8 +237,8 @@ static cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& 
   for (Params* q : {&pl, &pq})  // TMA destinations must start on 128-byte boundaries
     if ((q->ke * q->rbk_pad) % 128 || (q->ke * q->rbv_pad) % 128) q->raw_bulk = 0;
   // + 1024 for aligning the base, + 64 for the decoders' realigning reads past the last raw row
-  const int sm_l = RL::OFF_RAW + pl.raw_depth * pl.ke * (p.rbk_pad + p.rbv_pad) + 1024 + 64;
-  const int sm_q = RQ::OFF_RAW + pq.raw_depth * pq.ke * (p.rbk_pad + p.rbv_pad) + 1024 + 64;
+  const int sm_l = RL::OFF_RAW + raw_bytes(pl) + 1024 + 64;
+  const int sm_q = RQ::OFF_RAW + raw_bytes(pq) + 1024 + 64;
   if (sm_l > 232448 || sm_q > 232448) return cudaErrorInvalidValue;
   cudaError_t e;
   if ((e = set_smem(k_rows2<D, Dv, BK, 0>, sm_l)) != cudaSuccess) return e;

@@ -77,7 +77,8 @@ struct Params {
   int raw_bulk;        // 1: rows are 16-byte multiples, copied by bulk async copies; 0: 4-byte async copies
   int rbk_pad, rbv_pad;  // raw row strides in shared memory (16-byte multiples)
   int ke;              // keys per raw ring entry
-  int raw_depth;       // ring entries (2..4)
+  int raw_depth;       // entries of the K ring (2..8)
+  int raw_depth_v;     // entries of the V ring (1..8)
   int* err;
 };
 
@@ -180,10 +181,15 @@ __device__ __forceinline__ int group_cols(int type) { return (type == kTypeQ8 ||
 // Decoder thread -> (group, first row, row step).  For q8_0/q4_0 the 8 lanes of a quarter-warp
 // take one column group of 8 consecutive rows, so their 16-byte stores hit 8 distinct bank
 // groups of the swizzled tile; for f16/f32 they take 8 consecutive groups of one row.
+// With 8 blocks per row (D = 256) a warp's four groups are chosen so that their codes start at
+// word offsets of distinct residues mod 4 in the raw row: raw rows are 68 (q8_0) or 36 (q4_0)
+// words apart, so 8 rows x 4 groups then cover all 32 banks and the raw loads are
+// conflict-free (groups {0,1,3,5} and {7,2,4,6}).
 __device__ __forceinline__ void decoder_map(int type, int DD, int NT, int dt, int& g, int& r0, int& rs) {
   const int ng = DD / group_cols(type);
   if (type == kTypeQ8 || type == kTypeQ4) {
-    g = (dt >> 3) % ng;
+    const int gs = (dt >> 3) % ng;
+    g = ng == 8 ? (int)((0x64275310u >> (4 * gs)) & 7u) : gs;
     r0 = (dt & 7) + 8 * (dt / (8 * ng));
   } else {
     g = dt % ng;
@@ -569,15 +575,18 @@ struct Rows2Cfg {
 };
 
 // barrier indices
-constexpr int kMaxRawDepth = 8;  // raw staging entries
+constexpr int kMaxRawDepth = 8;  // raw staging entries per tensor
 enum {
-  B_RAW_FULL = 0,                           // [kMaxRawDepth]
-  B_RAW_EMPTY = B_RAW_FULL + kMaxRawDepth,  // [kMaxRawDepth]
-  B_KV_FULL = B_RAW_EMPTY + kMaxRawDepth,   // [2]
-  B_K_EMPTY = B_KV_FULL + 2,                // [2]
-  B_V_EMPTY = B_K_EMPTY + 2,                // [2]
-  B_S_FULL = B_V_EMPTY + 2,                 // [2]
-  B_S_FREE = B_S_FULL + 2,                  // [2]
+  B_KRAW_FULL = 0,                            // [kMaxRawDepth] raw K entry landed
+  B_KRAW_EMPTY = B_KRAW_FULL + kMaxRawDepth,  // [kMaxRawDepth] raw K entry decoded
+  B_VRAW_FULL = B_KRAW_EMPTY + kMaxRawDepth,  // [kMaxRawDepth]
+  B_VRAW_EMPTY = B_VRAW_FULL + kMaxRawDepth,  // [kMaxRawDepth]
+  B_K_FULL = B_VRAW_EMPTY + kMaxRawDepth,     // [2] K' tile decoded
+  B_V_FULL = B_K_FULL + 2,                    // [2] V' tile decoded
+  B_K_EMPTY = B_V_FULL + 2,                   // [2] K' tile's products done
+  B_V_EMPTY = B_K_EMPTY + 2,                  // [2] V' tile's product done
+  B_S_FULL = B_V_EMPTY + 2,                   // [2]
+  B_S_FREE = B_S_FULL + 2,                    // [2]
   B_DS_FULL = B_S_FREE + 2,
   B_DS_EMPTY,
   B_ACC_FULL,
@@ -585,6 +594,7 @@ enum {
   B_OPS_READY,
   B_COUNT
 };
+static_assert(8 * B_COUNT + 8 <= 512, "barrier area");
 
 struct Waiter {
   volatile int* abort;
@@ -629,17 +639,21 @@ __global__ void __launch_bounds__(512, 1)
     kt_end = min(kt_end, jmax < 0 ? 0 : (int)(jmax / BK) + 1);
   }
   const int ntiles = max(0, kt_end - kt_begin);
-  const int KE = p.ke, EPT = BK / KE, RD = p.raw_depth;
-  const int entry_bytes = KE * (p.rbk_pad + p.rbv_pad);
+  const int KE = p.ke, EPT = BK / KE, RK = p.raw_depth, RV = p.raw_depth_v;
+  const int kent = KE * p.rbk_pad, vent = KE * p.rbv_pad;  // bytes of one K / V ring entry
+  uint8_t* sRawV = sRaw + RK * kent;
 
   if (warp == 1) tmem_alloc(tslot, C::TCOLS);
   if (tid == 0) {
     for (int s = 0; s < kMaxRawDepth; ++s) {
-      mbar_init(&bar[B_RAW_FULL + s], p.raw_bulk ? 1 : 32);
-      mbar_init(&bar[B_RAW_EMPTY + s], C::NDEC);
+      mbar_init(&bar[B_KRAW_FULL + s], p.raw_bulk ? 1 : 32);
+      mbar_init(&bar[B_KRAW_EMPTY + s], C::NDEC);
+      mbar_init(&bar[B_VRAW_FULL + s], p.raw_bulk ? 1 : 32);
+      mbar_init(&bar[B_VRAW_EMPTY + s], C::NDEC);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar[B_KV_FULL + s], C::NDEC);
+      mbar_init(&bar[B_K_FULL + s], C::NDEC);
+      mbar_init(&bar[B_V_FULL + s], C::NDEC);
       mbar_init(&bar[B_K_EMPTY + s], 1);
       mbar_init(&bar[B_V_EMPTY + s], 1);
       mbar_init(&bar[B_S_FULL + s], 1);
@@ -662,6 +676,9 @@ __global__ void __launch_bounds__(512, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
+    // Two rings, one per tensor: entry e of a ring holds keys e*KE .. e*KE+KE-1 of the split.
+    // The K and V queues advance independently (whichever has a free slot), so the K rows of
+    // the next tile stream in while the V ring waits for the current tile's V' decode.
     if (lane == 0 && p.raw_bulk) {
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
@@ -671,40 +688,70 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) tma_load_3d(sQ + c * 128 * 128, &tmQ, &bar[B_Q_FULL], c * 64, r0, hk);
     }
-    int slot = 0, use = 0;  // raw ring position of entry t * EPT + h
-    for (int t = 0; t < ntiles; ++t) {
-      const int j0 = (kt_begin + t) * BK;
-      for (int h = 0; h < EPT; ++h, slot = (slot + 1 == RD) ? 0 : slot + 1, use += (slot == 0)) {
-        if (!wait(&bar[B_RAW_EMPTY + slot], (use & 1) ^ 1)) break;
-        const int ja = j0 + h * KE;
-        const int nv = max(0, min(KE, p.M - ja));
-        uint8_t* dk = sRaw + slot * entry_bytes;
-        uint8_t* dv = dk + KE * p.rbk_pad;
-        if (p.raw_bulk) {
-          // one TMA box per tensor: KE rows of this KV head (dims: row bytes, head, key)
-          if (lane == 0) {
-            if (nv > 0) {
-              mbar_arrive_expect_tx(&bar[B_RAW_FULL + slot], (uint32_t)(KE * (p.rbk + p.rbv)));
-              tma_load_3d(dk, &tmK, &bar[B_RAW_FULL + slot], 0, hk, ja);
-              tma_load_3d(dv, &tmV, &bar[B_RAW_FULL + slot], 0, hk, ja);
-            } else {
-              mbar_arrive(&bar[B_RAW_FULL + slot]);
-            }
+    const int tot = ntiles * EPT;
+    int ek = 0, ev = 0, sk = 0, uk = 0, sv = 0, uv = 0;
+    uint64_t t0 = globaltimer_ns();
+    // one entry of one tensor into its ring slot (bulk: one TMA box of KE rows of this KV head)
+    auto load_entry = [&](bool isv, int e, int slot) {
+      const int ja = kt_begin * BK + e * KE;
+      const int nv = max(0, min(KE, p.M - ja));
+      uint64_t* fb = &bar[(isv ? B_VRAW_FULL : B_KRAW_FULL) + slot];
+      uint8_t* dst = isv ? sRawV + slot * vent : sRaw + slot * kent;
+      const int rb = isv ? p.rbv : p.rbk, rbp = isv ? p.rbv_pad : p.rbk_pad;
+      if (p.raw_bulk) {
+        if (lane == 0) {
+          if (nv > 0) {
+            mbar_arrive_expect_tx(fb, (uint32_t)(KE * rb));
+            tma_load_3d(dst, isv ? &tmV : &tmK, fb, 0, hk, ja);
+          } else {
+            mbar_arrive(fb);
           }
-        } else {
-          const int wk = p.rbk / 4, wv = p.rbv / 4;
-          for (int x = lane; x < nv * wk; x += 32) {
-            const int rr = x / wk, c = x % wk;
-            cp_async4(dk + rr * p.rbk_pad + 4 * c, p.k + ((size_t)(ja + rr) * p.Hkv + hk) * p.rbk + 4 * c);
-          }
-          for (int x = lane; x < nv * wv; x += 32) {
-            const int rr = x / wv, c = x % wv;
-            cp_async4(dv + rr * p.rbv_pad + 4 * c, p.v + ((size_t)(ja + rr) * p.Hkv + hk) * p.rbv + 4 * c);
-          }
-          cp_async_arrive(&bar[B_RAW_FULL + slot]);
         }
+      } else {
+        const int w = rb / 4;
+        const uint8_t* src = isv ? p.v : p.k;
+        for (int x = lane; x < nv * w; x += 32) {
+          const int rr = x / w, c = x % w;
+          cp_async4(dst + rr * rbp + 4 * c, src + ((size_t)(ja + rr) * p.Hkv + hk) * rb + 4 * c);
+        }
+        cp_async_arrive(fb);
       }
-      if (*s_abort) break;
+    };
+    while (ek < tot || ev < tot) {
+      bool moved = false;
+      // the warp takes each decision together (lane 0 polls, the others follow)
+      int go_k = 0, go_v = 0;
+      if (lane == 0) {
+        go_k = ek < tot && mbar_try_wait(&bar[B_KRAW_EMPTY + sk], (uk & 1) ^ 1);
+        go_v = ev < tot && mbar_try_wait(&bar[B_VRAW_EMPTY + sv], (uv & 1) ^ 1);
+      }
+      go_k = __shfl_sync(0xffffffffu, go_k, 0);
+      go_v = __shfl_sync(0xffffffffu, go_v, 0);
+      if (go_v) {
+        load_entry(true, ev, sv);
+        ++ev;
+        if (++sv == RV) sv = 0, ++uv;
+        moved = true;
+      }
+      if (go_k) {
+        load_entry(false, ek, sk);
+        ++ek;
+        if (++sk == RK) sk = 0, ++uk;
+        moved = true;
+      }
+      if (moved) {
+        t0 = globaltimer_ns();
+      } else {
+        if (*s_abort) break;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          if (lane == 0) {
+            *s_abort = 1;
+            record_error(p.err, kErrTimeout);
+          }
+          break;
+        }
+        __nanosleep(64);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -713,12 +760,11 @@ __global__ void __launch_bounds__(512, 1)
       constexpr uint32_t ID_DQ = idesc_f16(128, D, false, true);
       const uint32_t tQ = tbase + C::T_Q, tO = tbase + C::T_O, tAcc = tbase + C::T_ACC;
       const bool ok = (MODE == 0 || wait(&bar[B_Q_FULL], 0)) && wait(&bar[B_OPS_READY], 0);
-      // S(t) = Q K'^T and dP(t) = dO V'^T into the tensor-memory slot of tile t
-      auto issue_sdp = [&](int t) {
-        const int ks = t & 1, vs = MODE ? 0 : (t & 1), sl = t % C::NSLOT;
-        const uint32_t tS = tbase + C::T_S + 2 * BK * sl, tP = tS + BK;
+      // S(t) = Q K'^T into the tensor-memory slot of tile t
+      auto issue_s = [&](int t) {
+        const uint32_t tS = tbase + C::T_S + 2 * BK * (t % C::NSLOT);
         tc_fence_after();
-        const uint32_t bk = smem_u32(sK + ks * C::KB), bv = smem_u32(sV + vs * C::VB);
+        const uint32_t bk = smem_u32(sK + (t & 1) * C::KB);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint64_t bd = sdesc_sw128(bk + (k / 4) * (BK * 128) + (k % 4) * 32, 16, 1024);
@@ -727,13 +773,20 @@ __global__ void __launch_bounds__(512, 1)
           else
             mma_f16_tmem_a(tS, tQ + k * 8, bd, ID_S, k > 0);
         }
+        if (MODE == 0) mma_commit(&bar[B_K_EMPTY + (t & 1)]);  // K' of tile t is not read again
+      };
+      // dP(t) = dO V'^T next to S(t); the slot is then complete
+      auto issue_dp = [&](int t) {
+        const int vs = MODE ? 0 : (t & 1), sl = t % C::NSLOT;
+        const uint32_t tP = tbase + C::T_S + 2 * BK * sl + BK;
+        tc_fence_after();
+        const uint32_t bv = smem_u32(sV + vs * C::VB);
 #pragma unroll
         for (int k = 0; k < Dv / 16; ++k)
           mma_f16_tmem_a(tP, tO + k * 8, sdesc_sw128(bv + (k / 4) * (BK * 128) + (k % 4) * 32, 16, 1024), ID_S,
                          k > 0);
         mma_commit(&bar[B_S_FULL + sl]);
         mma_commit(&bar[B_V_EMPTY + vs]);
-        if (MODE == 0) mma_commit(&bar[B_K_EMPTY + ks]);
       };
       // dQ += dS(t) K'(t)
       auto issue_dq = [&](int t) {
@@ -752,23 +805,32 @@ __global__ void __launch_bounds__(512, 1)
       };
       if (MODE == 0) {
         for (int t = 0; ok && t < ntiles; ++t) {
-          const int sl = t % C::NSLOT, su = t / C::NSLOT;
-          if (!wait(&bar[B_KV_FULL + (t & 1)], (t >> 1) & 1) || !wait(&bar[B_S_FREE + sl], (su & 1) ^ 1)) break;
-          issue_sdp(t);
+          const int su = t / C::NSLOT;
+          if (!wait(&bar[B_K_FULL + (t & 1)], (t >> 1) & 1) || !wait(&bar[B_S_FREE + t % C::NSLOT], (su & 1) ^ 1))
+            break;
+          issue_s(t);
+          if (!wait(&bar[B_V_FULL + (t & 1)], (t >> 1) & 1)) break;
+          issue_dp(t);
         }
       } else if (ok) {
-        // Issue whichever product is ready, dQ first: it frees the K' stage the decoders need next.
-        int ns = 0, nd = 0;
+        // Issue whatever is ready, dQ first (it frees the dS panel and a K' stage), then dP
+        // (it frees the single V' stage), then S of the next tile.
+        int ns = 0, np = 0, nd = 0;
         uint64_t t0 = globaltimer_ns();
         while (nd < ntiles) {
-          if (nd < ns && mbar_try_wait(&bar[B_DS_FULL], nd & 1)) {
+          if (nd < np && mbar_try_wait(&bar[B_DS_FULL], nd & 1)) {
             issue_dq(nd++);
             t0 = globaltimer_ns();
             continue;
           }
-          if (ns < ntiles && mbar_try_wait(&bar[B_KV_FULL + (ns & 1)], (ns >> 1) & 1) &&
+          if (np < ns && mbar_try_wait(&bar[B_V_FULL], np & 1)) {
+            issue_dp(np++);
+            t0 = globaltimer_ns();
+            continue;
+          }
+          if (ns < ntiles && ns == np && mbar_try_wait(&bar[B_K_FULL + (ns & 1)], (ns >> 1) & 1) &&
               mbar_try_wait(&bar[B_S_FREE], (ns & 1) ^ 1)) {
-            issue_sdp(ns++);
+            issue_s(ns++);
             t0 = globaltimer_ns();
             continue;
           }
@@ -783,36 +845,47 @@ __global__ void __launch_bounds__(512, 1)
     }
   } else if (warp >= 4 + C::NSOFT || warp == 2 || warp == 3) {
     // ------------------------------------------------------------------ decoders
+    // Per tile: the K' rows of all its entries, then (once the previous dP has released the
+    // V' stage) the V' rows.
     constexpr int NDT = C::NDEC * 32;
     static_assert(NDT % 64 == 0, "decoder_map needs a multiple of 8 column groups of 8 lanes");
     const int dt = (warp < 4 ? warp - 2 : warp - (4 + C::NSOFT) + 2) * 32 + lane;
     __half2 vsh[16];
     load_group_shift<Dv, NDT>(p.rsh + (size_t)hk * Dv, p.v_type, dt, vsh);
-    int slot = 0, use = 0;  // raw ring position of entry t * EPT + h
-    for (int t = 0; t < ntiles; ++t) {
+    int sk = 0, uk = 0, sv = 0, uv = 0;  // ring positions
+    bool ok = true;
+    for (int t = 0; ok && t < ntiles; ++t) {
       const int ks = t & 1, vs = MODE ? 0 : (t & 1);
-      if (!wait(&bar[B_K_EMPTY + ks], ((t >> 1) & 1) ^ 1)) break;
-      if (!wait(&bar[B_V_EMPTY + vs], MODE ? ((t & 1) ^ 1) : (((t >> 1) & 1) ^ 1))) break;
-      const uint32_t kd = smem_u32(sK + ks * C::KB), vd = smem_u32(sV + vs * C::VB);
       const int j0 = (kt_begin + t) * BK;
-      bool ok = true;
-      for (int h = 0; h < EPT; ++h, slot = (slot + 1 == RD) ? 0 : slot + 1, use += (slot == 0)) {
-        if (!wait(&bar[B_RAW_FULL + slot], use & 1)) {
-          ok = false;
-          break;
-        }
-        const uint32_t rk = smem_u32(sRaw) + slot * entry_bytes;
-        const uint32_t rv = rk + KE * p.rbk_pad;
+      if (!wait(&bar[B_K_EMPTY + ks], ((t >> 1) & 1) ^ 1)) break;
+      const uint32_t kd = smem_u32(sK + ks * C::KB), vd = smem_u32(sV + vs * C::VB);
+      for (int h = 0; h < EPT; ++h) {
+        if (!(ok = wait(&bar[B_KRAW_FULL + sk], uk & 1))) break;
         const int nv = max(0, min(KE, p.M - (j0 + h * KE)));
-        decode_rows<D, BK, NDT, false>(p.k_type, rk, p.rbk_pad, KE, nv, h * KE, kd, st.sK, vsh, dt);
-        decode_rows<Dv, BK, NDT, true>(p.v_type, rv, p.rbv_pad, KE, nv, h * KE, vd, st.sV, vsh, dt);
+        decode_rows<D, BK, NDT, false>(p.k_type, smem_u32(sRaw) + sk * kent, p.rbk_pad, KE, nv, h * KE, kd, st.sK,
+                                       vsh, dt);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[B_RAW_EMPTY + slot]);  // raw entry consumed
+        if (lane == 0) mbar_arrive(&bar[B_KRAW_EMPTY + sk]);  // raw entry consumed
+        if (++sk == RK) sk = 0, ++uk;
       }
       if (!ok) break;
       fence_proxy_async_smem();  // the tile's binary16 stores, visible to the tensor cores
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[B_KV_FULL + ks]);
+      if (lane == 0) mbar_arrive(&bar[B_K_FULL + ks]);
+      if (!wait(&bar[B_V_EMPTY + vs], MODE ? ((t & 1) ^ 1) : (((t >> 1) & 1) ^ 1))) break;
+      for (int h = 0; h < EPT; ++h) {
+        if (!(ok = wait(&bar[B_VRAW_FULL + sv], uv & 1))) break;
+        const int nv = max(0, min(KE, p.M - (j0 + h * KE)));
+        decode_rows<Dv, BK, NDT, true>(p.v_type, smem_u32(sRawV) + sv * vent, p.rbv_pad, KE, nv, h * KE, vd,
+                                       st.sV, vsh, dt);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[B_VRAW_EMPTY + sv]);
+        if (++sv == RV) sv = 0, ++uv;
+      }
+      if (!ok) break;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[B_V_FULL + vs]);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax
