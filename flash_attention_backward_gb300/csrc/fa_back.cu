@@ -42,6 +42,10 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 static int block_keys(int D, int Dv) { return (D + Dv <= 256) ? 128 : 64; }
 
+// Key tile of the LSE pass: 128 keys for every head size (its operands live in tensor memory,
+// so N = 128 products fit; they run at twice the rate per flop of N = 64 products).
+constexpr int kBKLse = 128;
+
 // Workspace offsets of a plan whose split counts are set.
 static void layout(Plan& P, int Hkv, int D, int Dv) {
   size_t o = 0;
@@ -76,6 +80,8 @@ static Plan make_plan(int N, int M, int H, int Hkv, int D, int Dv, int nsm, size
   P.nbv = std::max(1, std::min(256, (M + 255) / 256));
   auto set_split = [&](int ns) {
     P.kt_per_split = P.nKT > 0 ? (P.nKT + ns - 1) / ns : 1;
+    const int r = kBKLse / P.BK;  // whole LSE-pass tiles per split
+    P.kt_per_split = (P.kt_per_split + r - 1) / r * r;
     P.nsplit = P.nKT > 0 ? (P.nKT + P.kt_per_split - 1) / P.kt_per_split : 1;
     P.nsplit_dq = P.nsplit;
     layout(P, Hkv, D, Dv);
@@ -209,9 +215,14 @@ static cudaError_t set_smem(K kernel, int bytes) {
 // entries (the K rows of the next tile are what the decoders need first).
 static void pick_raw(Params& q, int budget, int BK) {
   const int pair = q.rbk_pad + q.rbv_pad;
-  // one entry per key tile (fewest waits) when two tiles of both tensors and a third K tile
-  // fit, else 32 keys
-  int ke = (2 * BK * pair + BK * q.rbk_pad <= budget) ? BK : std::min(32, BK);
+  // the largest entry (fewest waits) of which two of both tensors and a third K entry fit,
+  // else 32 keys
+  int ke = std::min(32, BK);
+  for (int c = BK; c > 32; c >>= 1)
+    if (2 * c * pair + c * q.rbk_pad <= budget) {
+      ke = c;
+      break;
+    }
   while (ke > 1 && 2 * ke * pair > budget) ke >>= 1;
   q.ke = ke;
   int d = std::max(1, std::min(kMaxRawDepth, budget / std::max(1, ke * pair)));
@@ -226,13 +237,18 @@ template <int D, int Dv>
 static cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& tmQ, const CUtensorMap& tmO,
                              cudaStream_t s, CallRec& rec) {
   constexpr int BK = (D + Dv <= 256) ? 128 : 64;
-  using RL = Rows2Cfg<D, Dv, BK, 0>;
+  constexpr int BKL = kBKLse;  // LSE-pass key tile
+  static_assert(BKL % BK == 0, "LSE tiles cover whole gradient-pass tiles");
+  using RL = Rows2Cfg<D, Dv, BKL, 0>;
   using RQ = Rows2Cfg<D, Dv, BK, 1>;
   using CC = Cols2Cfg<D, Dv, BK>;
   static_assert(RL::RAW_BUDGET > 0 && RQ::RAW_BUDGET > 0 && CC::SMEM <= 232448, "shared memory budget");
   static_assert(RL::TCOLS <= 512 && RQ::TCOLS <= 512 && CC::TCOLS <= 512, "tensor memory budget");
   Params pl = p, pq = p;
-  pick_raw(pl, RL::RAW_BUDGET, BK);
+  // the LSE pass walks the same key splits in BKL-key tiles (split sizes are multiples of BKL)
+  pl.nKT = (p.M + BKL - 1) / BKL;
+  pl.kt_per_split = p.kt_per_split / (BKL / BK);
+  pick_raw(pl, RL::RAW_BUDGET, BKL);
   pick_raw(pq, RQ::RAW_BUDGET, BK);
   for (Params* q : {&pl, &pq})  // TMA destinations must start on 128-byte boundaries
     if ((q->ke * q->rbk_pad) % 128 || (q->ke * q->rbv_pad) % 128) q->raw_bulk = 0;
@@ -241,7 +257,7 @@ static cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& 
   const int sm_q = RQ::OFF_RAW + raw_bytes(pq) + 1024 + 64;
   if (sm_l > 232448 || sm_q > 232448) return cudaErrorInvalidValue;
   cudaError_t e;
-  if ((e = set_smem(k_rows2<D, Dv, BK, 0>, sm_l)) != cudaSuccess) return e;
+  if ((e = set_smem(k_rows2<D, Dv, BKL, 0>, sm_l)) != cudaSuccess) return e;
   if ((e = set_smem(k_rows2<D, Dv, BK, 1>, sm_q)) != cudaSuccess) return e;
   if ((e = set_smem(k_cols2<D, Dv, BK>, CC::SMEM)) != cudaSuccess) return e;
 
@@ -254,7 +270,7 @@ static cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& 
       return cudaErrorInvalidValue;
   }
   dim3 grows(P.nQT, p.Hkv, P.nsplit);
-  k_rows2<D, Dv, BK, 0><<<grows, 512, sm_l, s>>>(tmQ, tkl, tvl, pl);
+  k_rows2<D, Dv, BKL, 0><<<grows, 512, sm_l, s>>>(tmQ, tkl, tvl, pl);
   rec.mark(KS_ROWS_LSE);
   k_lse_merge<<<(unsigned)(((long)p.Hkv * P.R + 255) / 256), 256, 0, s>>>(p);
   rec.mark(KS_MERGE);

@@ -545,7 +545,10 @@ __global__ void __launch_bounds__(256) k_convert(Params p) {
 template <int D, int Dv, int BK, int MODE>
 struct Rows2Cfg {
   static constexpr int NT = 512;
-  static constexpr int KSTAGES = 2, VSTAGES = MODE ? 1 : 2;
+  // binary16 K'/V' tile stages: two each where they fit beside the raw ring, else one (the LSE
+  // pass at 128 keys x D = 256); the dQ pass keeps one V' stage (its Q tile lives here too)
+  static constexpr int KSTAGES = (MODE == 0 && BK * (D + Dv) * 2 * 2 > 160 * 1024) ? 1 : 2;
+  static constexpr int VSTAGES = (MODE == 1 || BK * (D + Dv) * 2 * 2 > 160 * 1024) ? 1 : 2;
   static constexpr int QB = MODE ? 128 * D * 2 : 0;
   static constexpr int KB = BK * D * 2, VB = BK * Dv * 2;
   static constexpr int SB = MODE ? 128 * BK * 2 : 0;
@@ -764,7 +767,7 @@ __global__ void __launch_bounds__(512, 1)
       auto issue_s = [&](int t) {
         const uint32_t tS = tbase + C::T_S + 2 * BK * (t % C::NSLOT);
         tc_fence_after();
-        const uint32_t bk = smem_u32(sK + (t & 1) * C::KB);
+        const uint32_t bk = smem_u32(sK + (t % C::KSTAGES) * C::KB);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint64_t bd = sdesc_sw128(bk + (k / 4) * (BK * 128) + (k % 4) * 32, 16, 1024);
@@ -773,11 +776,11 @@ __global__ void __launch_bounds__(512, 1)
           else
             mma_f16_tmem_a(tS, tQ + k * 8, bd, ID_S, k > 0);
         }
-        if (MODE == 0) mma_commit(&bar[B_K_EMPTY + (t & 1)]);  // K' of tile t is not read again
+        if (MODE == 0) mma_commit(&bar[B_K_EMPTY + t % C::KSTAGES]);  // K' of tile t is not read again
       };
       // dP(t) = dO V'^T next to S(t); the slot is then complete
       auto issue_dp = [&](int t) {
-        const int vs = MODE ? 0 : (t & 1), sl = t % C::NSLOT;
+        const int vs = t % C::VSTAGES, sl = t % C::NSLOT;
         const uint32_t tP = tbase + C::T_S + 2 * BK * sl + BK;
         tc_fence_after();
         const uint32_t bv = smem_u32(sV + vs * C::VB);
@@ -791,7 +794,7 @@ __global__ void __launch_bounds__(512, 1)
       // dQ += dS(t) K'(t)
       auto issue_dq = [&](int t) {
         tc_fence_after();
-        const uint32_t kp = smem_u32(sK + (t & 1) * C::KB);
+        const uint32_t kp = smem_u32(sK + (t % C::KSTAGES) * C::KB);
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k)
           mma_f16(tAcc, sdesc_sw128(smem_u32(sS) + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024),
@@ -800,16 +803,17 @@ __global__ void __launch_bounds__(512, 1)
           mma_commit(&bar[B_ACC_FULL]);
         } else {
           mma_commit(&bar[B_DS_EMPTY]);
-          mma_commit(&bar[B_K_EMPTY + (t & 1)]);
+          mma_commit(&bar[B_K_EMPTY + t % C::KSTAGES]);
         }
       };
       if (MODE == 0) {
         for (int t = 0; ok && t < ntiles; ++t) {
           const int su = t / C::NSLOT;
-          if (!wait(&bar[B_K_FULL + (t & 1)], (t >> 1) & 1) || !wait(&bar[B_S_FREE + t % C::NSLOT], (su & 1) ^ 1))
+          if (!wait(&bar[B_K_FULL + t % C::KSTAGES], (t / C::KSTAGES) & 1) ||
+              !wait(&bar[B_S_FREE + t % C::NSLOT], (su & 1) ^ 1))
             break;
           issue_s(t);
-          if (!wait(&bar[B_V_FULL + (t & 1)], (t >> 1) & 1)) break;
+          if (!wait(&bar[B_V_FULL + t % C::VSTAGES], (t / C::VSTAGES) & 1)) break;
           issue_dp(t);
         }
       } else if (ok) {
@@ -823,12 +827,12 @@ __global__ void __launch_bounds__(512, 1)
             t0 = globaltimer_ns();
             continue;
           }
-          if (np < ns && mbar_try_wait(&bar[B_V_FULL], np & 1)) {
+          if (np < ns && mbar_try_wait(&bar[B_V_FULL + np % C::VSTAGES], (np / C::VSTAGES) & 1)) {
             issue_dp(np++);
             t0 = globaltimer_ns();
             continue;
           }
-          if (ns < ntiles && ns == np && mbar_try_wait(&bar[B_K_FULL + (ns & 1)], (ns >> 1) & 1) &&
+          if (ns < ntiles && ns == np && mbar_try_wait(&bar[B_K_FULL + ns % C::KSTAGES], (ns / C::KSTAGES) & 1) &&
               mbar_try_wait(&bar[B_S_FREE], (ns & 1) ^ 1)) {
             issue_s(ns++);
             t0 = globaltimer_ns();
@@ -855,9 +859,9 @@ __global__ void __launch_bounds__(512, 1)
     int sk = 0, uk = 0, sv = 0, uv = 0;  // ring positions
     bool ok = true;
     for (int t = 0; ok && t < ntiles; ++t) {
-      const int ks = t & 1, vs = MODE ? 0 : (t & 1);
+      const int ks = t % C::KSTAGES, vs = t % C::VSTAGES;
       const int j0 = (kt_begin + t) * BK;
-      if (!wait(&bar[B_K_EMPTY + ks], ((t >> 1) & 1) ^ 1)) break;
+      if (!wait(&bar[B_K_EMPTY + ks], ((t / C::KSTAGES) & 1) ^ 1)) break;
       const uint32_t kd = smem_u32(sK + ks * C::KB), vd = smem_u32(sV + vs * C::VB);
       for (int h = 0; h < EPT; ++h) {
         if (!(ok = wait(&bar[B_KRAW_FULL + sk], uk & 1))) break;
@@ -872,7 +876,7 @@ __global__ void __launch_bounds__(512, 1)
       fence_proxy_async_smem();  // the tile's binary16 stores, visible to the tensor cores
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[B_K_FULL + ks]);
-      if (!wait(&bar[B_V_EMPTY + vs], MODE ? ((t & 1) ^ 1) : (((t >> 1) & 1) ^ 1))) break;
+      if (!wait(&bar[B_V_EMPTY + vs], ((t / C::VSTAGES) & 1) ^ 1)) break;
       for (int h = 0; h < EPT; ++h) {
         if (!(ok = wait(&bar[B_VRAW_FULL + sv], uv & 1))) break;
         const int nv = max(0, min(KE, p.M - (j0 + h * KE)));
