@@ -84,27 +84,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// try_wait with a suspend-time hint: a thread whose phase is still open sleeps (up to `hint_ns`)
-// until the phase completes instead of spinning, leaving issue slots to the working warps.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-
-// Waits for the phase with the given parity to complete; gives up after `limit_ns`.
+// Waits for the phase with the given parity to complete; gives up after `limit_ns`.  (A
+// suspend-time hint on try_wait measured slower here: the woken thread resumes late.)
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-    if ((it & 15u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
