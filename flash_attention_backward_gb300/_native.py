@@ -43,6 +43,8 @@ def lib():
     L.fa_back_status_string.argtypes = [i]
     L.fa_back_noalloc.restype = i
     L.fa_back_noalloc.argtypes = [vp, vp, i, vp, i, vp, i, vp, f, i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp]
+    L.fa_back_selftest_timeout.restype = i
+    L.fa_back_selftest_timeout.argtypes = [ctypes.c_ulonglong, vp]
     L.fa_back_profile.restype = i
     L.fa_back_profile.argtypes = [i]
     L.fa_back_profile_read.restype = i
@@ -95,3 +97,7 @@ def fa_back_noalloc(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, 
     """fa_back with the library's static scratch instead of a caller workspace (see the header)."""
     return int(lib().fa_back_noalloc(q, k, k_type, v, v_type, mask, mask_heads, dO, float(scale), N, M, H, Hkv,
                                      D, Dv, int(causal), dQ, dK, dV, lse, delta, stream))
+
+
+def fa_back_selftest_timeout(limit_ns: int, stream=None) -> int:
+    return int(lib().fa_back_selftest_timeout(limit_ns, stream))

@@ -433,6 +433,14 @@ extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, 
   return pick(D, Dv)(p, P, tmQ, tmO, s, rec) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+extern "C" fa_status fa_back_selftest_timeout(unsigned long long limit_ns, void* stream) {
+  if (limit_ns == 0 || limit_ns > kWaitLimitNs) return FA_ERR_SHAPE;
+  int* errp = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&errp), g_err) != cudaSuccess) return FA_ERR_CUDA;
+  k_wait_selftest<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(errp, limit_ns);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 extern "C" fa_status fa_back_get_error(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
   int v = 0, zero = 0;

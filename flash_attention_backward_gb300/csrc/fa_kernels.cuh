@@ -1419,6 +1419,17 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
+// Failure-detection self-test: one thread waits on an mbarrier nothing arrives on, gives up
+// after limit_ns (the path every bounded wait of the backward takes) and records the timeout.
+__global__ void k_wait_selftest(int* err, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait_bounded(&bar, 0, limit_ns)) record_error(err, kErrTimeout);
+  }
+}
+
 // Fill kernel for degenerate shapes (a value into n floats).
 __global__ void k_fill(float* x, long n, float v) {
   const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;

@@ -138,6 +138,16 @@ fa_status fa_back_noalloc(const float* q, const void* k, int k_type, const void*
                           int M, int H, int Hkv, int D, int Dv, int causal, float* dQ, float* dK,
                           float* dV, float* lse, float* delta, void* stream);
 
+/*
+ * Exercises the failure-detection path of the bounded waits without a fault: enqueues one
+ * kernel on `stream` whose thread waits up to `limit_ns` nanoseconds (0 < limit_ns <= 2 s) on
+ * an mbarrier that nothing completes, records FA_ERR_TIMEOUT in the device error word exactly as
+ * the backward's kernels do when a wait runs out, and returns.  The context stays usable;
+ * fa_back_get_error() then reports FA_ERR_TIMEOUT once (and clears it).  Returns FA_OK when
+ * the kernel was enqueued, FA_ERR_SHAPE for a limit outside that range.
+ */
+fa_status fa_back_selftest_timeout(unsigned long long limit_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,8 +26,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
-        ["fa_back", "fa_back_get_error", "fa_back_noalloc", "fa_back_profile", "fa_back_profile_read", "fa_back_status_string",
-         "fa_back_workspace_size", "fa_row_bytes"])
+        ["fa_back", "fa_back_get_error", "fa_back_noalloc", "fa_back_profile", "fa_back_profile_read",
+         "fa_back_selftest_timeout", "fa_back_status_string", "fa_back_workspace_size", "fa_row_bytes"])
 
 
 def test_every_declared_symbol_is_exported(L):
