@@ -76,7 +76,7 @@ static Plan make_plan(int N, int M, int H, int Hkv, int D, int Dv, int nsm, size
   P.BK = block_keys(D, Dv);
   P.nKT = (M + P.BK - 1) / P.BK;
   const long rows = 2L * N * H + 2L * M * Hkv;
-  P.nblk_stats = (int)std::max(1L, std::min(4L * nsm, (rows + 7) / 8));
+  P.nblk_stats = (int)std::max(1L, std::min(8L * nsm, (rows + 7) / 8));
   P.nbv = std::max(1, std::min(256, (M + 255) / 256));
   auto set_split = [&](int ns) {
     P.kt_per_split = P.nKT > 0 ? (P.nKT + ns - 1) / ns : 1;
@@ -423,9 +423,9 @@ extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, 
   rec.begin(s);
   k_row_stats<<<P.nblk_stats, 256, 0, s>>>(p);
   rec.mark(KS_STATS);
-  k_vsum<<<dim3((Hkv * Dv + 255) / 256, P.nbv), 256, 0, s>>>(p);
+  k_vsum<<<(unsigned)((P.nbv * Hkv + 7) / 8), 256, 0, s>>>(p);
   rec.mark(KS_VSUM);
-  k_finalize<<<1, 256, 0, s>>>(p);
+  k_finalize<<<1, 1024, 0, s>>>(p);
   rec.mark(KS_FINAL);
   k_convert<<<(unsigned)std::min<long>(((long)N * H + 7) / 8, 8L * nsm), 256, 0, s>>>(p);
   rec.mark(KS_CONVERT);

@@ -363,7 +363,43 @@ __device__ __forceinline__ float warp_sum(float x) {
 // ------------------------------------------------------------------------------------------------
 // statistics and packing
 
-// One warp per row of Q, dO, K^ or V^: max |x| and max squared row norm, reduced per block.
+// Values c0 .. c0+7 of a raw cache row, decoded exactly to f32 (code * d, or the stored value).
+__device__ __forceinline__ void decode8_f(const uint8_t* row, int type, int c0, float* x) {
+  if (type == kTypeQ8 || type == kTypeQ4) {
+    const bool q8 = type == kTypeQ8;
+    const uint8_t* b = row + (q8 ? 34 : 18) * (c0 >> 5);
+    const float d = h2f(__ldg(reinterpret_cast<const unsigned short*>(b)));
+    const int o = c0 & 31;
+    const uint16_t* cp = reinterpret_cast<const uint16_t*>(b + 2 + (q8 ? o : (o & 15)));
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t pr = __ldg(cp + e);
+      if (q8) {
+        x[2 * e] = (float)(int8_t)(pr & 0xffu) * d;
+        x[2 * e + 1] = (float)(int8_t)(pr >> 8) * d;
+      } else {
+        const int sh = o >= 16 ? 4 : 0;
+        x[2 * e] = (float)((int)((pr >> sh) & 15u) - 8) * d;
+        x[2 * e + 1] = (float)((int)((pr >> (8 + sh)) & 15u) - 8) * d;
+      }
+    }
+  } else if (type == kTypeF16) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + 2 * c0));
+    const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __half22float2(u32_as_h2(in[e]));
+      x[2 * e] = f.x, x[2 * e + 1] = f.y;
+    }
+  } else {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(row + 4 * c0));
+    const float4 c = __ldg(reinterpret_cast<const float4*>(row + 4 * c0 + 16));
+    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = c.x, x[5] = c.y, x[6] = c.z, x[7] = c.w;
+  }
+}
+
+// One warp per row of Q, dO, K^ or V^ (lane = 8 consecutive values): max |x| and max squared
+// row norm, reduced per block.
 __global__ void __launch_bounds__(256) k_row_stats(Params p) {
   __shared__ float red[8][4][2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -379,14 +415,15 @@ __global__ void __launch_bounds__(256) k_row_stats(Params p) {
     else t = 3, r = rw - 2 * nQ - nK;
     const int DD = (t == 0 || t == 2) ? p.D : p.Dv;
     float am = 0.f, ss = 0.f;
-    for (int c = lane; c < DD; c += 32) {
-      float x;
-      if (t == 0) x = __ldg(p.q + r * p.D + c);
-      else if (t == 1) x = __ldg(p.dO + r * p.Dv + c);
-      else if (t == 2) x = decode_elem(p.k + r * p.rbk, p.k_type, c);
-      else x = decode_elem(p.v + r * p.rbv, p.v_type, c);
-      am = fmaxf(am, fabsf(x));
-      ss = fmaf(x, x, ss);
+    const int c0 = lane * 8;
+    if (c0 < DD) {
+      float x[8];
+      if (t == 0) decode8_f(reinterpret_cast<const uint8_t*>(p.q + r * p.D), kTypeF32, c0, x);
+      else if (t == 1) decode8_f(reinterpret_cast<const uint8_t*>(p.dO + r * p.Dv), kTypeF32, c0, x);
+      else if (t == 2) decode8_f(p.k + r * p.rbk, p.k_type, c0, x);
+      else decode8_f(p.v + r * p.rbv, p.v_type, c0, x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(x[e])), ss = fmaf(x[e], x[e], ss);
     }
     am = warp_max(am);
     ss = warp_sum(ss);
@@ -404,16 +441,28 @@ __global__ void __launch_bounds__(256) k_row_stats(Params p) {
   }
 }
 
-// Column sums of V^ over a chunk of keys; thread = (hk, c); keys summed in increasing order.
+// Column sums of V^ over one chunk of keys: warp = (chunk, hk), lane = 8 consecutive columns;
+// keys summed in increasing order.
 __global__ void __launch_bounds__(256) k_vsum(Params p) {
-  const int idx = blockIdx.x * 256 + threadIdx.x;
-  if (idx >= p.Hkv * p.Dv) return;
-  const int hk = idx / p.Dv, c = idx % p.Dv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wid = blockIdx.x * 8 + warp;
+  if (wid >= p.nbv * p.Hkv) return;
+  const int chunk = wid / p.Hkv, hk = wid % p.Hkv;
+  const int c0 = lane * 8;
+  if (c0 >= p.Dv) return;
   const long per = ((long)p.M + p.nbv - 1) / p.nbv;
-  const long ja = (long)blockIdx.y * per, jb = min((long)p.M, ja + per);
-  float s = 0.f;
-  for (long j = ja; j < jb; ++j) s += decode_elem(p.v + (j * p.Hkv + hk) * p.rbv, p.v_type, c);
-  p.vsum[((size_t)blockIdx.y * p.Hkv + hk) * p.Dv + c] = s;
+  const long ja = (long)chunk * per, jb = min((long)p.M, ja + per);
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll 2
+  for (long j = ja; j < jb; ++j) {
+    float x[8];
+    decode8_f(p.v + (j * p.Hkv + hk) * p.rbv, p.v_type, c0, x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] += x[e];
+  }
+  float* o = p.vsum + ((size_t)chunk * p.Hkv + hk) * p.Dv + c0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o[e] = acc[e];
 }
 
 __device__ __forceinline__ float pow2_scale_for(float amax, int target_exp) {
@@ -426,22 +475,26 @@ __device__ __forceinline__ float pow2_scale_for(float amax, int target_exp) {
   return ldexpf(1.f, s);
 }
 
-__global__ void __launch_bounds__(256) k_finalize(Params p) {
+__global__ void __launch_bounds__(1024) k_finalize(Params p) {
   __shared__ float am[4], nm[4];
   __shared__ float rn2[1024], ram[1024];
   const int tid = threadIdx.x;
-  if (tid < 8) {
-    const int t = tid >> 1, w = tid & 1;
+  if (tid < 256) {  // max over the per-block statistics: 32 threads per value, then a warp reduction
+    const int q = tid >> 5, lane = tid & 31;  // q = t * 2 + w
     float m = 0.f;
-    for (int b = 0; b < p.nblk_stats; ++b) m = fmaxf(m, p.bstat[((size_t)b * 4 + t) * 2 + w]);
-    if (w == 0) am[t] = m;
-    else nm[t] = m;
+    for (int b = lane; b < p.nblk_stats; b += 32) m = fmaxf(m, p.bstat[(size_t)b * 8 + q]);
+    m = warp_max(m);
+    if (lane == 0) {
+      if ((q & 1) == 0) am[q >> 1] = m;
+      else nm[q >> 1] = m;
+    }
   }
   // column means of V^ (chunks in order) and max |r|
   float my_am = 0.f;
   const float invM = p.M > 0 ? 1.f / (float)p.M : 0.f;
-  for (int idx = tid; idx < p.Hkv * p.Dv; idx += 256) {
+  for (int idx = tid; idx < p.Hkv * p.Dv; idx += blockDim.x) {
     float s = 0.f;
+#pragma unroll 8
     for (int b = 0; b < p.nbv; ++b) s += p.vsum[((size_t)b * p.Hkv) * p.Dv + idx];
     const float r = s * invM;
     p.rmean[idx] = r;
@@ -452,13 +505,13 @@ __global__ void __launch_bounds__(256) k_finalize(Params p) {
   __shared__ float s_sV;
   if (tid == 0) {
     float ramax = 0.f;
-    for (int t = 0; t < 256; ++t) ramax = fmaxf(ramax, ram[t]);
+    for (int t = 0; t < (int)blockDim.x; ++t) ramax = fmaxf(ramax, ram[t]);
     ram[0] = ramax;
     s_sV = pow2_scale_for(am[3] + ramax, 14);  // |v^ - r| <= |v^| + |r|
   }
   __syncthreads();
   // the shift actually applied is r' = binary16(r * sV) / sV, so that -r' * sV is exact in binary16
-  for (int idx = tid; idx < p.Hkv * p.Dv; idx += 256) {
+  for (int idx = tid; idx < p.Hkv * p.Dv; idx += blockDim.x) {
     const float rs = __half2float(__float2half_rn(p.rmean[idx] * s_sV));
     p.rmean[idx] = rs / s_sV;
     p.rsh[idx] = -rs;
