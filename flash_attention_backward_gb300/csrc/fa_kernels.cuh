@@ -729,6 +729,23 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t tbase = *tslot;
   const Waiter wait{s_abort, p.err};
   const Stats st = *p.st;
+  // dQ += dS(t) K'(t) (dQ pass; issued by the producer thread, beside the S/dP stream of warp 1)
+  auto issue_dq = [&](int t) {
+    if constexpr (MODE != 1) return;  // only the dQ pass has the accumulator and the dS panel
+    constexpr uint32_t ID_DQ = idesc_f16(128, D, false, true);
+    tc_fence_after();
+    const uint32_t kp = smem_u32(sK + (t % C::KSTAGES) * C::KB);
+#pragma unroll
+    for (int k = 0; k < BK / 16; ++k)
+      mma_f16(tbase + C::T_ACC, sdesc_sw128(smem_u32(sS) + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024),
+              sdesc_sw128(kp + k * 2048, BK * 128, 1024), ID_DQ, (t > 0 || k > 0) ? 1u : 0u);
+    if (t == ntiles - 1) {
+      mma_commit(&bar[B_ACC_FULL]);
+    } else {
+      mma_commit(&bar[B_DS_EMPTY]);
+      mma_commit(&bar[B_K_EMPTY + t % C::KSTAGES]);
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
@@ -773,16 +790,26 @@ __global__ void __launch_bounds__(512, 1)
         cp_async_arrive(fb);
       }
     };
-    while (ek < tot || ev < tot) {
+    int nd = 0;  // next dQ product (dQ pass)
+    const int ndq = MODE == 1 ? ntiles : 0;
+    while (ek < tot || ev < tot || nd < ndq) {
       bool moved = false;
       // the warp takes each decision together (lane 0 polls, the others follow)
-      int go_k = 0, go_v = 0;
+      int go_k = 0, go_v = 0, go_q = 0;
       if (lane == 0) {
+        go_q = nd < ndq && mbar_try_wait(&bar[B_DS_FULL], nd & 1);
         go_k = ek < tot && mbar_try_wait(&bar[B_KRAW_EMPTY + sk], (uk & 1) ^ 1);
         go_v = ev < tot && mbar_try_wait(&bar[B_VRAW_EMPTY + sv], (uv & 1) ^ 1);
       }
+      go_q = __shfl_sync(0xffffffffu, go_q, 0);
       go_k = __shfl_sync(0xffffffffu, go_k, 0);
       go_v = __shfl_sync(0xffffffffu, go_v, 0);
+      if (go_q) {
+        if (lane == 0) issue_dq(nd);
+        __syncwarp();
+        ++nd;
+        moved = true;
+      }
       if (go_v) {
         load_entry(true, ev, sv);
         ++ev;
@@ -813,8 +840,7 @@ __global__ void __launch_bounds__(512, 1)
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t ID_S = idesc_f16(128, BK, false, false);
-      constexpr uint32_t ID_DQ = idesc_f16(128, D, false, true);
-      const uint32_t tQ = tbase + C::T_Q, tO = tbase + C::T_O, tAcc = tbase + C::T_ACC;
+      const uint32_t tQ = tbase + C::T_Q, tO = tbase + C::T_O;
       const bool ok = (MODE == 0 || wait(&bar[B_Q_FULL], 0)) && wait(&bar[B_OPS_READY], 0);
       // S(t) = Q K'^T into the tensor-memory slot of tile t
       auto issue_s = [&](int t) {
@@ -844,21 +870,6 @@ __global__ void __launch_bounds__(512, 1)
         mma_commit(&bar[B_S_FULL + sl]);
         mma_commit(&bar[B_V_EMPTY + vs]);
       };
-      // dQ += dS(t) K'(t)
-      auto issue_dq = [&](int t) {
-        tc_fence_after();
-        const uint32_t kp = smem_u32(sK + (t % C::KSTAGES) * C::KB);
-#pragma unroll
-        for (int k = 0; k < BK / 16; ++k)
-          mma_f16(tAcc, sdesc_sw128(smem_u32(sS) + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024),
-                  sdesc_sw128(kp + k * 2048, BK * 128, 1024), ID_DQ, (t > 0 || k > 0) ? 1u : 0u);
-        if (t == ntiles - 1) {
-          mma_commit(&bar[B_ACC_FULL]);
-        } else {
-          mma_commit(&bar[B_DS_EMPTY]);
-          mma_commit(&bar[B_K_EMPTY + t % C::KSTAGES]);
-        }
-      };
       if (MODE == 0) {
         for (int t = 0; ok && t < ntiles; ++t) {
           const int su = t / C::NSLOT;
@@ -870,33 +881,13 @@ __global__ void __launch_bounds__(512, 1)
           issue_dp(t);
         }
       } else if (ok) {
-        // Issue whatever is ready, dQ first (it frees the dS panel and a K' stage), then dP
-        // (it frees the single V' stage), then S of the next tile.
-        int ns = 0, np = 0, nd = 0;
-        uint64_t t0 = globaltimer_ns();
-        while (nd < ntiles) {
-          if (nd < np && mbar_try_wait(&bar[B_DS_FULL], nd & 1)) {
-            issue_dq(nd++);
-            t0 = globaltimer_ns();
-            continue;
-          }
-          if (np < ns && mbar_try_wait(&bar[B_V_FULL + np % C::VSTAGES], (np / C::VSTAGES) & 1)) {
-            issue_dp(np++);
-            t0 = globaltimer_ns();
-            continue;
-          }
-          if (ns < ntiles && ns == np && mbar_try_wait(&bar[B_K_FULL + ns % C::KSTAGES], (ns / C::KSTAGES) & 1) &&
-              mbar_try_wait(&bar[B_S_FREE], (ns & 1) ^ 1)) {
-            issue_s(ns++);
-            t0 = globaltimer_ns();
-            continue;
-          }
-          if (*s_abort) break;
-          if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            *s_abort = 1;
-            record_error(p.err, kErrTimeout);
+        // S(t) and dP(t) in order; the dQ products are issued by the producer thread
+        for (int t = 0; t < ntiles; ++t) {
+          if (!wait(&bar[B_K_FULL + t % C::KSTAGES], (t / C::KSTAGES) & 1) || !wait(&bar[B_S_FREE], (t & 1) ^ 1))
             break;
-          }
+          issue_s(t);
+          if (!wait(&bar[B_V_FULL + t % C::VSTAGES], (t / C::VSTAGES) & 1)) break;
+          issue_dp(t);
         }
       }
     }
