@@ -952,8 +952,10 @@ __global__ void __launch_bounds__(512, 1)
       dl = p.dlt[(size_t)hk * R + r];
     }
     const bool live = MODE == 1 ? (lse2 > -CUDART_INF_F) : rvalid;
-    const float nlse2 = live ? -lse2 : -CUDART_INF_F;  // 2^(t2 + nlse2) = p, and 0 on a dead row
     const float c2 = st.c2, lam = st.lam, dq_fac = st.dq_fac;
+    // 2^(t2 + nlse2) = p (0 on a dead row); in the dQ pass the exponent also carries log2(lam),
+    // so the exponential yields lam * p directly (lam is a power of two)
+    const float nlse2 = live ? -lse2 + (MODE == 1 ? (float)ilogbf(lam) : 0.f) : -CUDART_INF_F;
     const uint32_t sS_u = smem_u32(sS);
     float m2 = -CUDART_INF_F, l = 0.f, lc = 0.f, sd = 0.f, sdc = 0.f;
 
@@ -1006,10 +1008,11 @@ __global__ void __launch_bounds__(512, 1)
         }
         // fully visible chunk without a mask: no per-key tests
         const bool full = mrow == nullptr && (long)(j0 + col0 + 31) <= jlast;
-        float t2[32];
+        float t2[32];  // log2-domain scores (dQ pass: already minus lse, plus log2(lam))
+        const float t2off = MODE == 1 ? nlse2 : 0.f;
         if (full) {
 #pragma unroll
-          for (int n = 0; n < 32; ++n) t2[n] = s[n] * c2;
+          for (int n = 0; n < 32; ++n) t2[n] = fmaf(s[n], c2, t2off);
         } else {
 #pragma unroll
           for (int n = 0; n < 32; ++n) {
@@ -1020,7 +1023,7 @@ __global__ void __launch_bounds__(512, 1)
               mv = h2f(__ldg(reinterpret_cast<const unsigned short*>(mrow) + j));
               ok = !(mv == -CUDART_INF_F);
             }
-            t2[n] = ok ? fmaf(s[n], c2, mv * kLog2e) : -CUDART_INF_F;
+            t2[n] = ok ? fmaf(s[n], c2, fmaf(mv, kLog2e, t2off)) : -CUDART_INF_F;
           }
         }
         if (MODE == 0) {
@@ -1050,8 +1053,8 @@ __global__ void __launch_bounds__(512, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int n = 0; n < 32; n += 2) {
-            const float p0 = ex2(t2[n] + nlse2), p1 = ex2(t2[n + 1] + nlse2);  // 0 for masked keys, dead rows
-            pk[n / 2] = h2_as_u32(__floats2half2_rn(p0 * (dp[n] - dl) * lam, p1 * (dp[n + 1] - dl) * lam));
+            const float p0 = ex2(t2[n]), p1 = ex2(t2[n + 1]);  // lam * p; 0 for masked keys, dead rows
+            pk[n / 2] = h2_as_u32(__floats2half2_rn(p0 * (dp[n] - dl), p1 * (dp[n + 1] - dl)));
           }
           if (!stored_wait) {
             if (!wait(&bar[B_DS_EMPTY], (t & 1) ^ 1)) break;
@@ -1362,14 +1365,16 @@ __global__ void __launch_bounds__(384, 1)
     long jlast = -1;
     const uint16_t* mrow = nullptr;
     const uint32_t sP_u = smem_u32(sP), sS_u = smem_u32(sS);
-    const float c2 = st.c2, pmul = st.sP, lam = st.lam;
+    // the exponent carries log2 of the P multiplier (a power of two), so the exponential is
+    // the scaled P directly and dS takes lam / sP
+    const float c2 = st.c2, lp = (float)ilogbf(st.sP), lam = st.lam / st.sP;
     if (nq > 0) row_stats(0, lse2, dl, jlast, mrow);
     for (int t = 0; t < nq; ++t) {
       float nlse2 = 0.f, ndl = 0.f;  // next tile's row values, fetched ahead
       long njlast = -1;
       const uint16_t* nmrow = nullptr;
       if (t + 1 < nq) row_stats(t + 1, nlse2, ndl, njlast, nmrow);
-      const float nl = lse2 > -CUDART_INF_F ? -lse2 : -CUDART_INF_F;  // p = 2^(t2 + nl); 0 on a dead row
+      const float nl = lse2 > -CUDART_INF_F ? lp - lse2 : -CUDART_INF_F;  // sP * p = 2^(t2 + nl); 0 on a dead row
       if (!wait(&bar[C_S_FULL], t & 1)) break;
       // the previous tile's P and dS panels are free once its gradient products completed
       if (!wait(&bar[C_DS_EMPTY], (t & 1) ^ 1)) break;
@@ -1405,8 +1410,8 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int n = 0; n < 8; n += 2) {
             const int x = g + n;
-            const float p0 = ex2(t2[x]), p1 = ex2(t2[x + 1]);  // 0 for masked keys and dead rows
-            pp[n / 2] = h2_as_u32(__floats2half2_rn(p0 * pmul, p1 * pmul));
+            const float p0 = ex2(t2[x]), p1 = ex2(t2[x + 1]);  // sP * p; 0 for masked keys and dead rows
+            pp[n / 2] = h2_as_u32(__floats2half2_rn(p0, p1));
             pd[n / 2] = h2_as_u32(__floats2half2_rn(p0 * (dp[x] - dl) * lam, p1 * (dp[x + 1] - dl) * lam));
           }
           const uint32_t off = panel_off_u(128, row, col0 + g);
