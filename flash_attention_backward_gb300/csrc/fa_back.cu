@@ -270,11 +270,11 @@ static cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& 
       return cudaErrorInvalidValue;
   }
   dim3 grows(P.nQT, p.Hkv, P.nsplit);
-  k_rows2<D, Dv, BKL, 0><<<grows, 512, sm_l, s>>>(tmQ, tkl, tvl, pl);
+  k_rows2<D, Dv, BKL, 0><<<grows, RL::NT, sm_l, s>>>(tmQ, tkl, tvl, pl);
   rec.mark(KS_ROWS_LSE);
   k_lse_merge<<<(unsigned)(((long)p.Hkv * P.R + 255) / 256), 256, 0, s>>>(p);
   rec.mark(KS_MERGE);
-  k_rows2<D, Dv, BK, 1><<<grows, 512, sm_q, s>>>(tmQ, tkq, tvq, pq);
+  k_rows2<D, Dv, BK, 1><<<grows, RQ::NT, sm_q, s>>>(tmQ, tkq, tvq, pq);
   rec.mark(KS_ROWS_DQ);
   if (P.nsplit_dq > 1) {
     k_dq_reduce<<<(unsigned)(((long)p.Hkv * P.R * (D / 4) + 255) / 256), 256, 0, s>>>(p);

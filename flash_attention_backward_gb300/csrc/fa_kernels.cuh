@@ -597,7 +597,6 @@ __global__ void __launch_bounds__(256) k_convert(Params p) {
 
 template <int D, int Dv, int BK, int MODE>
 struct Rows2Cfg {
-  static constexpr int NT = 512;
   // binary16 K'/V' tile stages: two each where they fit beside the raw ring, else one (the LSE
   // pass at 128 keys x D = 256); the dQ pass keeps one V' stage (its Q tile lives here too)
   static constexpr int KSTAGES = (MODE == 0 && BK * (D + Dv) * 2 * 2 > 160 * 1024) ? 1 : 2;
@@ -627,7 +626,8 @@ struct Rows2Cfg {
   static constexpr int NSOFT = 4;
   static constexpr int NCH = NSOFT / 4;
   static constexpr int HALF = BK / NCH;  // columns per softmax thread
-  static constexpr int NDEC = 16 - 2 - NSOFT;
+  static constexpr int NDEC = 10;
+  static constexpr int NT = 32 * (2 + NSOFT + NDEC);  // threads per CTA
 };
 
 // barrier indices
@@ -666,7 +666,7 @@ struct Waiter {
 };
 
 template <int D, int Dv, int BK, int MODE>
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(Rows2Cfg<D, Dv, BK, MODE>::NT, 1)
     k_rows2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
             const __grid_constant__ CUtensorMap tmV, Params p) {
   using C = Rows2Cfg<D, Dv, BK, MODE>;

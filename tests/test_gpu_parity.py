@@ -66,6 +66,12 @@ EDGE = {
     # one key, one query
     "single_key": dict(N=5, M=1, H=2, Hkv=1, D=64, Dv=64, k_type="q8_0", v_type="q8_0"),
     "single_query": dict(N=1, M=257, H=8, Hkv=2, D=256, Dv=256, k_type="q8_0", v_type="q8_0", causal=True),
+    # D = 64 everywhere (128-key tiles in every pass), q4_0 K, per-head mask with the causal tail,
+    # several key splits and a ragged last tile
+    "d64_q4_mask_causal": dict(N=200, M=3001, H=8, Hkv=2, D=64, Dv=64, k_type="q4_0", v_type="q8_0", causal=True,
+                               mask="random", mask_p=0.05, full_rows=2, mask_heads=8),
+    # D = 128 f16 K with q4_0 V, GQA 4, rows not a multiple of the 128-row tile
+    "d128_f16k_q4v": dict(N=77, M=1500, H=16, Hkv=4, D=128, Dv=128, k_type="f16", v_type="q4_0"),
     # large-magnitude inputs (scales are chosen from the data)
     "big_values": dict(N=16, M=128, H=2, Hkv=1, D=64, Dv=64, k_type="f32", v_type="f32", q_sigma=300.0,
                        k_sigma=0.01, do_sigma=1e4, v_sigma=50.0),
