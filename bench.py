@@ -268,31 +268,60 @@ def run_ours(args):
     clocks = clk.summary()
     launches = sum(c for _, c in kern.values())
 
-    # ---- end to end: pinned host inputs -> device, fa_back, results -> pinned host
+    # ---- end to end: pinned host inputs -> device, fa_back, results -> pinned host, every step.
+    # Pipelined: three streams and double buffers, so step i's compute overlaps step i+1's input
+    # copy and step i-1's result copy.  The serial form (one stream) is reported beside it.
     hq = synth.device.to_torch(p, "cpu", pin=True)
-    hout = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()}
-    dt_in = {k: torch.empty_like(v) for k, v in t.items() if v is not None}
-    dt_in["mask"] = None
-    h2d = sum(v.numel() * v.element_size() for k, v in hq.items() if v is not None)
+    keys_in = [k for k, v in hq.items() if v is not None]
+    hout = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()} for _ in range(2)]
+    din = [dict({k: torch.empty_like(t[k]) for k in keys_in}, mask=None) for _ in range(2)]
+    dout = [{k: torch.empty_like(v) for k, v in out.items()} for _ in range(2)]
+    h2d = sum(hq[k].numel() * hq[k].element_size() for k in keys_in)
     d2h = sum(v.numel() * v.element_size() for v in out.values())
-    e_steps = max(1, min(args.steps, 5))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(e_steps):
-        for k, v in hq.items():
-            if v is not None:
-                dt_in[k].copy_(v, non_blocking=True)
-        step(dt_in)
-        for k, v in out.items():
-            hout[k].copy_(v, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e_steps
+    e_steps = max(2, min(args.steps, 6))
+
+    def run_e2e(pipelined: bool) -> float:
+        s_c = stream
+        s_in = torch.cuda.Stream(dev) if pipelined else s_c
+        s_out = torch.cuda.Stream(dev) if pipelined else s_c
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_c = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(s_in)
+        for i in range(e_steps):
+            b = i % 2 if pipelined else 0
+            if pipelined and i >= 2:
+                s_in.wait_event(ev_c[b])  # inputs b are read by compute(i-2)
+            with torch.cuda.stream(s_in):
+                for k in keys_in:
+                    din[b][k].copy_(hq[k], non_blocking=True)
+            ev_in[b].record(s_in)
+            s_c.wait_event(ev_in[b])
+            if pipelined and i >= 2:
+                s_c.wait_event(ev_out[b])  # outputs b still being copied back for step i-2
+            fb.backward(din[b]["q"], din[b]["k"], p.k_type, din[b]["v"], p.v_type, din[b]["dO"], H=p.H, Hkv=p.Hkv,
+                        D=p.D, Dv=p.Dv, M=p.M, scale=p.scale, causal=p.causal, mask=din[b]["mask"],
+                        mask_heads=p.mask_heads, out=dout[b], workspace=ws, stream=s_c)
+            ev_c[b].record(s_c)
+            s_out.wait_event(ev_c[b])
+            with torch.cuda.stream(s_out):
+                for k, v in dout[b].items():
+                    hout[b][k].copy_(v, non_blocking=True)
+            ev_out[b].record(s_out)
+        e1.record(s_out)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / e_steps
+
+    e2e_serial_ms = run_e2e(False)
+    e2e_ms = run_e2e(True)
+    rc = fb.fa_back_get_error()
+    assert rc == 0, fb.fa_back_status_string(rc)
     if dist is not None:
-        x = torch.tensor([e2e_ms], device=dev)
+        x = torch.tensor([e2e_ms, e2e_serial_ms], device=dev)
         dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        e2e_ms = float(x.item())
+        e2e_ms, e2e_serial_ms = float(x[0].item()), float(x[1].item())
 
     flops = p.flops()
     tflops = world * flops / (ms * 1e-3) / 1e12
@@ -323,7 +352,9 @@ def run_ours(args):
             "roofline": roofline, "kernels_ms": {k: v[0] / v[1] for k, v in kern.items()},
             "gpu_launches": launches, "clocks": clocks,
             "e2e": {"value": e2e_tflops, "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h}}
+                    "d2h_bytes_per_step": d2h,
+                    "pipelining": "input copy, backward and result copy on three streams, double-buffered",
+                    "serial": {"value": world * flops / (e2e_serial_ms * 1e-3) / 1e12, "ms_per_step": e2e_serial_ms}}}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(p)
     if rank == 0:
