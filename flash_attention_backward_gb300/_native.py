@@ -35,6 +35,8 @@ def lib():
     L.fa_row_bytes.argtypes = [i, i]
     L.fa_back_workspace_size.restype = sz
     L.fa_back_workspace_size.argtypes = [i] * 6
+    L.fa_back_workspace_size_min.restype = sz
+    L.fa_back_workspace_size_min.argtypes = [i] * 6
     L.fa_back.restype = i
     L.fa_back.argtypes = [vp, vp, i, vp, i, vp, i, vp, f, i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, sz, vp]
     L.fa_back_get_error.restype = i
@@ -59,6 +61,10 @@ def fa_row_bytes(type_: int, D: int) -> int:
 
 def fa_back_workspace_size(N: int, M: int, H: int, Hkv: int, D: int, Dv: int) -> int:
     return int(lib().fa_back_workspace_size(N, M, H, Hkv, D, Dv))
+
+
+def fa_back_workspace_size_min(N: int, M: int, H: int, Hkv: int, D: int, Dv: int) -> int:
+    return int(lib().fa_back_workspace_size_min(N, M, H, Hkv, D, Dv))
 
 
 def fa_back(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal,

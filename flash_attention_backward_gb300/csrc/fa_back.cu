@@ -34,8 +34,10 @@ __device__ int g_err = 0;
 struct Plan {
   int G, R, nQT, BK, nKT, nsplit, kt_per_split, nsplit_dq;
   int nblk_stats, nbv;
+  int pre;  // 1: binary16 K'/V' copies in the workspace feed the row passes by TMA
+  int nsm;
   size_t off_stats, off_rmean, off_rsh, off_dOr, off_lse2, off_dlt, off_part, off_dqpart, off_q16, off_do16,
-      off_bstat, off_vsum, total;
+      off_bstat, off_vsum, off_kd, off_vd, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -47,7 +49,7 @@ static int block_keys(int D, int Dv) { return (D + Dv <= 256) ? 128 : 64; }
 constexpr int kBKLse = 128;
 
 // Workspace offsets of a plan whose split counts are set.
-static void layout(Plan& P, int Hkv, int D, int Dv) {
+static void layout(Plan& P, int M, int Hkv, int D, int Dv) {
   size_t o = 0;
   P.off_stats = o; o = align256(o + sizeof(Stats));
   P.off_rmean = o; o = align256(o + sizeof(float) * (size_t)Hkv * Dv);
@@ -61,15 +63,20 @@ static void layout(Plan& P, int Hkv, int D, int Dv) {
   P.off_do16 = o; o = align256(o + 2 * (size_t)Hkv * P.R * Dv);
   P.off_bstat = o; o = align256(o + sizeof(float) * 8 * (size_t)P.nblk_stats);
   P.off_vsum = o; o = align256(o + sizeof(float) * (size_t)P.nbv * Hkv * Dv);
+  P.off_kd = o; o = align256(o + (P.pre ? 2 * (size_t)Hkv * M * D : 0));
+  P.off_vd = o; o = align256(o + (P.pre ? 2 * (size_t)Hkv * M * Dv : 0));
   P.total = o;
 }
 
-// Launch plan and workspace layout.  The keys of each row tile are split so that the last wave
-// of CTAs (one per SM) wastes least, counting a small cost per split for the partial merges;
-// among split counts whose workspace fits `ws_cap`, the cheapest is taken (1 if none fits).
-static Plan make_plan(int N, int M, int H, int Hkv, int D, int Dv, int nsm, size_t ws_cap = SIZE_MAX) {
+// Launch plan and workspace layout for one row-pass variant (pre: binary16 K'/V' copies).  The
+// keys of each row tile are split so that the last wave of CTAs (one per SM) wastes least,
+// counting a small cost per split for the partial merges; among split counts whose workspace
+// fits `ws_cap`, the cheapest is taken (1 if none fits).
+static Plan plan_variant(int N, int M, int H, int Hkv, int D, int Dv, int nsm, size_t ws_cap, int pre) {
   Plan P;
   std::memset(&P, 0, sizeof(P));
+  P.pre = pre;
+  P.nsm = nsm;
   P.G = H / Hkv;
   P.R = N * P.G;
   P.nQT = (P.R + 127) / 128;
@@ -84,7 +91,7 @@ static Plan make_plan(int N, int M, int H, int Hkv, int D, int Dv, int nsm, size
     P.kt_per_split = (P.kt_per_split + r - 1) / r * r;
     P.nsplit = P.nKT > 0 ? (P.nKT + P.kt_per_split - 1) / P.kt_per_split : 1;
     P.nsplit_dq = P.nsplit;
-    layout(P, Hkv, D, Dv);
+    layout(P, M, Hkv, D, Dv);
   };
   const int base = std::max(1, P.nQT * Hkv);
   int ns = 1;
@@ -99,6 +106,15 @@ static Plan make_plan(int N, int M, int H, int Hkv, int D, int Dv, int nsm, size
   }
   set_split(ns);
   return P;
+}
+
+// The fastest plan whose workspace fits ws_cap: the producer-fed row passes over binary16 K'/V'
+// copies where they fit, else the row passes that decode the raw cache in shared memory (whose
+// one-split plan is the smallest workspace fa_back() accepts).
+static Plan make_plan(int N, int M, int H, int Hkv, int D, int Dv, int nsm, size_t ws_cap = SIZE_MAX) {
+  const Plan P = plan_variant(N, M, H, Hkv, D, Dv, nsm, ws_cap, 1);
+  if (P.total <= ws_cap) return P;
+  return plan_variant(N, M, H, Hkv, D, Dv, nsm, ws_cap, 0);
 }
 
 static int device_sms(int* major, int* minor) {
@@ -127,13 +143,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// binary16 tensor [d2][d1][d0] (d0 fastest); boxes of 64 x 128 x 1 with the 128-byte swizzle.
-static bool make_map(CUtensorMap* m, void* base, int d0, int d1, int d2) {
+// binary16 tensor [d2][d1][d0] (d0 fastest); boxes of 64 x rows x 1 with the 128-byte swizzle
+// (one box is one operand panel of `rows` 128-byte rows).
+static bool make_map(CUtensorMap* m, void* base, int d0, int d1, int d2, int rows = 128) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
   cuuint64_t strides[2] = {(cuuint64_t)d0 * 2, (cuuint64_t)d0 * d1 * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -144,10 +161,14 @@ static bool make_map(CUtensorMap* m, void* base, int d0, int d1, int d2) {
 // measurement hook: one CUDA event before the sequence and one after each launch
 
 constexpr int kProfCalls = 256, kProfSlots = 16;
+// in launch order (the read-out measures each kernel from the previous recorded marker)
 static const char* const kKernelNames[kProfSlots] = {
-    "k_row_stats", "k_vsum", "k_finalize", "k_convert", "k_rows_lse", "k_lse_merge", "k_rows_dq", "k_dq_reduce",
-    "k_cols", "", "", "", "", "", "", ""};
-enum { KS_STATS = 0, KS_VSUM, KS_FINAL, KS_CONVERT, KS_ROWS_LSE, KS_MERGE, KS_ROWS_DQ, KS_DQ_REDUCE, KS_COLS, KS_N };
+    "k_row_stats", "k_vsum", "k_finalize", "k_convert", "k_predecode", "k_rows_lse", "k_lse_merge", "k_rows_dq",
+    "k_dq_reduce", "k_cols", "", "", "", "", "", ""};
+enum {
+  KS_STATS = 0, KS_VSUM, KS_FINAL, KS_CONVERT, KS_PREDECODE, KS_ROWS_LSE, KS_MERGE, KS_ROWS_DQ, KS_DQ_REDUCE,
+  KS_COLS, KS_N
+};
 
 struct Profiler {
   std::mutex mu;
@@ -233,21 +254,39 @@ static void pick_raw(Params& q, int budget, int BK) {
 
 static int raw_bytes(const Params& q) { return q.ke * (q.raw_depth * q.rbk_pad + q.raw_depth_v * q.rbv_pad); }
 
-template <int D, int Dv>
-static cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& tmQ, const CUtensorMap& tmO,
-                             cudaStream_t s, CallRec& rec) {
-  constexpr int BK = (D + Dv <= 256) ? 128 : 64;
-  constexpr int BKL = kBKLse;  // LSE-pass key tile
-  static_assert(BKL % BK == 0, "LSE tiles cover whole gradient-pass tiles");
+// Row passes over the binary16 K'/V' copies (written here by k_predecode), fed by TMA.
+template <int D, int Dv, int BK, int BKL>
+static cudaError_t rows_pre(const Params& pl, const Params& pq, const Plan& P, const CUtensorMap& tmQ, dim3 grid,
+                            cudaStream_t s, CallRec& rec) {
+  using FL = Rows3Cfg<D, Dv, BKL, 0>;
+  using FQ = Rows3Cfg<D, Dv, BK, 1>;
+  CUtensorMap tkl, tvl, tkq, tvq;
+  if (!make_map(&tkl, pl.kd, D, pl.M, pl.Hkv, BKL) || !make_map(&tvl, pl.vd, Dv, pl.M, pl.Hkv, BKL) ||
+      !make_map(&tkq, pq.kd, D, pq.M, pq.Hkv, BK) || !make_map(&tvq, pq.vd, Dv, pq.M, pq.Hkv, BK))
+    return cudaErrorInvalidValue;
+  cudaError_t e;
+  if ((e = set_smem(k_rows3<D, Dv, BKL, 0>, FL::SMEM)) != cudaSuccess) return e;
+  if ((e = set_smem(k_rows3<D, Dv, BK, 1>, FQ::SMEM)) != cudaSuccess) return e;
+  const long units = (long)pl.M * pl.Hkv * ((D + Dv) / 8);
+  k_predecode<<<(unsigned)std::min<long>((units + 255) / 256, 16L * P.nsm), 256, 0, s>>>(pl);
+  rec.mark(KS_PREDECODE);
+  k_rows3<D, Dv, BKL, 0><<<grid, FL::NT, FL::SMEM, s>>>(tmQ, tkl, tvl, pl);
+  rec.mark(KS_ROWS_LSE);
+  k_lse_merge<<<(unsigned)(((long)pl.Hkv * P.R + 255) / 256), 256, 0, s>>>(pl);
+  rec.mark(KS_MERGE);
+  k_rows3<D, Dv, BK, 1><<<grid, FQ::NT, FQ::SMEM, s>>>(tmQ, tkq, tvq, pq);
+  rec.mark(KS_ROWS_DQ);
+  return cudaSuccess;
+}
+
+// Row passes that stage raw cache rows in shared memory and decode them there.
+template <int D, int Dv, int BK, int BKL>
+static cudaError_t rows_raw(Params pl, Params pq, const Plan& P, const CUtensorMap& tmQ, dim3 grid, cudaStream_t s,
+                            CallRec& rec) {
   using RL = Rows2Cfg<D, Dv, BKL, 0>;
   using RQ = Rows2Cfg<D, Dv, BK, 1>;
-  using CC = Cols2Cfg<D, Dv, BK>;
-  static_assert(RL::RAW_BUDGET > 0 && RQ::RAW_BUDGET > 0 && CC::SMEM <= 232448, "shared memory budget");
-  static_assert(RL::TCOLS <= 512 && RQ::TCOLS <= 512 && CC::TCOLS <= 512, "tensor memory budget");
-  Params pl = p, pq = p;
-  // the LSE pass walks the same key splits in BKL-key tiles (split sizes are multiples of BKL)
-  pl.nKT = (p.M + BKL - 1) / BKL;
-  pl.kt_per_split = p.kt_per_split / (BKL / BK);
+  static_assert(RL::RAW_BUDGET > 0 && RQ::RAW_BUDGET > 0, "shared memory budget");
+  static_assert(RL::TCOLS <= 512 && RQ::TCOLS <= 512, "tensor memory budget");
   pick_raw(pl, RL::RAW_BUDGET, BKL);
   pick_raw(pq, RQ::RAW_BUDGET, BK);
   for (Params* q : {&pl, &pq})  // TMA destinations must start on 128-byte boundaries
@@ -259,28 +298,46 @@ static cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& 
   cudaError_t e;
   if ((e = set_smem(k_rows2<D, Dv, BKL, 0>, sm_l)) != cudaSuccess) return e;
   if ((e = set_smem(k_rows2<D, Dv, BK, 1>, sm_q)) != cudaSuccess) return e;
-  if ((e = set_smem(k_cols2<D, Dv, BK>, CC::SMEM)) != cudaSuccess) return e;
-
   CUtensorMap tkl, tvl, tkq, tvq;
   std::memset(&tkl, 0, sizeof(tkl));
   tvl = tkq = tvq = tkl;
-  if (p.raw_bulk) {
-    if (!make_raw_map(&tkl, p.k, p.rbk, p.Hkv, p.M, pl.ke) || !make_raw_map(&tvl, p.v, p.rbv, p.Hkv, p.M, pl.ke) ||
-        !make_raw_map(&tkq, p.k, p.rbk, p.Hkv, p.M, pq.ke) || !make_raw_map(&tvq, p.v, p.rbv, p.Hkv, p.M, pq.ke))
+  if (pl.raw_bulk) {
+    if (!make_raw_map(&tkl, pl.k, pl.rbk, pl.Hkv, pl.M, pl.ke) ||
+        !make_raw_map(&tvl, pl.v, pl.rbv, pl.Hkv, pl.M, pl.ke) ||
+        !make_raw_map(&tkq, pq.k, pq.rbk, pq.Hkv, pq.M, pq.ke) || !make_raw_map(&tvq, pq.v, pq.rbv, pq.Hkv, pq.M, pq.ke))
       return cudaErrorInvalidValue;
   }
-  dim3 grows(P.nQT, p.Hkv, P.nsplit);
-  k_rows2<D, Dv, BKL, 0><<<grows, RL::NT, sm_l, s>>>(tmQ, tkl, tvl, pl);
+  k_rows2<D, Dv, BKL, 0><<<grid, RL::NT, sm_l, s>>>(tmQ, tkl, tvl, pl);
   rec.mark(KS_ROWS_LSE);
-  k_lse_merge<<<(unsigned)(((long)p.Hkv * P.R + 255) / 256), 256, 0, s>>>(p);
+  k_lse_merge<<<(unsigned)(((long)pl.Hkv * P.R + 255) / 256), 256, 0, s>>>(pl);
   rec.mark(KS_MERGE);
-  k_rows2<D, Dv, BK, 1><<<grows, RQ::NT, sm_q, s>>>(tmQ, tkq, tvq, pq);
+  k_rows2<D, Dv, BK, 1><<<grid, RQ::NT, sm_q, s>>>(tmQ, tkq, tvq, pq);
   rec.mark(KS_ROWS_DQ);
+  return cudaSuccess;
+}
+
+template <int D, int Dv>
+static cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& tmQ, const CUtensorMap& tmO,
+                             cudaStream_t s, CallRec& rec) {
+  constexpr int BK = (D + Dv <= 256) ? 128 : 64;
+  constexpr int BKL = kBKLse;  // LSE-pass key tile
+  static_assert(BKL % BK == 0, "LSE tiles cover whole gradient-pass tiles");
+  using CC = Cols2Cfg<D, Dv, BK>;
+  static_assert(CC::SMEM <= 232448 && CC::TCOLS <= 512, "dK/dV pass budgets");
+  Params pl = p, pq = p;
+  // the LSE pass walks the same key splits in BKL-key tiles (split sizes are multiples of BKL)
+  pl.nKT = (p.M + BKL - 1) / BKL;
+  pl.kt_per_split = p.kt_per_split / (BKL / BK);
+  const dim3 grid(P.nQT, p.Hkv, P.nsplit);
+  cudaError_t e = P.pre ? rows_pre<D, Dv, BK, BKL>(pl, pq, P, tmQ, grid, s, rec)
+                        : rows_raw<D, Dv, BK, BKL>(pl, pq, P, tmQ, grid, s, rec);
+  if (e != cudaSuccess) return e;
   if (P.nsplit_dq > 1) {
     k_dq_reduce<<<(unsigned)(((long)p.Hkv * P.R * (D / 4) + 255) / 256), 256, 0, s>>>(p);
     rec.mark(KS_DQ_REDUCE);
   }
   if (P.nKT > 0) {
+    if ((e = set_smem(k_cols2<D, Dv, BK>, CC::SMEM)) != cudaSuccess) return e;
     k_cols2<D, Dv, BK><<<dim3(P.nKT, p.Hkv), 384, CC::SMEM, s>>>(tmQ, tmO, p);
     rec.mark(KS_COLS);
   }
@@ -334,12 +391,17 @@ extern "C" size_t fa_back_workspace_size(int N, int M, int H, int Hkv, int D, in
   return fab_workspace_size_capped(N, M, H, Hkv, D, Dv, SIZE_MAX);
 }
 
+extern "C" size_t fa_back_workspace_size_min(int N, int M, int H, int Hkv, int D, int Dv) {
+  return fab_workspace_size_capped(N, M, H, Hkv, D, Dv, 0);
+}
+
 extern "C" fa_status fa_back(const float* q, const void* k, int k_type, const void* v, int v_type,
                              const uint16_t* mask, int mask_heads, const float* dO, float scale, int N, int M,
                              int H, int Hkv, int D, int Dv, int causal, float* dQ, float* dK, float* dV,
                              float* lse, float* delta, void* workspace, size_t workspace_bytes, void* stream) {
+  // the plan is the fastest one whose workspace fits the caller's
   return fab_back_capped(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal, dQ,
-                         dK, dV, lse, delta, workspace, workspace_bytes, stream, SIZE_MAX);
+                         dK, dV, lse, delta, workspace, workspace_bytes, stream, workspace_bytes);
 }
 
 extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, const void* v, int v_type,
@@ -411,6 +473,8 @@ extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, 
   p.vsum = reinterpret_cast<float*>(ws + P.off_vsum);
   p.nbv = P.nbv;
   p.rsh = reinterpret_cast<float*>(ws + P.off_rsh);
+  p.kd = P.pre ? reinterpret_cast<__half*>(ws + P.off_kd) : nullptr;
+  p.vd = P.pre ? reinterpret_cast<__half*>(ws + P.off_vd) : nullptr;
   p.raw_bulk = (rbk % 16 == 0 && rbv % 16 == 0 && rbk <= 2048 && rbv <= 2048) ? 1 : 0;
   p.rbk_pad = (int)((rbk + 15) / 16 * 16);
   p.rbv_pad = (int)((rbv + 15) / 16 * 16);

@@ -73,6 +73,8 @@ struct Params {
   float* vsum;    // [nbv][Hkv][Dv]
   int nbv;
   float* rsh;     // [Hkv][Dv]  -r' * sV, an exact binary16 value (the decoders' V shift)
+  __half* kd;     // [Hkv][M][D]   binary16 K' = k^ sK (producer-fed row passes; else null)
+  __half* vd;     // [Hkv][M][Dv]  binary16 V' = v^ sV - r' sV
   // raw K/V staging of the row passes
   int raw_bulk;        // 1: rows are 16-byte multiples, copied by bulk async copies; 0: 4-byte async copies
   int rbk_pad, rbv_pad;  // raw row strides in shared memory (16-byte multiples)
@@ -153,11 +155,15 @@ __device__ __forceinline__ uint4 decode8_h(const uint8_t* row, int type, int c0,
       w[e] = h2_as_u32(__hfma2(code, ds, sh[e]));
     }
   } else if (type == kTypeF16) {
+    // in f32: the power-of-two scale can exceed binary16's range (small-magnitude caches);
+    // x * sig is exact there, so the one rounding is the final conversion
     const uint4 u = *reinterpret_cast<const uint4*>(row + 2 * c0);
     const uint32_t in[4] = {u.x, u.y, u.z, u.w};
-    const __half2 s2 = __float2half2_rn(sig);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) w[e] = h2_as_u32(__hfma2(u32_as_h2(in[e]), s2, sh[e]));
+    for (int e = 0; e < 4; ++e) {
+      const float2 x = __half22float2(u32_as_h2(in[e])), f = __half22float2(sh[e]);
+      w[e] = h2_as_u32(__floats2half2_rn(fmaf(x.x, sig, f.x), fmaf(x.y, sig, f.y)));
+    }
   } else {
     const float4 a = *reinterpret_cast<const float4*>(row + 4 * c0);
     const float4 c = *reinterpret_cast<const float4*>(row + 4 * c0 + 16);
@@ -229,13 +235,12 @@ __device__ __forceinline__ void decode_rows(int type, uint32_t raw0, int rb_pad,
     const bool q8 = type == kTypeQ8;
     const int bbytes = q8 ? 34 : 18;
     const __half2 bias = q8 ? __float2half2_rn(1152.f) : __float2half2_rn(1032.f);
-    const __half2 sig2 = __float2half2_rn(sig);
     for (int rr = rfirst; rr < nrows; rr += rs) {
       uint32_t o[16];
       if (rr < nvalid) {
         const uint32_t blk = raw0 + rr * rb_pad + g * bbytes;
-        const uint32_t dd = lds_u16(blk);
-        const __half2 ds = __hmul2(u32_as_h2(dd | (dd << 16)), sig2);  // exact: power-of-two scale
+        // d * sigma in f32 (sigma may exceed binary16's range), rounded once to binary16
+        const __half2 ds = __float2half2_rn(h2f((uint16_t)lds_u16(blk)) * sig);
         const uint32_t cs = blk + 2, cb = cs & ~3u;
         const bool al = (cs & 3u) == 0;
         const uint32_t sa = al ? 0x5140u : 0x7362u, sb = al ? 0x7362u : 0x5140u;
@@ -281,7 +286,6 @@ __device__ __forceinline__ void decode_rows(int type, uint32_t raw0, int rb_pad,
     }
   } else {
     const bool f16 = type == kTypeF16;
-    const __half2 s2 = __float2half2_rn(sig);
     for (int rr = rfirst; rr < nrows; rr += rs) {
       uint32_t o[4] = {0u, 0u, 0u, 0u};
       if (rr < nvalid) {
@@ -290,7 +294,10 @@ __device__ __forceinline__ void decode_rows(int type, uint32_t raw0, int rb_pad,
           const uint4 v = lds_v4(a);
           const uint32_t in[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) o[e] = h2_as_u32(__hfma2(u32_as_h2(in[e]), s2, SHIFT ? sh[e] : z));
+          for (int e = 0; e < 4; ++e) {  // in f32, as decode8_h
+            const float2 x = __half22float2(u32_as_h2(in[e])), f = __half22float2(SHIFT ? sh[e] : z);
+            o[e] = h2_as_u32(__floats2half2_rn(fmaf(x.x, sig, f.x), fmaf(x.y, sig, f.y)));
+          }
         } else {
           const uint4 u0 = lds_v4(a), u1 = lds_v4(a + 16);
           const uint32_t in[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
@@ -576,6 +583,28 @@ __global__ void __launch_bounds__(256) k_convert(Params p) {
     }
     dot = warp_sum(dot);
     if (lane == 0) p.dOr[(size_t)hk * p.R + r] = dot;
+  }
+}
+
+// Binary16 operand copies of the cache for the producer-fed row passes: K'[hk][j] = k^_j sK and
+// V'[hk][j] = v^_j sV - r' sV, with the rounding of the in-kernel decoders (decode8_h), so both
+// row-pass variants see the same operands.  Thread = 8 values; cache rows are read in order.
+__global__ void __launch_bounds__(256) k_predecode(Params p) {
+  const float sK = p.st->sK, sV = p.st->sV;
+  const long uk = (long)p.M * p.Hkv * (p.D / 8), uv = (long)p.M * p.Hkv * (p.Dv / 8);
+  for (long u = (long)blockIdx.x * 256 + threadIdx.x; u < uk + uv; u += (long)gridDim.x * 256) {
+    const bool isv = u >= uk;
+    const long w = isv ? u - uk : u;
+    const int DD = isv ? p.Dv : p.D;
+    const long row = w / (DD / 8);  // cache row j * Hkv + hk
+    const int c0 = (int)(w % (DD / 8)) * 8;
+    const long j = row / p.Hkv;
+    const int hk = (int)(row % p.Hkv);
+    const uint8_t* src = (isv ? p.v : p.k) + row * (isv ? p.rbv : p.rbk);
+    const uint4 o = decode8_h(src, isv ? p.v_type : p.k_type, c0, isv ? sV : sK,
+                              isv ? p.rsh + (size_t)hk * DD : nullptr);
+    __half* dst = (isv ? p.vd : p.kd) + ((size_t)hk * p.M + j) * DD + c0;
+    *reinterpret_cast<uint4*>(dst) = o;
   }
 }
 
@@ -1100,6 +1129,437 @@ __global__ void __launch_bounds__(Rows2Cfg<D, Dv, BK, MODE>::NT, 1)
       if (have) tc_fence_after();
 #pragma unroll 1
       for (int c = ch * (D / C::NCH); c < (ch + 1) * (D / C::NCH); c += 32) {
+        float v[32];
+        if (have) {
+          tmem_ld32(tbase + C::T_ACC + lane_off + c, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0.f;
+        }
+        if (out) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(out + c + e) =
+                make_float4(v[e] * dq_fac, v[e + 1] * dq_fac, v[e + 2] * dq_fac, v[e + 3] * dq_fac);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::TCOLS);
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// producer-fed row passes: the LSE/D pass (MODE 0) and the dQ pass (MODE 1) over the binary16
+// K'/V' copies written by k_predecode, which arrive as 128-byte-swizzled TMA panels.  With no
+// decoding inside the CTA, the operand stages take the shared memory the raw rings held.
+//
+// Warp roles: warp 0 producer (TMA loads of K'/V' tiles and, in the dQ pass, of the Q tile; it
+// also issues the dQ products), warp 1 tensor-memory owner and S/dP issuer, warps 2.. softmax:
+// four per 32-key chunk of the tile (one per tensor-memory lane quarter), so a softmax thread
+// owns one row and one chunk.  S and dP each have a full/free barrier pair; the softmax frees
+// S as soon as its chunk is in registers, so S(t+1) is computed while dP(t) is still read.
+
+template <int D, int Dv, int BK, int MODE>
+struct Rows3Cfg {
+  static constexpr int QB = MODE ? 128 * D * 2 : 0;
+  static constexpr int KB = BK * D * 2, VB = BK * Dv * 2;
+  static constexpr int SB = MODE ? 128 * BK * 2 : 0;
+  static constexpr int NCH = BK / 32;  // 32-key chunks per tile
+  static constexpr int NSOFT = 4 * NCH;
+  static constexpr int NT = 32 * (2 + NSOFT);
+  static constexpr int MERGE_BYTES = MODE == 0 ? (NCH - 1) * 128 * 3 * 4 : 0;
+  static constexpr int BAR_BYTES = 512 + MERGE_BYTES;
+  static constexpr int SMEM_MAX = 232448;
+  static constexpr int AVAIL = SMEM_MAX - 1024 - BAR_BYTES - QB - SB;
+  // K'/V' stages (at most 4 each): K first, then alternately, while they fit
+  static constexpr int stage_pair() {
+    int k = 1, v = 1;
+    for (;;) {
+      if (k <= v && k < 4 && (k + 1) * KB + v * VB <= AVAIL)
+        ++k;
+      else if (v < k && v < 4 && k * KB + (v + 1) * VB <= AVAIL)
+        ++v;
+      else if (k < 4 && (k + 1) * KB + v * VB <= AVAIL)
+        ++k;
+      else
+        break;
+    }
+    return k * 8 + v;
+  }
+  static constexpr int KSTAGES = stage_pair() / 8, VSTAGES = stage_pair() % 8;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + QB;
+  static constexpr int OFF_V = OFF_K + KSTAGES * KB;
+  static constexpr int OFF_S = OFF_V + VSTAGES * VB;
+  static constexpr int OFF_BAR = OFF_S + SB;
+  static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;  // + 1024 for aligning the base
+  // tensor-memory columns: [Q' (LSE pass)] [dO'] [S] [dP] [dQ accumulator (dQ pass)]
+  static constexpr int T_Q = 0;
+  static constexpr int T_O = MODE ? 0 : D / 2;
+  static constexpr int T_S = T_O + Dv / 2;
+  static constexpr int T_P = T_S + BK;
+  static constexpr int T_ACC = T_P + BK;
+  static constexpr int TCOLS = pow2_at_least(MODE ? T_ACC + D : T_ACC);
+  static_assert(KB + VB <= AVAIL && SMEM <= SMEM_MAX, "shared memory budget");
+  static_assert(TCOLS <= 512, "tensor memory budget");
+  static_assert(BK % 32 == 0 && BK <= 128, "key tile");
+};
+
+enum {
+  R3_K_FULL = 0,   // [4] K' tile landed
+  R3_K_EMPTY = 4,  // [4] K' tile's products done
+  R3_V_FULL = 8,   // [4]
+  R3_V_EMPTY = 12,  // [4]
+  R3_S_FULL = 16,
+  R3_S_FREE,
+  R3_P_FULL,
+  R3_P_FREE,
+  R3_DS_FULL,
+  R3_DS_EMPTY,
+  R3_ACC_FULL,
+  R3_Q_FULL,
+  R3_OPS_READY,
+  R3_COUNT
+};
+static_assert(8 * R3_COUNT + 8 <= 512, "barrier area");
+
+template <int D, int Dv, int BK, int MODE>
+__global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
+    k_rows3(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+            const __grid_constant__ CUtensorMap tmV, Params p) {
+  using C = Rows3Cfg<D, Dv, BK, MODE>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sQ = sm + C::OFF_Q;
+  uint8_t* sK = sm + C::OFF_K;
+  uint8_t* sV = sm + C::OFF_V;
+  uint8_t* sS = sm + C::OFF_S;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 8 * R3_COUNT);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + C::OFF_BAR + 8 * R3_COUNT + 4);
+  float* s_merge = reinterpret_cast<float*>(sm + C::OFF_BAR + 512);  // [NCH-1][128][3]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qt = blockIdx.x, hk = blockIdx.y, split = blockIdx.z;
+  const int r0 = qt * 128;
+  const int R = p.R, G = p.G;
+
+  const int kt_begin = split * p.kt_per_split;
+  int kt_end = min(p.nKT, kt_begin + p.kt_per_split);
+  if (p.causal) {
+    const long i_hi = (long)min(R - 1, r0 + 127) / G;
+    const long jmax = (long)p.M - p.N + i_hi;
+    kt_end = min(kt_end, jmax < 0 ? 0 : (int)(jmax / BK) + 1);
+  }
+  const int ntiles = max(0, kt_end - kt_begin);
+
+  if (warp == 1) tmem_alloc(tslot, C::TCOLS);
+  if (tid == 0) {
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&bar[R3_K_FULL + s], 1);
+      mbar_init(&bar[R3_K_EMPTY + s], 1);
+      mbar_init(&bar[R3_V_FULL + s], 1);
+      mbar_init(&bar[R3_V_EMPTY + s], 1);
+    }
+    mbar_init(&bar[R3_S_FULL], 1);
+    mbar_init(&bar[R3_S_FREE], C::NSOFT);
+    mbar_init(&bar[R3_P_FULL], 1);
+    mbar_init(&bar[R3_P_FREE], C::NSOFT);
+    mbar_init(&bar[R3_DS_FULL], C::NSOFT);
+    mbar_init(&bar[R3_DS_EMPTY], 1);
+    mbar_init(&bar[R3_ACC_FULL], 1);
+    mbar_init(&bar[R3_Q_FULL], 1);
+    mbar_init(&bar[R3_OPS_READY], C::NSOFT);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  const Waiter wait{s_abort, p.err};
+  const Stats st = *p.st;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      if (MODE == 1 && ntiles > 0) {
+        mbar_arrive_expect_tx(&bar[R3_Q_FULL], (uint32_t)C::QB);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) tma_load_3d(sQ + c * 128 * 128, &tmQ, &bar[R3_Q_FULL], c * 64, r0, hk);
+      }
+      // dQ += dS(t) K'(t) (dQ pass), beside the S/dP stream of warp 1
+      auto issue_dq = [&](int t) {
+        constexpr uint32_t ID_DQ = idesc_f16(128, D, false, true);
+        tc_fence_after();
+        const uint32_t kp = smem_u32(sK + (t % C::KSTAGES) * C::KB);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)
+          mma_f16(tbase + C::T_ACC, sdesc_sw128(smem_u32(sS) + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024),
+                  sdesc_sw128(kp + k * 2048, BK * 128, 1024), ID_DQ, (t > 0 || k > 0) ? 1u : 0u);
+        if (t == ntiles - 1) {
+          mma_commit(&bar[R3_ACC_FULL]);
+        } else {
+          mma_commit(&bar[R3_DS_EMPTY]);
+          mma_commit(&bar[R3_K_EMPTY + t % C::KSTAGES]);
+        }
+      };
+      const int ndq = MODE == 1 ? ntiles : 0;
+      int kt = 0, vt = 0, nd = 0;
+      uint64_t t0 = globaltimer_ns();
+      while (kt < ntiles || vt < ntiles || nd < ndq) {
+        bool moved = false;
+        if (nd < ndq && mbar_try_wait(&bar[R3_DS_FULL], nd & 1)) {
+          issue_dq(nd);
+          ++nd;
+          moved = true;
+        }
+        if (kt < ntiles && mbar_try_wait(&bar[R3_K_EMPTY + kt % C::KSTAGES], ((kt / C::KSTAGES) & 1) ^ 1)) {
+          uint64_t* fb = &bar[R3_K_FULL + kt % C::KSTAGES];
+          uint8_t* dst = sK + (kt % C::KSTAGES) * C::KB;
+          const int j0 = (kt_begin + kt) * BK;
+          mbar_arrive_expect_tx(fb, (uint32_t)C::KB);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * BK * 128, &tmK, fb, c * 64, j0, hk);
+          ++kt;
+          moved = true;
+        }
+        if (vt < ntiles && mbar_try_wait(&bar[R3_V_EMPTY + vt % C::VSTAGES], ((vt / C::VSTAGES) & 1) ^ 1)) {
+          uint64_t* fb = &bar[R3_V_FULL + vt % C::VSTAGES];
+          uint8_t* dst = sV + (vt % C::VSTAGES) * C::VB;
+          const int j0 = (kt_begin + vt) * BK;
+          mbar_arrive_expect_tx(fb, (uint32_t)C::VB);
+#pragma unroll
+          for (int c = 0; c < Dv / 64; ++c) tma_load_3d(dst + c * BK * 128, &tmV, fb, c * 64, j0, hk);
+          ++vt;
+          moved = true;
+        }
+        if (moved) {
+          t0 = globaltimer_ns();
+        } else {
+          if (*s_abort) break;
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *s_abort = 1;
+            record_error(p.err, kErrTimeout);
+            break;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ S/dP issuer
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t ID_S = idesc_f16(128, BK, false, false);
+      const uint32_t tQ = tbase + C::T_Q, tO = tbase + C::T_O;
+      const uint32_t tS = tbase + C::T_S, tP = tbase + C::T_P;
+      const bool ok = (MODE == 0 || wait(&bar[R3_Q_FULL], 0)) && wait(&bar[R3_OPS_READY], 0);
+      for (int t = 0; ok && t < ntiles; ++t) {
+        const int ks = t % C::KSTAGES, vs = t % C::VSTAGES;
+        if (!wait(&bar[R3_K_FULL + ks], (t / C::KSTAGES) & 1) || !wait(&bar[R3_S_FREE], (t & 1) ^ 1)) break;
+        tc_fence_after();
+        const uint32_t bk = smem_u32(sK + ks * C::KB);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t bd = sdesc_sw128(bk + (k / 4) * (BK * 128) + (k % 4) * 32, 16, 1024);
+          if (MODE == 1)
+            mma_f16(tS, sdesc_sw128(smem_u32(sQ) + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024), bd, ID_S, k > 0);
+          else
+            mma_f16_tmem_a(tS, tQ + k * 8, bd, ID_S, k > 0);
+        }
+        mma_commit(&bar[R3_S_FULL]);
+        if (MODE == 0) mma_commit(&bar[R3_K_EMPTY + ks]);  // the LSE pass reads K'(t) only here
+        if (!wait(&bar[R3_V_FULL + vs], (t / C::VSTAGES) & 1) || !wait(&bar[R3_P_FREE], (t & 1) ^ 1)) break;
+        tc_fence_after();
+        const uint32_t bv = smem_u32(sV + vs * C::VB);
+#pragma unroll
+        for (int k = 0; k < Dv / 16; ++k)
+          mma_f16_tmem_a(tP, tO + k * 8, sdesc_sw128(bv + (k / 4) * (BK * 128) + (k % 4) * 32, 16, 1024), ID_S,
+                         k > 0);
+        mma_commit(&bar[R3_P_FULL]);
+        mma_commit(&bar[R3_V_EMPTY + vs]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax
+    const int q4 = warp & 3, ch = (warp - 2) >> 2;  // ch < C::NCH
+    const int row = q4 * 32 + lane;
+    const int col0 = ch * 32;
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const int r = r0 + row;
+    const bool rvalid = r < R;
+    const int i = rvalid ? r / G : 0;
+    const int h = hk * G + (rvalid ? r % G : 0);
+    const long jlast = rvalid ? (p.causal ? min((long)p.M - 1, (long)p.M - p.N + i) : (long)p.M - 1) : -1;
+    const uint16_t* mrow = p.mask ? p.mask + ((size_t)(h % p.Hm) * p.N + i) * p.M : nullptr;
+    float lse2 = -CUDART_INF_F, dl = 0.f;
+    if (MODE == 1 && rvalid) {
+      lse2 = p.lse2[(size_t)hk * R + r];
+      dl = p.dlt[(size_t)hk * R + r];
+    }
+    const bool live = MODE == 1 ? (lse2 > -CUDART_INF_F) : rvalid;
+    const float c2 = st.c2, lam = st.lam, dq_fac = st.dq_fac;
+    // 2^(t2 + nlse2) = p (0 on a dead row); in the dQ pass the exponent also carries log2(lam),
+    // so the exponential yields lam * p directly (lam is a power of two)
+    const float nlse2 = live ? -lse2 + (MODE == 1 ? (float)ilogbf(lam) : 0.f) : -CUDART_INF_F;
+    const float t2off = MODE == 1 ? nlse2 : 0.f;
+    const uint32_t sS_u = smem_u32(sS);
+    float m2 = -CUDART_INF_F, l = 0.f, lc = 0.f, sd = 0.f, sdc = 0.f;
+
+    if (ntiles > 0) {
+      // this thread's share of the row's A operands into tensor memory (binary16 pairs per column)
+      auto put_row = [&](const __half* src, int DD, uint32_t tcol) {
+        const int wpr = DD / 2;
+        const int per = wpr / C::NCH;
+        const int w0 = per >= 32 ? ch * per : 0, nw = per >= 32 ? per : (ch == 0 ? wpr : 0);
+        const uint4* s4 = reinterpret_cast<const uint4*>(src) + w0 / 4;
+        for (int c = 0; c < nw; c += 32) {
+          uint32_t wv[32];
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            const uint4 u = rvalid ? __ldg(s4 + c / 4 + x) : make_uint4(0, 0, 0, 0);
+            wv[4 * x] = u.x, wv[4 * x + 1] = u.y, wv[4 * x + 2] = u.z, wv[4 * x + 3] = u.w;
+          }
+          tmem_st32(tbase + lane_off + tcol + w0 + c, wv);
+        }
+      };
+      const size_t rowq = (size_t)hk * R + (rvalid ? r : 0);
+      if (MODE == 0) put_row(p.q16 + rowq * D, D, C::T_Q);
+      put_row(p.do16 + rowq * Dv, Dv, C::T_O);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[R3_OPS_READY]);
+    }
+
+    for (int t = 0; t < ntiles; ++t) {
+      const int j0 = (kt_begin + t) * BK;
+      float s[32], dp[32];
+      if (!wait(&bar[R3_S_FULL], t & 1)) break;
+      tc_fence_after();
+      tmem_ld32(tbase + C::T_S + lane_off + col0, s);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[R3_S_FREE]);
+      // log2-domain scores (dQ pass: already minus lse, plus log2(lam)); masked keys -> -inf
+      if (mrow == nullptr && (long)(j0 + col0 + 31) <= jlast) {
+#pragma unroll
+        for (int n = 0; n < 32; ++n) s[n] = fmaf(s[n], c2, t2off);
+      } else {
+#pragma unroll
+        for (int n = 0; n < 32; ++n) {
+          const int j = j0 + col0 + n;
+          bool ok = (long)j <= jlast;
+          float mv = 0.f;
+          if (ok && mrow) {
+            mv = h2f(__ldg(reinterpret_cast<const unsigned short*>(mrow) + j));
+            ok = !(mv == -CUDART_INF_F);
+          }
+          s[n] = ok ? fmaf(s[n], c2, fmaf(mv, kLog2e, t2off)) : -CUDART_INF_F;
+        }
+      }
+      bool any = true;
+      if (MODE == 0) {
+        float cmax = -CUDART_INF_F;
+#pragma unroll
+        for (int n = 0; n < 32; ++n) cmax = fmaxf(cmax, s[n]);
+        if (cmax > m2) {
+          const float f = ex2(m2 - cmax);  // 0 while m2 = -inf
+          l *= f, lc *= f, sd *= f, sdc *= f;
+          m2 = cmax;
+        }
+        any = cmax > -CUDART_INF_F;
+        if (any) {
+#pragma unroll
+          for (int n = 0; n < 32; ++n) s[n] = ex2(s[n] - m2);
+        }
+      } else {
+#pragma unroll
+        for (int n = 0; n < 32; ++n) s[n] = ex2(s[n]);  // lam * p; 0 for masked keys, dead rows
+      }
+      if (!wait(&bar[R3_P_FULL], t & 1)) break;
+      tc_fence_after();
+      tmem_ld32(tbase + C::T_P + lane_off + col0, dp);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[R3_P_FREE]);
+      if (MODE == 0) {
+        if (any) {
+          float cl = 0.f, cs = 0.f;
+#pragma unroll
+          for (int n = 0; n < 32; ++n) {
+            cl += s[n];
+            cs = fmaf(s[n], dp[n], cs);
+          }
+          // compensated accumulation of the chunk sums
+          float y = cl - lc, tt = l + y;
+          lc = (tt - l) - y, l = tt;
+          y = cs - sdc, tt = sd + y;
+          sdc = (tt - sd) - y, sd = tt;
+        }
+      } else {
+        uint32_t pk[16];
+#pragma unroll
+        for (int n = 0; n < 32; n += 2)
+          pk[n / 2] = h2_as_u32(__floats2half2_rn(s[n] * (dp[n] - dl), s[n + 1] * (dp[n + 1] - dl)));
+        if (!wait(&bar[R3_DS_EMPTY], (t & 1) ^ 1)) break;
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+          sts_v4(sS_u + panel_off_u(128, row, col0 + 8 * x), pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[R3_DS_FULL]);
+      }
+      if (*s_abort) break;
+    }
+
+    // epilogue
+    if (MODE == 0) {
+      // merge the row's NCH chunk partials in chunk order
+      if (C::NCH > 1) {
+        if (ch > 0) {
+          float* m = s_merge + ((ch - 1) * 128 + row) * 3;
+          m[0] = m2, m[1] = l, m[2] = sd;
+        }
+        named_bar_sync(1, 32 * C::NSOFT);
+      }
+      if (ch == 0 && rvalid) {
+        float mm = m2;
+#pragma unroll
+        for (int c = 1; c < C::NCH; ++c) mm = fmaxf(mm, s_merge[((c - 1) * 128 + row) * 3]);
+        float L = 0.f, SD = 0.f;
+        if (mm > -CUDART_INF_F) {
+          const float fa = ex2(m2 - mm);
+          L = l * fa, SD = sd * fa;
+#pragma unroll
+          for (int c = 1; c < C::NCH; ++c) {
+            const float* m = s_merge + ((c - 1) * 128 + row) * 3;
+            const float fb = ex2(m[0] - mm);
+            L = fmaf(m[1], fb, L);
+            SD = fmaf(m[2], fb, SD);
+          }
+        }
+        float* o = p.part + (((size_t)split * p.Hkv + hk) * R + r) * 3;
+        o[0] = mm, o[1] = L, o[2] = SD;
+      }
+    } else {
+      float* out = !rvalid ? nullptr
+                   : p.nsplit == 1 ? p.dQ + ((size_t)i * p.H + h) * D
+                                   : p.dqpart + (((size_t)split * p.Hkv + hk) * R + r) * D;
+      const bool have = ntiles > 0 && wait(&bar[R3_ACC_FULL], 0);
+      if (have) tc_fence_after();
+#pragma unroll 1
+      for (int c = col0; c < D; c += 32 * C::NCH) {
         float v[32];
         if (have) {
           tmem_ld32(tbase + C::T_ACC + lane_off + c, v);

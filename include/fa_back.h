@@ -73,14 +73,22 @@ typedef enum {
   FA_ERR_DEVICE = 6,      /* the current device is not compute capability 10.3                  */
   FA_ERR_CUDA = 7,        /* a CUDA runtime call or kernel launch failed                        */
   FA_ERR_TIMEOUT = 8,     /* a kernel gave up on a bounded wait (see fa_back_get_error)         */
-  FA_ERR_WORKSPACE = 9    /* workspace is NULL or smaller than fa_back_workspace_size()         */
+  FA_ERR_WORKSPACE = 9    /* workspace is NULL or smaller than fa_back_workspace_size_min()     */
 } fa_status;
 
 /* Bytes in one cache row of `type` holding D values (-1 if D does not fit the format). */
 long fa_row_bytes(int type, int D);
 
-/* Workspace bytes fa_back() needs on the current device for this shape. */
+/* Workspace bytes of fa_back()'s fastest plan on the current device for this shape.  That plan
+ * holds binary16 copies of the decoded K and V cache (2 * Hkv * M * (D + Dv) bytes) beside the
+ * per-row statistics and split partials. */
 size_t fa_back_workspace_size(int N, int M, int H, int Hkv, int D, int Dv);
+
+/* The smallest workspace fa_back() accepts for this shape: its plan decodes the raw cache inside
+ * the row passes and does not split the keys.  A workspace between the two sizes gets the
+ * fastest plan that fits it; one plan and its results are fixed by the shape and
+ * workspace_bytes, so equal calls give bit-identical outputs. */
+size_t fa_back_workspace_size_min(int N, int M, int H, int Hkv, int D, int Dv);
 
 /*
  * The backward.  scale multiplies q.k before the mask is added (the reading used for the
@@ -123,8 +131,9 @@ int fa_back_profile_read(float* ms_sum, int* launches, const char** names, int m
  * file-scope device array of FA_NOALLOC_SCRATCH_BYTES (64 MiB), which every GPU that loads the
  * library holds until the process exits.  It calls no cudaMalloc, cudaFree or other allocating
  * routine; the caller still passes every input and output.
- *   - Problems whose fa_back_workspace_size() exceeds FA_NOALLOC_SCRATCH_BYTES are rejected
- *     with FA_ERR_WORKSPACE before anything is enqueued.
+ *   - The plan is fa_back()'s for a workspace of FA_NOALLOC_SCRATCH_BYTES: the fastest that
+ *     fits.  Problems whose fa_back_workspace_size_min() exceeds it are rejected with
+ *     FA_ERR_WORKSPACE before anything is enqueued.
  *   - The first call on a device looks up the array's device address with that device
  *     current; make that first call before any stream capture.
  *   - Every call on a device shares the one array, which keeps the last call's contents.

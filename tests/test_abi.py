@@ -27,7 +27,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
         ["fa_back", "fa_back_get_error", "fa_back_noalloc", "fa_back_profile", "fa_back_profile_read",
-         "fa_back_selftest_timeout", "fa_back_status_string", "fa_back_workspace_size", "fa_row_bytes"])
+         "fa_back_selftest_timeout", "fa_back_status_string", "fa_back_workspace_size",
+         "fa_back_workspace_size_min", "fa_row_bytes"])
 
 
 def test_every_declared_symbol_is_exported(L):
@@ -80,3 +81,11 @@ def test_workspace_size_grows_with_the_problem(L):
     b = fb.fa_back_workspace_size(2048, 75520, 24, 4, 256, 256)
     assert 0 < a < b
     assert fb.fa_back_workspace_size(8, 32, 6, 4, 64, 64) == 0  # H % Hkv != 0
+
+
+def test_minimum_workspace_leaves_out_the_binary16_cache_copy(L):
+    for N, M, H, Hkv, D, Dv in [(64, 512, 8, 2, 128, 128), (2048, 75520, 24, 4, 256, 256), (5, 1, 2, 1, 64, 64)]:
+        full = fb.fa_back_workspace_size(N, M, H, Hkv, D, Dv)
+        small = fb.fa_back_workspace_size_min(N, M, H, Hkv, D, Dv)
+        assert 0 < small < full
+        assert full - small >= 2 * Hkv * M * (D + Dv)

@@ -24,20 +24,20 @@ def fb():
     return m
 
 
-def run_gpu(fb, p, ws=None):
+def run_gpu(fb, p, ws=None, workspace_bytes=None):
     t = synth.device.to_torch(p, "cuda")
     out = fb.backward(t["q"], t["k"], p.k_type, t["v"], p.v_type, t["dO"], H=p.H, Hkv=p.Hkv, D=p.D, Dv=p.Dv,
                       M=p.M, scale=p.scale, causal=p.causal, mask=t["mask"], mask_heads=p.mask_heads,
-                      workspace=ws)
+                      workspace=ws, workspace_bytes=workspace_bytes)
     torch.cuda.synchronize()
     assert fb.fa_back_get_error() == 0
     return {k: v.cpu().numpy() for k, v in out.items()}
 
 
-def parity(fb, p, tol=NMSE_TOL):
+def parity(fb, p, tol=NMSE_TOL, workspace_bytes=None):
     import oracle
     ref = oracle.fa_back(p)
-    got = run_gpu(fb, p)
+    got = run_gpu(fb, p, workspace_bytes=workspace_bytes)
     res = check_components(got, ref, tol)
     dead = ~np.isfinite(ref["lse"])
     assert np.all(got["dQ"][dead] == 0.0)
@@ -75,6 +75,10 @@ EDGE = {
     # large-magnitude inputs (scales are chosen from the data)
     "big_values": dict(N=16, M=128, H=2, Hkv=1, D=64, Dv=64, k_type="f32", v_type="f32", q_sigma=300.0,
                        k_sigma=0.01, do_sigma=1e4, v_sigma=50.0),
+    # small-magnitude binary16 K and q8_0 V: their power-of-two operand scales exceed 2^16, which
+    # binary16 cannot hold (the decoders apply them in f32)
+    "small_f16k_q8v": dict(N=40, M=300, H=4, Hkv=2, D=128, Dv=128, k_type="f16", v_type="q8_0", k_sigma=0.004,
+                           v_sigma=0.003, causal=True),
 }
 
 
@@ -82,6 +86,22 @@ EDGE = {
 def test_edge_cases(fb, name):
     p = synth.make_problem(name, seed=2000 + sorted(EDGE).index(name), **EDGE[name])
     print(name, parity(fb, p))
+
+
+# The plan for the smallest workspace: row passes that decode the raw cache in shared memory.
+@pytest.mark.parametrize("name", ["d256_dv128", "d64_q4_mask_causal", "ragged_f16_causal", "small_f16k_q8v",
+                                  "finite_mask_hm1"])
+def test_edge_cases_minimum_workspace(fb, name):
+    p = synth.make_problem(name, seed=2000 + sorted(EDGE).index(name), **EDGE[name])
+    wmin = fb.fa_back_workspace_size_min(p.N, p.M, p.H, p.Hkv, p.D, p.Dv)
+    print(name, parity(fb, p, workspace_bytes=wmin))
+
+
+@pytest.mark.parametrize("cfg", ["1", "3"])
+def test_configs_minimum_workspace(fb, cfg):
+    p = synth.from_config(cfg)
+    wmin = fb.fa_back_workspace_size_min(p.N, p.M, p.H, p.Hkv, p.D, p.Dv)
+    print(cfg, parity(fb, p, workspace_bytes=wmin))
 
 
 @pytest.mark.parametrize("N,M", [(0, 64), (16, 0)])
@@ -103,7 +123,7 @@ def test_bit_identical_reruns(fb):
 def test_workspace_too_small_is_rejected(fb):
     p = synth.from_config("1")
     t = synth.device.to_torch(p, "cuda")
-    need = fb.fa_back_workspace_size(p.N, p.M, p.H, p.Hkv, p.D, p.Dv)
+    need = fb.fa_back_workspace_size_min(p.N, p.M, p.H, p.Hkv, p.D, p.Dv)
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
     outs = [torch.empty(1 << 20, device="cuda") for _ in range(5)]
     rc = fb.fa_back(t["q"].data_ptr(), t["k"].data_ptr(), p.k_type, t["v"].data_ptr(), p.v_type, None, 0,

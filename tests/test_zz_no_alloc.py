@@ -62,7 +62,7 @@ def test_noalloc_matches_fa_back_on_two_calls_in_a_row(fb):
 
 def test_noalloc_rejects_problems_beyond_its_scratch(fb):
     N, M, H, Hkv, D = 16384, 262144, 32, 8, 256
-    assert fb.fa_back_workspace_size(N, M, H, Hkv, D, D) > fb._native.NOALLOC_SCRATCH_BYTES
+    assert fb.fa_back_workspace_size_min(N, M, H, Hkv, D, D) > fb._native.NOALLOC_SCRATCH_BYTES
     rc = fb.fa_back_noalloc(0x1000, 0x2000, 2, 0x3000, 2, None, 0, 0x4000, 0.0625, N, M, H, Hkv, D, D, 1,
                             0x5000, 0x6000, 0x7000, 0x8000, 0x9000, None)
     assert fb.STATUS[rc] == "FA_ERR_WORKSPACE"
