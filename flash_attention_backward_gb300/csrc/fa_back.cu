@@ -35,9 +35,11 @@ struct Plan {
   int G, R, nQT, BK, nKT, nsplit, kt_per_split, nsplit_dq;
   int nblk_stats, nbv;
   int pre;  // 1: binary16 K'/V' copies in the workspace feed the row passes by TMA
+  int dsq;  // 1 (with pre): the dK/dV pass stores dS and dQ is one product over it (k_dq_gemm)
+  int ldds; // keys per stored dS row (M rounded up to 64)
   int nsm;
   size_t off_stats, off_rmean, off_rsh, off_dOr, off_lse2, off_dlt, off_part, off_dqpart, off_q16, off_do16,
-      off_bstat, off_vsum, off_kd, off_vd, total;
+      off_bstat, off_vsum, off_kd, off_vd, off_ds, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -65,17 +67,21 @@ static void layout(Plan& P, int M, int Hkv, int D, int Dv) {
   P.off_vsum = o; o = align256(o + sizeof(float) * (size_t)P.nbv * Hkv * Dv);
   P.off_kd = o; o = align256(o + (P.pre ? 2 * (size_t)Hkv * M * D : 0));
   P.off_vd = o; o = align256(o + (P.pre ? 2 * (size_t)Hkv * M * Dv : 0));
+  P.off_ds = o; o = align256(o + (P.dsq ? 2 * (size_t)Hkv * P.R * P.ldds : 0));
   P.total = o;
 }
 
-// Launch plan and workspace layout for one row-pass variant (pre: binary16 K'/V' copies).  The
+// Launch plan and workspace layout for one variant (level 2: stored dS and a dQ product over it;
+// 1: binary16 K'/V' copies feeding the row passes; 0: row passes decoding the raw cache).  The
 // keys of each row tile are split so that the last wave of CTAs (one per SM) wastes least,
 // counting a small cost per split for the partial merges; among split counts whose workspace
 // fits `ws_cap`, the cheapest is taken (1 if none fits).
-static Plan plan_variant(int N, int M, int H, int Hkv, int D, int Dv, int nsm, size_t ws_cap, int pre) {
+static Plan plan_variant(int N, int M, int H, int Hkv, int D, int Dv, int nsm, size_t ws_cap, int level) {
   Plan P;
   std::memset(&P, 0, sizeof(P));
-  P.pre = pre;
+  P.pre = level >= 1;
+  P.dsq = level >= 2;
+  P.ldds = (M + 63) / 64 * 64;
   P.nsm = nsm;
   P.G = H / Hkv;
   P.R = N * P.G;
@@ -108,12 +114,13 @@ static Plan plan_variant(int N, int M, int H, int Hkv, int D, int Dv, int nsm, s
   return P;
 }
 
-// The fastest plan whose workspace fits ws_cap: the producer-fed row passes over binary16 K'/V'
-// copies where they fit, else the row passes that decode the raw cache in shared memory (whose
-// one-split plan is the smallest workspace fa_back() accepts).
+// The fastest plan whose workspace fits ws_cap, trying the levels from 2 down; level 0 with one
+// split is the smallest workspace fa_back() accepts.
 static Plan make_plan(int N, int M, int H, int Hkv, int D, int Dv, int nsm, size_t ws_cap = SIZE_MAX) {
-  const Plan P = plan_variant(N, M, H, Hkv, D, Dv, nsm, ws_cap, 1);
-  if (P.total <= ws_cap) return P;
+  for (int level = 2; level > 0; --level) {
+    const Plan P = plan_variant(N, M, H, Hkv, D, Dv, nsm, ws_cap, level);
+    if (P.total <= ws_cap) return P;
+  }
   return plan_variant(N, M, H, Hkv, D, Dv, nsm, ws_cap, 0);
 }
 
@@ -161,13 +168,13 @@ static bool make_map(CUtensorMap* m, void* base, int d0, int d1, int d2, int row
 // measurement hook: one CUDA event before the sequence and one after each launch
 
 constexpr int kProfCalls = 256, kProfSlots = 16;
-// in launch order (the read-out measures each kernel from the previous recorded marker)
+// (the read-out measures each kernel from the marker recorded before it)
 static const char* const kKernelNames[kProfSlots] = {
     "k_row_stats", "k_vsum", "k_finalize", "k_convert", "k_predecode", "k_rows_lse", "k_lse_merge", "k_rows_dq",
-    "k_dq_reduce", "k_cols", "", "", "", "", "", ""};
+    "k_dq_reduce", "k_cols", "k_dq_gemm", "", "", "", "", ""};
 enum {
   KS_STATS = 0, KS_VSUM, KS_FINAL, KS_CONVERT, KS_PREDECODE, KS_ROWS_LSE, KS_MERGE, KS_ROWS_DQ, KS_DQ_REDUCE,
-  KS_COLS, KS_N
+  KS_COLS, KS_DQ_GEMM, KS_N
 };
 
 struct Profiler {
@@ -175,7 +182,8 @@ struct Profiler {
   bool on = false;
   int ncalls = 0;
   cudaEvent_t ev[kProfCalls][kProfSlots + 1];
-  bool used[kProfCalls][kProfSlots];
+  int order[kProfCalls][kProfSlots];  // slots in launch order
+  int nmarks[kProfCalls];
   bool created = false;
 };
 static Profiler g_prof;
@@ -194,14 +202,14 @@ struct CallRec {
       g_prof.created = true;
     }
     call = g_prof.ncalls++;
-    for (int k = 0; k < kProfSlots; ++k) g_prof.used[call][k] = false;
+    g_prof.nmarks[call] = 0;
     cudaEventRecord(g_prof.ev[call][kProfSlots], s);  // start marker
   }
   // kernel `slot` was just launched: its duration is measured from the previous marker
   void mark(int slot) {
-    if (call < 0) return;
+    if (call < 0 || g_prof.nmarks[call] >= kProfSlots) return;
     cudaEventRecord(g_prof.ev[call][slot], s);
-    g_prof.used[call][slot] = true;
+    g_prof.order[call][g_prof.nmarks[call]++] = slot;
   }
 };
 
@@ -274,8 +282,10 @@ static cudaError_t rows_pre(const Params& pl, const Params& pq, const Plan& P, c
   rec.mark(KS_ROWS_LSE);
   k_lse_merge<<<(unsigned)(((long)pl.Hkv * P.R + 255) / 256), 256, 0, s>>>(pl);
   rec.mark(KS_MERGE);
-  k_rows3<D, Dv, BK, 1><<<grid, FQ::NT, FQ::SMEM, s>>>(tmQ, tkq, tvq, pq);
-  rec.mark(KS_ROWS_DQ);
+  if (!P.dsq) {  // else dQ comes from the stored dS after the dK/dV pass
+    k_rows3<D, Dv, BK, 1><<<grid, FQ::NT, FQ::SMEM, s>>>(tmQ, tkq, tvq, pq);
+    rec.mark(KS_ROWS_DQ);
+  }
   return cudaSuccess;
 }
 
@@ -332,14 +342,25 @@ static cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& 
   cudaError_t e = P.pre ? rows_pre<D, Dv, BK, BKL>(pl, pq, P, tmQ, grid, s, rec)
                         : rows_raw<D, Dv, BK, BKL>(pl, pq, P, tmQ, grid, s, rec);
   if (e != cudaSuccess) return e;
+  CUtensorMap tmS;  // stored dS [Hkv][R][ldds] (level 2 only)
+  std::memset(&tmS, 0, sizeof(tmS));
+  if (P.dsq && !make_map(&tmS, p.ds, p.ldds, P.R, p.Hkv)) return cudaErrorInvalidValue;
+  if (P.nKT > 0) {
+    if ((e = set_smem(k_cols2<D, Dv, BK>, CC::SMEM)) != cudaSuccess) return e;
+    k_cols2<D, Dv, BK><<<dim3(P.nKT, p.Hkv), 384, CC::SMEM, s>>>(tmQ, tmO, tmS, p);
+    rec.mark(KS_COLS);
+  }
+  if (P.dsq) {
+    using GC = GemmCfg<D, BK>;
+    CUtensorMap tkg;
+    if (!make_map(&tkg, p.kd, D, p.M, p.Hkv, BK)) return cudaErrorInvalidValue;
+    if ((e = set_smem(k_dq_gemm<D, BK>, GC::SMEM)) != cudaSuccess) return e;
+    k_dq_gemm<D, BK><<<grid, 256, GC::SMEM, s>>>(tmS, tkg, p);
+    rec.mark(KS_DQ_GEMM);
+  }
   if (P.nsplit_dq > 1) {
     k_dq_reduce<<<(unsigned)(((long)p.Hkv * P.R * (D / 4) + 255) / 256), 256, 0, s>>>(p);
     rec.mark(KS_DQ_REDUCE);
-  }
-  if (P.nKT > 0) {
-    if ((e = set_smem(k_cols2<D, Dv, BK>, CC::SMEM)) != cudaSuccess) return e;
-    k_cols2<D, Dv, BK><<<dim3(P.nKT, p.Hkv), 384, CC::SMEM, s>>>(tmQ, tmO, p);
-    rec.mark(KS_COLS);
   }
   return cudaGetLastError();
 }
@@ -475,6 +496,8 @@ extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, 
   p.rsh = reinterpret_cast<float*>(ws + P.off_rsh);
   p.kd = P.pre ? reinterpret_cast<__half*>(ws + P.off_kd) : nullptr;
   p.vd = P.pre ? reinterpret_cast<__half*>(ws + P.off_vd) : nullptr;
+  p.ds = P.dsq ? reinterpret_cast<__half*>(ws + P.off_ds) : nullptr;
+  p.ldds = P.ldds;
   p.raw_bulk = (rbk % 16 == 0 && rbv % 16 == 0 && rbk <= 2048 && rbv <= 2048) ? 1 : 0;
   p.rbk_pad = (int)((rbk + 15) / 16 * 16);
   p.rbv_pad = (int)((rbv + 15) / 16 * 16);
@@ -545,8 +568,8 @@ extern "C" int fa_back_profile_read(float* ms_sum, int* launches, const char** n
   }
   for (int c = 0; c < g_prof.ncalls; ++c) {
     int prev = kProfSlots;  // start marker
-    for (int k = 0; k < KS_N; ++k) {
-      if (!g_prof.used[c][k]) continue;
+    for (int m = 0; m < g_prof.nmarks[c]; ++m) {
+      const int k = g_prof.order[c][m];
       float ms = 0.f;
       if (cudaEventSynchronize(g_prof.ev[c][k]) == cudaSuccess &&
           cudaEventElapsedTime(&ms, g_prof.ev[c][prev], g_prof.ev[c][k]) == cudaSuccess && k < n) {

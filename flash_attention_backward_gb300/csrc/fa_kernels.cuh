@@ -75,6 +75,8 @@ struct Params {
   float* rsh;     // [Hkv][Dv]  -r' * sV, an exact binary16 value (the decoders' V shift)
   __half* kd;     // [Hkv][M][D]   binary16 K' = k^ sK (producer-fed row passes; else null)
   __half* vd;     // [Hkv][M][Dv]  binary16 V' = v^ sV - r' sV
+  __half* ds;     // [Hkv][R][ldds] binary16 lam * dS from the dK/dV pass, read by k_dq_gemm (or null)
+  int ldds;       // keys per dS row: M rounded up to 64
   // raw K/V staging of the row passes
   int raw_bulk;        // 1: rows are 16-byte multiples, copied by bulk async copies; 0: 4-byte async copies
   int rbk_pad, rbv_pad;  // raw row strides in shared memory (16-byte multiples)
@@ -1648,8 +1650,10 @@ __global__ void __launch_bounds__(256) k_dq_reduce(Params p) {
 // Q and dO arrive as 64-column TMA panels with one full/empty barrier pair each; a panel is
 // released when the last product reading it completes, so the next tile's loads overlap this
 // tile's final products without a second buffer.
-// Warp roles (16 warps): 0 producer, 1 MMA issuer / tensor-memory owner, 4-11 softmax and
-// epilogue, every warp decodes K' and V' at the start.
+// Warp roles (12 warps): 0 producer, 1 MMA issuer / tensor-memory owner, 4-11 softmax and
+// epilogue, every warp decodes K' and V' at the start.  Where the plan keeps dS for a separate
+// dQ product (p.ds), warp 2 stores each tile's dS panels to it with TMA, and the dS buffer is
+// released only once both the gradient products and that store have read it.
 
 template <int D, int Dv, int BK>
 struct Cols2Cfg {
@@ -1678,7 +1682,8 @@ enum {
 
 template <int D, int Dv, int BK>
 __global__ void __launch_bounds__(384, 1)
-    k_cols2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO, Params p) {
+    k_cols2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
+            const __grid_constant__ CUtensorMap tmS, Params p) {
   using C = Cols2Cfg<D, Dv, BK>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -1713,7 +1718,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(&bar[C_S_FULL], 1);
     mbar_init(&bar[C_DS_FULL], 8);
-    mbar_init(&bar[C_DS_EMPTY], 1);
+    mbar_init(&bar[C_DS_EMPTY], p.ds ? 2 : 1);
     mbar_init(&bar[C_DONE], 1);
     *s_abort = 0;
     fence_mbar_init();
@@ -1805,6 +1810,20 @@ __global__ void __launch_bounds__(384, 1)
         mma_commit(&bar[C_DS_EMPTY]);
       }
       mma_commit(&bar[C_DONE]);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------------ dS store (dQ by GEMM)
+    if (lane == 0 && p.ds) {
+      prefetch_tmap(&tmS);
+      for (int t = 0; t < nq; ++t) {
+        if (!wait(&bar[C_DS_FULL], t & 1)) break;
+#pragma unroll
+        for (int c = 0; c < BK / 64; ++c) tma_store_3d(&tmS, sS + c * (128 * 128), j0 + c * 64, (qt_begin + t) * 128, hk);
+        bulk_commit_group();
+        bulk_wait_read_all();  // the panels may be overwritten once read
+        mbar_arrive(&bar[C_DS_EMPTY]);
+      }
+      bulk_wait_all();
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax, then epilogue
@@ -1943,6 +1962,141 @@ __global__ void k_wait_selftest(int* err, unsigned long long limit_ns) {
 __global__ void k_fill(float* x, long n, float v) {
   const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx < n) x[idx] = v;
+}
+
+// ------------------------------------------------------------------------------------------------
+// dQ as one product over the stored dS: dQ_r = dq_fac * sum_j dS'_rj K'_j per (row tile, KV head,
+// key split), over the key tiles the row tile can see.  dS' (binary16 lam * dS, written by the
+// dK/dV pass) is the A operand (K-major, 64-key panels); K' is the B operand (MN-major).  Both
+// arrive by TMA into a ring of stages; the accumulator is the whole 128 x D tile in tensor memory.
+// Warp roles: 0 producer, 1 tensor-memory owner and MMA issuer, 4-7 epilogue.
+
+template <int D, int BK>
+struct GemmCfg {
+  static constexpr int AB = 128 * BK * 2, BB = BK * D * 2, SB = AB + BB;  // bytes of one stage
+  static constexpr int FIT = (232448 - 1024 - 256) / SB;
+  static constexpr int NST = FIT < 6 ? FIT : 6;
+  static constexpr int OFF_BAR = NST * SB;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;  // + 1024 for aligning the base
+  static constexpr int TCOLS = pow2_at_least(D);
+  static_assert(NST >= 2 && SMEM <= 232448, "shared memory budget");
+};
+
+enum { G_FULL = 0, G_EMPTY = 6, G_ACC = 12, G_COUNT };
+
+template <int D, int BK>
+__global__ void __launch_bounds__(256, 1)
+    k_dq_gemm(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmK, Params p) {
+  using C = GemmCfg<D, BK>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 8 * G_COUNT);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + C::OFF_BAR + 8 * G_COUNT + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qt = blockIdx.x, hk = blockIdx.y, split = blockIdx.z;
+  const int r0 = qt * 128;
+  const int R = p.R, G = p.G;
+  const int kt_begin = split * p.kt_per_split;
+  int kt_end = min(p.nKT, kt_begin + p.kt_per_split);
+  if (p.causal) {
+    const long i_hi = (long)min(R - 1, r0 + 127) / G;
+    const long jmax = (long)p.M - p.N + i_hi;
+    kt_end = min(kt_end, jmax < 0 ? 0 : (int)(jmax / BK) + 1);
+  }
+  const int ntiles = max(0, kt_end - kt_begin);
+
+  if (warp == 1) tmem_alloc(tslot, C::TCOLS);
+  if (tid == 0) {
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(&bar[G_FULL + s], 1);
+      mbar_init(&bar[G_EMPTY + s], 1);
+    }
+    mbar_init(&bar[G_ACC], 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  const Waiter wait{s_abort, p.err};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmS);
+      prefetch_tmap(&tmK);
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % C::NST;
+        if (!wait(&bar[G_EMPTY + s], ((t / C::NST) & 1) ^ 1)) break;
+        uint8_t* a = sm + s * C::SB;
+        uint8_t* b = a + C::AB;
+        const int j0 = (kt_begin + t) * BK;
+        mbar_arrive_expect_tx(&bar[G_FULL + s], (uint32_t)C::SB);
+#pragma unroll
+        for (int c = 0; c < BK / 64; ++c) tma_load_3d(a + c * (128 * 128), &tmS, &bar[G_FULL + s], j0 + c * 64, r0, hk);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) tma_load_3d(b + c * (BK * 128), &tmK, &bar[G_FULL + s], c * 64, j0, hk);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t ID = idesc_f16(128, D, false, true);
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % C::NST;
+        if (!wait(&bar[G_FULL + s], (t / C::NST) & 1)) break;
+        tc_fence_after();
+        const uint32_t a = smem_u32(sm + s * C::SB), b = a + C::AB;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)
+          mma_f16(tbase, sdesc_sw128(a + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024),
+                  sdesc_sw128(b + k * 2048, BK * 128, 1024), ID, (t > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&bar[G_EMPTY + s]);
+      }
+      mma_commit(&bar[G_ACC]);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------------ epilogue
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int r = r0 + row;
+    const bool rvalid = r < R;
+    const int i = rvalid ? r / G : 0;
+    const int h = hk * G + (rvalid ? r % G : 0);
+    float* out = !rvalid ? nullptr
+                 : p.nsplit == 1 ? p.dQ + ((size_t)i * p.H + h) * D
+                                 : p.dqpart + (((size_t)split * p.Hkv + hk) * R + r) * D;
+    const float dq_fac = p.st->dq_fac;
+    const bool have = ntiles > 0 && wait(&bar[G_ACC], 0);
+    if (have) tc_fence_after();
+#pragma unroll 1
+    for (int c = 0; c < D; c += 32) {
+      float v[32];
+      if (have) {
+        tmem_ld32(tbase + lane_off + c, v);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = 0.f;
+      }
+      if (out) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(out + c + e) =
+              make_float4(v[e] * dq_fac, v[e + 1] * dq_fac, v[e + 2] * dq_fac, v[e + 3] * dq_fac);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::TCOLS);
+  }
 }
 
 }  // namespace fab

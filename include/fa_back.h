@@ -79,9 +79,11 @@ typedef enum {
 /* Bytes in one cache row of `type` holding D values (-1 if D does not fit the format). */
 long fa_row_bytes(int type, int D);
 
-/* Workspace bytes of fa_back()'s fastest plan on the current device for this shape.  That plan
- * holds binary16 copies of the decoded K and V cache (2 * Hkv * M * (D + Dv) bytes) beside the
- * per-row statistics and split partials. */
+/* Workspace bytes of fa_back()'s fastest plan on the current device for this shape.  Beside the
+ * per-row statistics and split partials, that plan holds binary16 copies of the decoded K and V
+ * cache (2 * Hkv * M * (D + Dv) bytes) and the binary16 dS of every row and key (2 * N * H * M'
+ * bytes, M' = M rounded up to 64), from which dQ is one product.  A workspace too small for dS
+ * but large enough for the K/V copies gets the plan that recomputes dS in a dQ pass. */
 size_t fa_back_workspace_size(int N, int M, int H, int Hkv, int D, int Dv);
 
 /* The smallest workspace fa_back() accepts for this shape: its plan decodes the raw cache inside

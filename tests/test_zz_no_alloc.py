@@ -78,3 +78,25 @@ def test_noalloc_long_context_within_the_scratch(fb):
     ref = _with_workspace(fb, p, t)
     got = _noalloc(fb, p, t)
     check_components(got, ref, NMSE_TOL)
+
+
+def test_noalloc_middle_plan_parity(fb):
+    """A shape whose stored dS (2 N H M bytes) exceeds the 64 MiB scratch while the binary16 K/V
+    copies fit: the plan recomputes dS in a dQ pass (k_rows_dq).  Sampled rows and keys against
+    the oracle."""
+    import oracle
+    p = synth.make_problem("middle", N=256, M=17000, H=8, Hkv=2, D=128, Dv=128, k_type="q8_0", v_type="q8_0",
+                           causal=True, seed=77)
+    assert 2 * p.N * p.H * p.M > fb._native.NOALLOC_SCRATCH_BYTES
+    t = synth.device.to_torch(p, "cuda")
+    fb.fa_back_profile(True)
+    got = _noalloc(fb, p, t)
+    fb.fa_back_profile(False)
+    launched = {k for k, v in fb.fa_back_profile_read().items() if v[1] > 0}
+    assert "k_rows_dq" in launched and "k_dq_gemm" not in launched, launched
+    rows = synth.sample_indices(78, synth.gen.S_SAMPLE, p.N, 48)
+    keys = synth.sample_indices(78, synth.gen.S_SAMPLE + 1, p.M, 128)
+    ref = oracle.fa_back(p, dq_rows=rows, dkv_keys=keys)
+    sub = {"lse": got["lse"], "delta": got["delta"], "dQ": got["dQ"][rows], "dK": got["dK"][keys],
+           "dV": got["dV"][keys]}
+    print(check_components(sub, ref, NMSE_TOL))
