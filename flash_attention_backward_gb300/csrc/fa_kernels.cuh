@@ -765,11 +765,12 @@ __global__ void __launch_bounds__(Rows2Cfg<D, Dv, BK, MODE>::NT, 1)
     if constexpr (MODE != 1) return;  // only the dQ pass has the accumulator and the dS panel
     constexpr uint32_t ID_DQ = idesc_f16(128, D, false, true);
     tc_fence_after();
-    const uint32_t kp = smem_u32(sK + (t % C::KSTAGES) * C::KB);
+    const uint64_t da = sdesc_sw128(smem_u32(sS), 16, 1024);
+    const uint64_t db = sdesc_sw128(smem_u32(sK + (t % C::KSTAGES) * C::KB), BK * 128, 1024);
 #pragma unroll
     for (int k = 0; k < BK / 16; ++k)
-      mma_f16(tbase + C::T_ACC, sdesc_sw128(smem_u32(sS) + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024),
-              sdesc_sw128(kp + k * 2048, BK * 128, 1024), ID_DQ, (t > 0 || k > 0) ? 1u : 0u);
+      mma_f16(tbase + C::T_ACC, sdesc_adv(da, (k / 4) * (128 * 128) + (k % 4) * 32), sdesc_adv(db, k * 2048), ID_DQ,
+              (t > 0 || k > 0) ? 1u : 0u);
     if (t == ntiles - 1) {
       mma_commit(&bar[B_ACC_FULL]);
     } else {
@@ -877,12 +878,13 @@ __global__ void __launch_bounds__(Rows2Cfg<D, Dv, BK, MODE>::NT, 1)
       auto issue_s = [&](int t) {
         const uint32_t tS = tbase + C::T_S + 2 * BK * (t % C::NSLOT);
         tc_fence_after();
-        const uint32_t bk = smem_u32(sK + (t % C::KSTAGES) * C::KB);
+        const uint64_t db = sdesc_sw128(smem_u32(sK + (t % C::KSTAGES) * C::KB), 16, 1024);
+        const uint64_t da = sdesc_sw128(smem_u32(sQ), 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint64_t bd = sdesc_sw128(bk + (k / 4) * (BK * 128) + (k % 4) * 32, 16, 1024);
+          const uint64_t bd = sdesc_adv(db, (k / 4) * (BK * 128) + (k % 4) * 32);
           if (MODE == 1)
-            mma_f16(tS, sdesc_sw128(smem_u32(sQ) + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024), bd, ID_S, k > 0);
+            mma_f16(tS, sdesc_adv(da, (k / 4) * (128 * 128) + (k % 4) * 32), bd, ID_S, k > 0);
           else
             mma_f16_tmem_a(tS, tQ + k * 8, bd, ID_S, k > 0);
         }
@@ -893,11 +895,10 @@ __global__ void __launch_bounds__(Rows2Cfg<D, Dv, BK, MODE>::NT, 1)
         const int vs = t % C::VSTAGES, sl = t % C::NSLOT;
         const uint32_t tP = tbase + C::T_S + 2 * BK * sl + BK;
         tc_fence_after();
-        const uint32_t bv = smem_u32(sV + vs * C::VB);
+        const uint64_t dv = sdesc_sw128(smem_u32(sV + vs * C::VB), 16, 1024);
 #pragma unroll
         for (int k = 0; k < Dv / 16; ++k)
-          mma_f16_tmem_a(tP, tO + k * 8, sdesc_sw128(bv + (k / 4) * (BK * 128) + (k % 4) * 32, 16, 1024), ID_S,
-                         k > 0);
+          mma_f16_tmem_a(tP, tO + k * 8, sdesc_adv(dv, (k / 4) * (BK * 128) + (k % 4) * 32), ID_S, k > 0);
         mma_commit(&bar[B_S_FULL + sl]);
         mma_commit(&bar[B_V_EMPTY + vs]);
       };
@@ -1303,11 +1304,12 @@ __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
       auto issue_dq = [&](int t) {
         constexpr uint32_t ID_DQ = idesc_f16(128, D, false, true);
         tc_fence_after();
-        const uint32_t kp = smem_u32(sK + (t % C::KSTAGES) * C::KB);
+        const uint64_t da = sdesc_sw128(smem_u32(sS), 16, 1024);
+        const uint64_t db = sdesc_sw128(smem_u32(sK + (t % C::KSTAGES) * C::KB), BK * 128, 1024);
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k)
-          mma_f16(tbase + C::T_ACC, sdesc_sw128(smem_u32(sS) + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024),
-                  sdesc_sw128(kp + k * 2048, BK * 128, 1024), ID_DQ, (t > 0 || k > 0) ? 1u : 0u);
+          mma_f16(tbase + C::T_ACC, sdesc_adv(da, (k / 4) * (128 * 128) + (k % 4) * 32), sdesc_adv(db, k * 2048),
+                  ID_DQ, (t > 0 || k > 0) ? 1u : 0u);
         if (t == ntiles - 1) {
           mma_commit(&bar[R3_ACC_FULL]);
         } else {
@@ -1368,12 +1370,13 @@ __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
         const int ks = t % C::KSTAGES, vs = t % C::VSTAGES;
         if (!wait(&bar[R3_K_FULL + ks], (t / C::KSTAGES) & 1) || !wait(&bar[R3_S_FREE], (t & 1) ^ 1)) break;
         tc_fence_after();
-        const uint32_t bk = smem_u32(sK + ks * C::KB);
+        const uint64_t db = sdesc_sw128(smem_u32(sK + ks * C::KB), 16, 1024);
+        const uint64_t da = sdesc_sw128(smem_u32(sQ), 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint64_t bd = sdesc_sw128(bk + (k / 4) * (BK * 128) + (k % 4) * 32, 16, 1024);
+          const uint64_t bd = sdesc_adv(db, (k / 4) * (BK * 128) + (k % 4) * 32);
           if (MODE == 1)
-            mma_f16(tS, sdesc_sw128(smem_u32(sQ) + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024), bd, ID_S, k > 0);
+            mma_f16(tS, sdesc_adv(da, (k / 4) * (128 * 128) + (k % 4) * 32), bd, ID_S, k > 0);
           else
             mma_f16_tmem_a(tS, tQ + k * 8, bd, ID_S, k > 0);
         }
@@ -1381,11 +1384,10 @@ __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
         if (MODE == 0) mma_commit(&bar[R3_K_EMPTY + ks]);  // the LSE pass reads K'(t) only here
         if (!wait(&bar[R3_V_FULL + vs], (t / C::VSTAGES) & 1) || !wait(&bar[R3_P_FREE], (t & 1) ^ 1)) break;
         tc_fence_after();
-        const uint32_t bv = smem_u32(sV + vs * C::VB);
+        const uint64_t dv = sdesc_sw128(smem_u32(sV + vs * C::VB), 16, 1024);
 #pragma unroll
         for (int k = 0; k < Dv / 16; ++k)
-          mma_f16_tmem_a(tP, tO + k * 8, sdesc_sw128(bv + (k / 4) * (BK * 128) + (k % 4) * 32, 16, 1024), ID_S,
-                         k > 0);
+          mma_f16_tmem_a(tP, tO + k * 8, sdesc_adv(dv, (k / 4) * (BK * 128) + (k % 4) * 32), ID_S, k > 0);
         mma_commit(&bar[R3_P_FULL]);
         mma_commit(&bar[R3_V_EMPTY + vs]);
       }
@@ -1764,8 +1766,11 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t LBO_O = Dv >= 128 ? 128 * 128 : 0;  // second 64-row block of dO^T (repeat if Dv = 64)
       constexpr uint32_t LBO_Q = D >= 128 ? 128 * 128 : 0;
       const uint32_t tS = tbase + C::T_S, tP = tbase + C::T_P, tV = tbase + C::T_V, tK = tbase + C::T_K;
-      const uint32_t aq = smem_u32(sQ), ao = smem_u32(sO), bk = smem_u32(sK), bv = smem_u32(sV),
-                     bp = smem_u32(sP), bs = smem_u32(sS);
+      // operand descriptors (K-major for S and dP; MN-major Q^T, dO^T and dS, P for the gradients)
+      const uint64_t dq0 = sdesc_sw128(smem_u32(sQ), 16, 1024), do0 = sdesc_sw128(smem_u32(sO), 16, 1024),
+                     dk0 = sdesc_sw128(smem_u32(sK), 16, 1024), dv0 = sdesc_sw128(smem_u32(sV), 16, 1024),
+                     dqt = sdesc_sw128(smem_u32(sQ), LBO_Q, 1024), dot = sdesc_sw128(smem_u32(sO), LBO_O, 1024),
+                     ds0 = sdesc_sw128(smem_u32(sS), 128 * 128, 1024), dp0 = sdesc_sw128(smem_u32(sP), 128 * 128, 1024);
       for (int t = 0; t < nq; ++t) {
         bool ok = true;
         for (int c = 0; ok && c < C::NQP; ++c) {
@@ -1773,16 +1778,16 @@ __global__ void __launch_bounds__(384, 1)
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_f16(tS, sdesc_sw128(aq + c * (128 * 128) + k * 32, 16, 1024),
-                    sdesc_sw128(bk + c * (BK * 128) + k * 32, 16, 1024), ID_S, (c > 0 || k > 0) ? 1u : 0u);
+            mma_f16(tS, sdesc_adv(dq0, c * (128 * 128) + k * 32), sdesc_adv(dk0, c * (BK * 128) + k * 32), ID_S,
+                    (c > 0 || k > 0) ? 1u : 0u);
         }
         for (int c = 0; ok && c < C::NOP; ++c) {
           if (!(ok = wait(&bar[C_O_FULL + c], t & 1))) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_f16(tP, sdesc_sw128(ao + c * (128 * 128) + k * 32, 16, 1024),
-                    sdesc_sw128(bv + c * (BK * 128) + k * 32, 16, 1024), ID_S, (c > 0 || k > 0) ? 1u : 0u);
+            mma_f16(tP, sdesc_adv(do0, c * (128 * 128) + k * 32), sdesc_adv(dv0, c * (BK * 128) + k * 32), ID_S,
+                    (c > 0 || k > 0) ? 1u : 0u);
         }
         if (!ok) break;
         mma_commit(&bar[C_S_FULL]);
@@ -1793,8 +1798,8 @@ __global__ void __launch_bounds__(384, 1)
         for (int hh = 0; hh < C::NDH; ++hh) {
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_f16(tK + hh * BK, sdesc_sw128(aq + hh * 2 * (128 * 128) + k * 2048, LBO_Q, 1024),
-                    sdesc_sw128(bs + k * 2048, 128 * 128, 1024), ID_T, (acc0 || k > 0) ? 1u : 0u);
+            mma_f16(tK + hh * BK, sdesc_adv(dqt, hh * 2 * (128 * 128) + k * 2048), sdesc_adv(ds0, k * 2048), ID_T,
+                    (acc0 || k > 0) ? 1u : 0u);
           mma_commit(&bar[C_Q_EMPTY + 2 * hh]);
           if (2 * hh + 1 < C::NQP) mma_commit(&bar[C_Q_EMPTY + 2 * hh + 1]);
         }
@@ -1802,8 +1807,8 @@ __global__ void __launch_bounds__(384, 1)
         for (int hh = 0; hh < C::NVH; ++hh) {
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_f16(tV + hh * BK, sdesc_sw128(ao + hh * 2 * (128 * 128) + k * 2048, LBO_O, 1024),
-                    sdesc_sw128(bp + k * 2048, 128 * 128, 1024), ID_T, (acc0 || k > 0) ? 1u : 0u);
+            mma_f16(tV + hh * BK, sdesc_adv(dot, hh * 2 * (128 * 128) + k * 2048), sdesc_adv(dp0, k * 2048), ID_T,
+                    (acc0 || k > 0) ? 1u : 0u);
           mma_commit(&bar[C_O_EMPTY + 2 * hh]);
           if (2 * hh + 1 < C::NOP) mma_commit(&bar[C_O_EMPTY + 2 * hh + 1]);
         }
@@ -2049,11 +2054,12 @@ __global__ void __launch_bounds__(256, 1)
         const int s = t % C::NST;
         if (!wait(&bar[G_FULL + s], (t / C::NST) & 1)) break;
         tc_fence_after();
-        const uint32_t a = smem_u32(sm + s * C::SB), b = a + C::AB;
+        const uint64_t da = sdesc_sw128(smem_u32(sm + s * C::SB), 16, 1024);
+        const uint64_t db = sdesc_sw128(smem_u32(sm + s * C::SB + C::AB), BK * 128, 1024);
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k)
-          mma_f16(tbase, sdesc_sw128(a + (k / 4) * (128 * 128) + (k % 4) * 32, 16, 1024),
-                  sdesc_sw128(b + k * 2048, BK * 128, 1024), ID, (t > 0 || k > 0) ? 1u : 0u);
+          mma_f16(tbase, sdesc_adv(da, (k / 4) * (128 * 128) + (k % 4) * 32), sdesc_adv(db, k * 2048), ID,
+                  (t > 0 || k > 0) ? 1u : 0u);
         mma_commit(&bar[G_EMPTY + s]);
       }
       mma_commit(&bar[G_ACC]);

@@ -242,6 +242,10 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Descriptor `d` with its start address advanced by `bytes` (a multiple of 16; shared-memory
+// addresses stay below 2^18, so the 14-bit address field does not carry into the next field).
+__device__ __forceinline__ uint64_t sdesc_adv(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
 // Instruction descriptor: f16 x f16 -> f32, M x N tile, operand majorness (false = K-major).
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
   return (1u << 4) | (0u << 7) | (0u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
