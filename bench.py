@@ -13,6 +13,7 @@ own GPU (the operation has no exchange step); value = work of all ranks / slowes
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -47,10 +48,11 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms while running; the summary
+    keeps the samples taken inside the marked region (mark_start / mark_end)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -62,10 +64,20 @@ class ClockSampler:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.file, stderr=subprocess.DEVNULL)
+            t0 = time.time()
+            while time.time() - t0 < 3.0 and os.path.getsize(self.file.name) == 0:  # wait for the first sample
+                time.sleep(0.02)
         except Exception:
             self.proc = None
+        self.t_start = self.t_end = None
         return self
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -81,6 +93,17 @@ class ClockSampler:
         self.file.flush()
         rows = [ln.strip().split(",") for ln in open(self.file.name) if ln.strip()]
         os.unlink(self.file.name)
+        def when(r):
+            try:
+                return datetime.datetime.strptime(r[9].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except (ValueError, IndexError):
+                return None
+        if self.t_start is not None and self.t_end is not None:
+            inside = [r for r in rows if when(r) is not None and self.t_start <= when(r) <= self.t_end + 0.01]
+            if not inside:  # a region shorter than the sampling period: the first sample after it starts
+                after = [r for r in rows if when(r) is not None and when(r) >= self.t_start]
+                inside = after[:1]
+            rows = inside
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
@@ -253,11 +276,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     fb.fa_back_profile(True)
     with ClockSampler(local) as clk:
+        clk.mark_start()
         ev0.record(stream)
         for _ in range(args.steps):
             step()
         ev1.record(stream)
         torch.cuda.synchronize()
+        clk.mark_end()
     fb.fa_back_profile(False)
     kern = fb.fa_back_profile_read()
     ms = ev0.elapsed_time(ev1) / args.steps
