@@ -510,7 +510,7 @@ extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, 
   rec.begin(s);
   k_row_stats<<<P.nblk_stats, 256, 0, s>>>(p);
   rec.mark(KS_STATS);
-  k_vsum<<<(unsigned)((P.nbv * Hkv + 7) / 8), 256, 0, s>>>(p);
+  k_vsum<<<(unsigned)(P.nbv * Hkv), 256, 0, s>>>(p);
   rec.mark(KS_VSUM);
   k_finalize<<<1, 1024, 0, s>>>(p);
   rec.mark(KS_FINAL);

@@ -415,29 +415,42 @@ __global__ void __launch_bounds__(256) k_row_stats(Params p) {
   const long nQ = (long)p.N * p.H, nK = (long)p.M * p.Hkv;
   const long tot = 2 * nQ + 2 * nK;
   float amax[4] = {0, 0, 0, 0}, nrm[4] = {0, 0, 0, 0};
-  for (long rw = (long)blockIdx.x * 8 + warp; rw < tot; rw += (long)gridDim.x * 8) {
-    int t;
-    long r;
-    if (rw < nQ) t = 0, r = rw;
-    else if (rw < 2 * nQ) t = 1, r = rw - nQ;
-    else if (rw < 2 * nQ + nK) t = 2, r = rw - 2 * nQ;
-    else t = 3, r = rw - 2 * nQ - nK;
-    const int DD = (t == 0 || t == 2) ? p.D : p.Dv;
-    float am = 0.f, ss = 0.f;
-    const int c0 = lane * 8;
-    if (c0 < DD) {
-      float x[8];
-      if (t == 0) decode8_f(reinterpret_cast<const uint8_t*>(p.q + r * p.D), kTypeF32, c0, x);
-      else if (t == 1) decode8_f(reinterpret_cast<const uint8_t*>(p.dO + r * p.Dv), kTypeF32, c0, x);
-      else if (t == 2) decode8_f(p.k + r * p.rbk, p.k_type, c0, x);
-      else decode8_f(p.v + r * p.rbv, p.v_type, c0, x);
+  const int c0 = lane * 8;
+  // four rows per step: their loads are issued before any of their reductions
+  const long step = (long)gridDim.x * 8;
+  for (long rw0 = (long)blockIdx.x * 8 + warp; rw0 < tot; rw0 += 4 * step) {
+    float x[4][8];
+    int tt[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(x[e])), ss = fmaf(x[e], x[e], ss);
+    for (int u = 0; u < 4; ++u) {
+      const long rw = rw0 + u * step;
+      int t = -1;
+      long r = 0;
+      if (rw < nQ) t = 0, r = rw;
+      else if (rw < 2 * nQ) t = 1, r = rw - nQ;
+      else if (rw < 2 * nQ + nK) t = 2, r = rw - 2 * nQ;
+      else if (rw < tot) t = 3, r = rw - 2 * nQ - nK;
+      tt[u] = t;
+      const int DD = (t == 0 || t == 2) ? p.D : p.Dv;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[u][e] = 0.f;
+      if (t >= 0 && c0 < DD) {
+        if (t == 0) decode8_f(reinterpret_cast<const uint8_t*>(p.q + r * p.D), kTypeF32, c0, x[u]);
+        else if (t == 1) decode8_f(reinterpret_cast<const uint8_t*>(p.dO + r * p.Dv), kTypeF32, c0, x[u]);
+        else if (t == 2) decode8_f(p.k + r * p.rbk, p.k_type, c0, x[u]);
+        else decode8_f(p.v + r * p.rbv, p.v_type, c0, x[u]);
+      }
     }
-    am = warp_max(am);
-    ss = warp_sum(ss);
-    amax[t] = fmaxf(amax[t], am);
-    nrm[t] = fmaxf(nrm[t], ss);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float am = 0.f, ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(x[u][e])), ss = fmaf(x[u][e], x[u][e], ss);
+      am = warp_max(am);
+      ss = warp_sum(ss);
+      const int t = tt[u];
+      if (t >= 0) amax[t] = fmaxf(amax[t], am), nrm[t] = fmaxf(nrm[t], ss);
+    }
   }
   if (lane == 0)
     for (int t = 0; t < 4; ++t) red[warp][t][0] = amax[t], red[warp][t][1] = nrm[t];
@@ -449,29 +462,34 @@ __global__ void __launch_bounds__(256) k_row_stats(Params p) {
     p.bstat[((size_t)blockIdx.x * 4 + t) * 2 + w] = m;
   }
 }
-
-// Column sums of V^ over one chunk of keys: warp = (chunk, hk), lane = 8 consecutive columns;
-// keys summed in increasing order.
 __global__ void __launch_bounds__(256) k_vsum(Params p) {
+  // block = (chunk, hk); its eight warps take every eighth key of the chunk and their sums are
+  // added in warp order, so the result does not depend on timing
+  __shared__ float part[8][256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int wid = blockIdx.x * 8 + warp;
-  if (wid >= p.nbv * p.Hkv) return;
-  const int chunk = wid / p.Hkv, hk = wid % p.Hkv;
+  const int chunk = blockIdx.x / p.Hkv, hk = blockIdx.x % p.Hkv;
   const int c0 = lane * 8;
-  if (c0 >= p.Dv) return;
   const long per = ((long)p.M + p.nbv - 1) / p.nbv;
   const long ja = (long)chunk * per, jb = min((long)p.M, ja + per);
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (c0 < p.Dv) {
 #pragma unroll 2
-  for (long j = ja; j < jb; ++j) {
-    float x[8];
-    decode8_f(p.v + (j * p.Hkv + hk) * p.rbv, p.v_type, c0, x);
+    for (long j = ja + warp; j < jb; j += 8) {
+      float x[8];
+      decode8_f(p.v + (j * p.Hkv + hk) * p.rbv, p.v_type, c0, x);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] += x[e];
+      for (int e = 0; e < 8; ++e) acc[e] += x[e];
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) part[warp][c0 + e] = acc[e];
   }
-  float* o = p.vsum + ((size_t)chunk * p.Hkv + hk) * p.Dv + c0;
+  __syncthreads();
+  for (int c = threadIdx.x; c < p.Dv; c += 256) {
+    float t = 0.f;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) o[e] = acc[e];
+    for (int w = 0; w < 8; ++w) t += part[w][c];
+    p.vsum[((size_t)chunk * p.Hkv + hk) * p.Dv + c] = t;
+  }
 }
 
 __device__ __forceinline__ float pow2_scale_for(float amax, int target_exp) {
