@@ -1664,9 +1664,10 @@ __global__ void __launch_bounds__(256) k_dq_reduce(Params p) {
 //
 // A CTA owns BK keys of one KV head: their K' and V' tiles are decoded once into shared memory,
 // then the CTA walks the 128-row query tiles that can see them.  Per query tile:
-//   S = Q K'^T, dP = dO V'^T              (M = 128 rows, N = BK keys)
-//   P, dS = P * (dP - delta)              (softmax warps, written as binary16 [row][key])
-//   dK^T += Q^T dS, dV^T += dO^T P        (M = 128 feature rows per half, N = BK keys, K = 128 rows)
+//   dP = dO V'^T, S = Q K'^T              (M = 128 rows, N = BK keys)
+//   P                                     (softmax warps, written as binary16 [row][key])
+//   dV^T += dO^T P, while the softmax forms dS = P * (dP - delta)
+//   dK^T += Q^T dS                        (M = 128 feature rows per half, N = BK keys, K = 128 rows)
 // Q and dO arrive as 64-column TMA panels with one full/empty barrier pair each; a panel is
 // released when the last product reading it completes, so the next tile's loads overlap this
 // tile's final products without a second buffer.
@@ -1694,6 +1695,8 @@ enum {
   C_O_FULL = 8,   // [4]
   C_O_EMPTY = 12, // [4]
   C_S_FULL = 16,
+  C_P_FULL,   // the softmax wrote P (dV product may start)
+  C_P_EMPTY,  // the dV product read P
   C_DS_FULL,
   C_DS_EMPTY,
   C_DONE,
@@ -1737,6 +1740,8 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bar[C_O_EMPTY + c], 1);
     }
     mbar_init(&bar[C_S_FULL], 1);
+    mbar_init(&bar[C_P_FULL], 8);
+    mbar_init(&bar[C_P_EMPTY], 1);
     mbar_init(&bar[C_DS_FULL], 8);
     mbar_init(&bar[C_DS_EMPTY], p.ds ? 2 : 1);
     mbar_init(&bar[C_DONE], 1);
@@ -1762,16 +1767,17 @@ __global__ void __launch_bounds__(384, 1)
       prefetch_tmap(&tmO);
       for (int t = 0; t < nq; ++t) {
         const int r0 = (qt_begin + t) * 128;
+        // dO first: the dP product comes first, and the dV product frees its panels first
         bool ok = true;
-        for (int c = 0; ok && c < C::NQP; ++c) {
-          if (!(ok = wait(&bar[C_Q_EMPTY + c], (t & 1) ^ 1))) break;
-          mbar_arrive_expect_tx(&bar[C_Q_FULL + c], 128 * 128);
-          tma_load_3d(sQ + c * 128 * 128, &tmQ, &bar[C_Q_FULL + c], c * 64, r0, hk);
-        }
         for (int c = 0; ok && c < C::NOP; ++c) {
           if (!(ok = wait(&bar[C_O_EMPTY + c], (t & 1) ^ 1))) break;
           mbar_arrive_expect_tx(&bar[C_O_FULL + c], 128 * 128);
           tma_load_3d(sO + c * 128 * 128, &tmO, &bar[C_O_FULL + c], c * 64, r0, hk);
+        }
+        for (int c = 0; ok && c < C::NQP; ++c) {
+          if (!(ok = wait(&bar[C_Q_EMPTY + c], (t & 1) ^ 1))) break;
+          mbar_arrive_expect_tx(&bar[C_Q_FULL + c], 128 * 128);
+          tma_load_3d(sQ + c * 128 * 128, &tmQ, &bar[C_Q_FULL + c], c * 64, r0, hk);
         }
         if (!ok) break;
       }
@@ -1789,16 +1795,11 @@ __global__ void __launch_bounds__(384, 1)
                      dk0 = sdesc_sw128(smem_u32(sK), 16, 1024), dv0 = sdesc_sw128(smem_u32(sV), 16, 1024),
                      dqt = sdesc_sw128(smem_u32(sQ), LBO_Q, 1024), dot = sdesc_sw128(smem_u32(sO), LBO_O, 1024),
                      ds0 = sdesc_sw128(smem_u32(sS), 128 * 128, 1024), dp0 = sdesc_sw128(smem_u32(sP), 128 * 128, 1024);
+      // Per query tile: dP, then S (so the Q panels, released last, have dP's time to arrive),
+      // then dV^T once P is written and dK^T once dS is: the softmax's dS arithmetic overlaps
+      // the dV^T product.
       for (int t = 0; t < nq; ++t) {
         bool ok = true;
-        for (int c = 0; ok && c < C::NQP; ++c) {
-          if (!(ok = wait(&bar[C_Q_FULL + c], t & 1))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_f16(tS, sdesc_adv(dq0, c * (128 * 128) + k * 32), sdesc_adv(dk0, c * (BK * 128) + k * 32), ID_S,
-                    (c > 0 || k > 0) ? 1u : 0u);
-        }
         for (int c = 0; ok && c < C::NOP; ++c) {
           if (!(ok = wait(&bar[C_O_FULL + c], t & 1))) break;
           tc_fence_after();
@@ -1807,20 +1808,19 @@ __global__ void __launch_bounds__(384, 1)
             mma_f16(tP, sdesc_adv(do0, c * (128 * 128) + k * 32), sdesc_adv(dv0, c * (BK * 128) + k * 32), ID_S,
                     (c > 0 || k > 0) ? 1u : 0u);
         }
+        for (int c = 0; ok && c < C::NQP; ++c) {
+          if (!(ok = wait(&bar[C_Q_FULL + c], t & 1))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f16(tS, sdesc_adv(dq0, c * (128 * 128) + k * 32), sdesc_adv(dk0, c * (BK * 128) + k * 32), ID_S,
+                    (c > 0 || k > 0) ? 1u : 0u);
+        }
         if (!ok) break;
         mma_commit(&bar[C_S_FULL]);
-        if (!wait(&bar[C_DS_FULL], t & 1)) break;
-        tc_fence_after();
         const uint32_t acc0 = t > 0 ? 1u : 0u;
-#pragma unroll
-        for (int hh = 0; hh < C::NDH; ++hh) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_f16(tK + hh * BK, sdesc_adv(dqt, hh * 2 * (128 * 128) + k * 2048), sdesc_adv(ds0, k * 2048), ID_T,
-                    (acc0 || k > 0) ? 1u : 0u);
-          mma_commit(&bar[C_Q_EMPTY + 2 * hh]);
-          if (2 * hh + 1 < C::NQP) mma_commit(&bar[C_Q_EMPTY + 2 * hh + 1]);
-        }
+        if (!wait(&bar[C_P_FULL], t & 1)) break;
+        tc_fence_after();
 #pragma unroll
         for (int hh = 0; hh < C::NVH; ++hh) {
 #pragma unroll
@@ -1829,6 +1829,18 @@ __global__ void __launch_bounds__(384, 1)
                     (acc0 || k > 0) ? 1u : 0u);
           mma_commit(&bar[C_O_EMPTY + 2 * hh]);
           if (2 * hh + 1 < C::NOP) mma_commit(&bar[C_O_EMPTY + 2 * hh + 1]);
+        }
+        mma_commit(&bar[C_P_EMPTY]);
+        if (!wait(&bar[C_DS_FULL], t & 1)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int hh = 0; hh < C::NDH; ++hh) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_f16(tK + hh * BK, sdesc_adv(dqt, hh * 2 * (128 * 128) + k * 2048), sdesc_adv(ds0, k * 2048), ID_T,
+                    (acc0 || k > 0) ? 1u : 0u);
+          mma_commit(&bar[C_Q_EMPTY + 2 * hh]);
+          if (2 * hh + 1 < C::NQP) mma_commit(&bar[C_Q_EMPTY + 2 * hh + 1]);
         }
         mma_commit(&bar[C_DS_EMPTY]);
       }
@@ -1878,21 +1890,15 @@ __global__ void __launch_bounds__(384, 1)
       if (t + 1 < nq) row_stats(t + 1, nlse2, ndl, njlast, nmrow);
       const float nl = lse2 > -CUDART_INF_F ? lp - lse2 : -CUDART_INF_F;  // sP * p = 2^(t2 + nl); 0 on a dead row
       if (!wait(&bar[C_S_FULL], t & 1)) break;
-      // the previous tile's P and dS panels are free once its gradient products completed
-      if (!wait(&bar[C_DS_EMPTY], (t & 1) ^ 1)) break;
+      // the previous tile's P panel is free once its dV product read it
+      if (!wait(&bar[C_P_EMPTY], (t & 1) ^ 1)) break;
       tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < C::HALF; c += 32) {
-        const int col0 = ch * C::HALF + c;
-        float s[32], dp[32];
-        tmem_ld32(tbase + C::T_S + lane_off + col0, s);
-        tmem_ld32(tbase + C::T_P + lane_off + col0, dp);
-        tmem_ld_wait();
-        // log2-domain exponents; a fully visible chunk without a mask takes no per-key tests
-        float t2[32];
+      // log2-domain exponents of one 32-key chunk; a fully visible chunk without a mask takes
+      // no per-key tests
+      auto exponents = [&](int col0, float* v) {
         if (mrow == nullptr && (long)(j0 + col0 + 31) <= jlast) {
 #pragma unroll
-          for (int x = 0; x < 32; ++x) t2[x] = fmaf(s[x], c2, nl);
+          for (int x = 0; x < 32; ++x) v[x] = fmaf(v[x], c2, nl);
         } else {
 #pragma unroll
           for (int x = 0; x < 32; ++x) {
@@ -1903,23 +1909,65 @@ __global__ void __launch_bounds__(384, 1)
               mv = h2f(__ldg(reinterpret_cast<const unsigned short*>(mrow) + j));
               ok = !(mv == -CUDART_INF_F);
             }
-            t2[x] = ok ? fmaf(s[x], c2, mv * kLog2e) + nl : -CUDART_INF_F;
+            v[x] = ok ? fmaf(v[x], c2, mv * kLog2e) + nl : -CUDART_INF_F;
           }
         }
+      };
+      if constexpr (C::HALF == 32) {
+        // one chunk per thread: P is written and handed to the dV product first, then dS
+        const int col0 = ch * 32;
+        float s[32], dp[32];
+        tmem_ld32(tbase + C::T_S + lane_off + col0, s);
+        tmem_ld32(tbase + C::T_P + lane_off + col0, dp);
+        tmem_ld_wait();
+        exponents(col0, s);
 #pragma unroll
-        for (int g = 0; g < 32; g += 8) {
-          uint32_t pp[4], pd[4];
+        for (int x = 0; x < 32; ++x) s[x] = ex2(s[x]);  // sP * p; 0 for masked keys and dead rows
 #pragma unroll
-          for (int n = 0; n < 8; n += 2) {
-            const int x = g + n;
-            const float p0 = ex2(t2[x]), p1 = ex2(t2[x + 1]);  // sP * p; 0 for masked keys and dead rows
-            pp[n / 2] = h2_as_u32(__floats2half2_rn(p0, p1));
-            pd[n / 2] = h2_as_u32(__floats2half2_rn(p0 * (dp[x] - dl) * lam, p1 * (dp[x + 1] - dl) * lam));
+        for (int g = 0; g < 32; g += 8)
+          sts_v4(sP_u + panel_off_u(128, row, col0 + g), h2_as_u32(__floats2half2_rn(s[g], s[g + 1])),
+                 h2_as_u32(__floats2half2_rn(s[g + 2], s[g + 3])), h2_as_u32(__floats2half2_rn(s[g + 4], s[g + 5])),
+                 h2_as_u32(__floats2half2_rn(s[g + 6], s[g + 7])));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[C_P_FULL]);
+        uint32_t pd[16];
+#pragma unroll
+        for (int x = 0; x < 32; x += 2)
+          pd[x / 2] = h2_as_u32(__floats2half2_rn(s[x] * (dp[x] - dl) * lam, s[x + 1] * (dp[x + 1] - dl) * lam));
+        // the previous tile's dS panel is free once its dK product and its store read it
+        if (!wait(&bar[C_DS_EMPTY], (t & 1) ^ 1)) break;
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          sts_v4(sS_u + panel_off_u(128, row, col0 + 8 * g), pd[4 * g], pd[4 * g + 1], pd[4 * g + 2], pd[4 * g + 3]);
+      } else {
+        if (!wait(&bar[C_DS_EMPTY], (t & 1) ^ 1)) break;
+#pragma unroll 1
+        for (int c = 0; c < C::HALF; c += 32) {
+          const int col0 = ch * C::HALF + c;
+          float s[32], dp[32];
+          tmem_ld32(tbase + C::T_S + lane_off + col0, s);
+          tmem_ld32(tbase + C::T_P + lane_off + col0, dp);
+          tmem_ld_wait();
+          exponents(col0, s);
+#pragma unroll
+          for (int g = 0; g < 32; g += 8) {
+            uint32_t pp[4], pd[4];
+#pragma unroll
+            for (int n = 0; n < 8; n += 2) {
+              const int x = g + n;
+              const float p0 = ex2(s[x]), p1 = ex2(s[x + 1]);  // sP * p; 0 for masked keys and dead rows
+              pp[n / 2] = h2_as_u32(__floats2half2_rn(p0, p1));
+              pd[n / 2] = h2_as_u32(__floats2half2_rn(p0 * (dp[x] - dl) * lam, p1 * (dp[x + 1] - dl) * lam));
+            }
+            const uint32_t off = panel_off_u(128, row, col0 + g);
+            sts_v4(sP_u + off, pp[0], pp[1], pp[2], pp[3]);
+            sts_v4(sS_u + off, pd[0], pd[1], pd[2], pd[3]);
           }
-          const uint32_t off = panel_off_u(128, row, col0 + g);
-          sts_v4(sP_u + off, pp[0], pp[1], pp[2], pp[3]);
-          sts_v4(sS_u + off, pd[0], pd[1], pd[2], pd[3]);
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[C_P_FULL]);
       }
       if (*s_abort) break;
       tc_fence_before();
