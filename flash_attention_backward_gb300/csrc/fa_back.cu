@@ -36,7 +36,7 @@ struct Plan {
   int nblk_stats, nbv;
   int pre;  // 1: binary16 K'/V' copies in the workspace feed the row passes by TMA
   int dsq;  // 1 (with pre): the dK/dV pass stores dS and dQ is one product over it (k_dq_gemm)
-  int ldds; // keys per stored dS row (M rounded up to 64)
+  int ldds; // 64-key tiles per stored dS row tile (whole gradient-pass key tiles)
   int nsm;
   size_t off_stats, off_rmean, off_rsh, off_dOr, off_lse2, off_dlt, off_part, off_dqpart, off_q16, off_do16,
       off_bstat, off_vsum, off_kd, off_vd, off_ds, total;
@@ -67,7 +67,7 @@ static void layout(Plan& P, int M, int Hkv, int D, int Dv) {
   P.off_vsum = o; o = align256(o + sizeof(float) * (size_t)P.nbv * Hkv * Dv);
   P.off_kd = o; o = align256(o + (P.pre ? 2 * (size_t)Hkv * M * D : 0));
   P.off_vd = o; o = align256(o + (P.pre ? 2 * (size_t)Hkv * M * Dv : 0));
-  P.off_ds = o; o = align256(o + (P.dsq ? 2 * (size_t)Hkv * P.R * P.ldds : 0));
+  P.off_ds = o; o = align256(o + (P.dsq ? (size_t)Hkv * P.nQT * P.ldds * (128 * 64 * 2) : 0));
   P.total = o;
 }
 
@@ -81,7 +81,7 @@ static Plan plan_variant(int N, int M, int H, int Hkv, int D, int Dv, int nsm, s
   std::memset(&P, 0, sizeof(P));
   P.pre = level >= 1;
   P.dsq = level >= 2;
-  P.ldds = (M + 63) / 64 * 64;
+  P.ldds = (M + block_keys(D, Dv) - 1) / block_keys(D, Dv) * (block_keys(D, Dv) / 64);  // whole key tiles
   P.nsm = nsm;
   P.G = H / Hkv;
   P.R = N * P.G;
@@ -342,9 +342,11 @@ static cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& 
   cudaError_t e = P.pre ? rows_pre<D, Dv, BK, BKL>(pl, pq, P, tmQ, grid, s, rec)
                         : rows_raw<D, Dv, BK, BKL>(pl, pq, P, tmQ, grid, s, rec);
   if (e != cudaSuccess) return e;
-  CUtensorMap tmS;  // stored dS [Hkv][R][ldds] (level 2 only)
+  // stored dS (level 2 only): contiguous 128-row x 64-key tiles, tile (hk, row tile, key tile)
+  // at index (hk * nQT + qt) * ldds + kt64; one TMA box is one tile
+  CUtensorMap tmS;
   std::memset(&tmS, 0, sizeof(tmS));
-  if (P.dsq && !make_map(&tmS, p.ds, p.ldds, P.R, p.Hkv)) return cudaErrorInvalidValue;
+  if (P.dsq && !make_map(&tmS, p.ds, 64, 128, p.Hkv * P.nQT * p.ldds)) return cudaErrorInvalidValue;
   if (P.nKT > 0) {
     if ((e = set_smem(k_cols2<D, Dv, BK>, CC::SMEM)) != cudaSuccess) return e;
     k_cols2<D, Dv, BK><<<dim3(P.nKT, p.Hkv), 384, CC::SMEM, s>>>(tmQ, tmO, tmS, p);

@@ -75,8 +75,10 @@ struct Params {
   float* rsh;     // [Hkv][Dv]  -r' * sV, an exact binary16 value (the decoders' V shift)
   __half* kd;     // [Hkv][M][D]   binary16 K' = k^ sK (producer-fed row passes; else null)
   __half* vd;     // [Hkv][M][Dv]  binary16 V' = v^ sV - r' sV
-  __half* ds;     // [Hkv][R][ldds] binary16 lam * dS from the dK/dV pass, read by k_dq_gemm (or null)
-  int ldds;       // keys per dS row: M rounded up to 64
+  __half* ds;     // binary16 lam * dS from the dK/dV pass, read by k_dq_gemm (or null): contiguous
+                  // [128 rows][64 keys] tiles, tile (hk, row tile qt, key tile kt64) at
+                  // (hk * nQT + qt) * ldds + kt64
+  int ldds;       // 64-key tiles per row tile (whole gradient-pass key tiles)
   // raw K/V staging of the row passes
   int raw_bulk;        // 1: rows are 16-byte multiples, copied by bulk async copies; 0: 4-byte async copies
   int rbk_pad, rbv_pad;  // raw row strides in shared memory (16-byte multiples)
@@ -1853,7 +1855,8 @@ __global__ void __launch_bounds__(384, 1)
       for (int t = 0; t < nq; ++t) {
         if (!wait(&bar[C_DS_FULL], t & 1)) break;
 #pragma unroll
-        for (int c = 0; c < BK / 64; ++c) tma_store_3d(&tmS, sS + c * (128 * 128), j0 + c * 64, (qt_begin + t) * 128, hk);
+        for (int c = 0; c < BK / 64; ++c)
+          tma_store_3d(&tmS, sS + c * (128 * 128), 0, 0, (hk * p.nQT + qt_begin + t) * p.ldds + j0 / 64 + c);
         bulk_commit_group();
         bulk_wait_read_all();  // the panels may be overwritten once read
         mbar_arrive(&bar[C_DS_EMPTY]);
@@ -2107,7 +2110,8 @@ __global__ void __launch_bounds__(256, 1)
         const int j0 = (kt_begin + t) * BK;
         mbar_arrive_expect_tx(&bar[G_FULL + s], (uint32_t)C::SB);
 #pragma unroll
-        for (int c = 0; c < BK / 64; ++c) tma_load_3d(a + c * (128 * 128), &tmS, &bar[G_FULL + s], j0 + c * 64, r0, hk);
+        for (int c = 0; c < BK / 64; ++c)
+          tma_load_3d(a + c * (128 * 128), &tmS, &bar[G_FULL + s], 0, 0, (hk * p.nQT + qt) * p.ldds + j0 / 64 + c);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) tma_load_3d(b + c * (BK * 128), &tmK, &bar[G_FULL + s], c * 64, j0, hk);
       }
