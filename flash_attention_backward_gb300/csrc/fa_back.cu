@@ -152,7 +152,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // binary16 tensor [d2][d1][d0] (d0 fastest); boxes of 64 x rows x 1 with the 128-byte swizzle
 // (one box is one operand panel of `rows` 128-byte rows).
-static bool make_map(CUtensorMap* m, void* base, int d0, int d1, int d2, int rows = 128) {
+static bool make_map(CUtensorMap* m, void* base, int d0, int d1, int d2, int rows = 128,
+                     CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_128B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
@@ -160,7 +161,7 @@ static bool make_map(CUtensorMap* m, void* base, int d0, int d1, int d2, int row
   cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  CU_TENSOR_MAP_SWIZZLE_128B, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -269,8 +270,10 @@ static cudaError_t rows_pre(const Params& pl, const Params& pq, const Plan& P, c
   using FL = Rows3Cfg<D, Dv, BKL, 0>;
   using FQ = Rows3Cfg<D, Dv, BK, 1>;
   CUtensorMap tkl, tvl, tkq, tvq;
-  if (!make_map(&tkl, pl.kd, D, pl.M, pl.Hkv, BKL) || !make_map(&tvl, pl.vd, Dv, pl.M, pl.Hkv, BKL) ||
-      !make_map(&tkq, pq.kd, D, pq.M, pq.Hkv, BK) || !make_map(&tvq, pq.vd, Dv, pq.M, pq.Hkv, BK))
+  // panel-major copies: [Hkv * D/64 panels][M keys][64 columns]
+  if (!make_map(&tkl, pl.kd, 64, pl.M, pl.Hkv * (D / 64), BKL) ||
+      !make_map(&tvl, pl.vd, 64, pl.M, pl.Hkv * (Dv / 64), BKL) ||
+      !make_map(&tkq, pq.kd, 64, pq.M, pq.Hkv * (D / 64), BK) || !make_map(&tvq, pq.vd, 64, pq.M, pq.Hkv * (Dv / 64), BK))
     return cudaErrorInvalidValue;
   cudaError_t e;
   if ((e = set_smem(k_rows3<D, Dv, BKL, 0>, FL::SMEM)) != cudaSuccess) return e;
@@ -355,7 +358,7 @@ static cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& 
   if (P.dsq) {
     using GC = GemmCfg<D, BK>;
     CUtensorMap tkg;
-    if (!make_map(&tkg, p.kd, D, p.M, p.Hkv, BK)) return cudaErrorInvalidValue;
+    if (!make_map(&tkg, p.kd, 64, p.M, p.Hkv * (D / 64), BK)) return cudaErrorInvalidValue;
     if ((e = set_smem(k_dq_gemm<D, BK>, GC::SMEM)) != cudaSuccess) return e;
     k_dq_gemm<D, BK><<<grid, 256, GC::SMEM, s>>>(tmS, tkg, p);
     rec.mark(KS_DQ_GEMM);

@@ -73,8 +73,8 @@ struct Params {
   float* vsum;    // [nbv][Hkv][Dv]
   int nbv;
   float* rsh;     // [Hkv][Dv]  -r' * sV, an exact binary16 value (the decoders' V shift)
-  __half* kd;     // [Hkv][M][D]   binary16 K' = k^ sK (producer-fed row passes; else null)
-  __half* vd;     // [Hkv][M][Dv]  binary16 V' = v^ sV - r' sV
+  __half* kd;     // [Hkv][D/64][M][64]   binary16 K' = k^ sK, panel-major (TMA-fed passes; else null)
+  __half* vd;     // [Hkv][Dv/64][M][64]  binary16 V' = v^ sV - r' sV
   __half* ds;     // binary16 lam * dS from the dK/dV pass, read by k_dq_gemm (or null): contiguous
                   // [128 rows][64 keys] tiles, tile (hk, row tile qt, key tile kt64) at
                   // (hk * nQT + qt) * ldds + kt64
@@ -611,6 +611,8 @@ __global__ void __launch_bounds__(256) k_convert(Params p) {
 // Binary16 operand copies of the cache for the producer-fed row passes: K'[hk][j] = k^_j sK and
 // V'[hk][j] = v^_j sV - r' sV, with the rounding of the in-kernel decoders (decode8_h), so both
 // row-pass variants see the same operands.  Thread = 8 values; cache rows are read in order.
+// The copies are panel-major, [hk][64-column panel][key][64]: the TMA box of one operand panel
+// (BK keys x 64 columns) is then one contiguous block.
 __global__ void __launch_bounds__(256) k_predecode(Params p) {
   const float sK = p.st->sK, sV = p.st->sV;
   const long uk = (long)p.M * p.Hkv * (p.D / 8), uv = (long)p.M * p.Hkv * (p.Dv / 8);
@@ -625,7 +627,7 @@ __global__ void __launch_bounds__(256) k_predecode(Params p) {
     const uint8_t* src = (isv ? p.v : p.k) + row * (isv ? p.rbv : p.rbk);
     const uint4 o = decode8_h(src, isv ? p.v_type : p.k_type, c0, isv ? sV : sK,
                               isv ? p.rsh + (size_t)hk * DD : nullptr);
-    __half* dst = (isv ? p.vd : p.kd) + ((size_t)hk * p.M + j) * DD + c0;
+    __half* dst = (isv ? p.vd : p.kd) + (((size_t)hk * (DD / 64) + c0 / 64) * p.M + j) * 64 + (c0 & 63);
     *reinterpret_cast<uint4*>(dst) = o;
   }
 }
@@ -1353,7 +1355,7 @@ __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
           const int j0 = (kt_begin + kt) * BK;
           mbar_arrive_expect_tx(fb, (uint32_t)C::KB);
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * BK * 128, &tmK, fb, c * 64, j0, hk);
+          for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * BK * 128, &tmK, fb, 0, j0, hk * (D / 64) + c);
           ++kt;
           moved = true;
         }
@@ -1363,7 +1365,7 @@ __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
           const int j0 = (kt_begin + vt) * BK;
           mbar_arrive_expect_tx(fb, (uint32_t)C::VB);
 #pragma unroll
-          for (int c = 0; c < Dv / 64; ++c) tma_load_3d(dst + c * BK * 128, &tmV, fb, c * 64, j0, hk);
+          for (int c = 0; c < Dv / 64; ++c) tma_load_3d(dst + c * BK * 128, &tmV, fb, 0, j0, hk * (Dv / 64) + c);
           ++vt;
           moved = true;
         }
@@ -2113,7 +2115,8 @@ __global__ void __launch_bounds__(256, 1)
         for (int c = 0; c < BK / 64; ++c)
           tma_load_3d(a + c * (128 * 128), &tmS, &bar[G_FULL + s], 0, 0, (hk * p.nQT + qt) * p.ldds + j0 / 64 + c);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) tma_load_3d(b + c * (BK * 128), &tmK, &bar[G_FULL + s], c * 64, j0, hk);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(b + c * (BK * 128), &tmK, &bar[G_FULL + s], 0, j0, hk * (D / 64) + c);
       }
     }
   } else if (warp == 1) {
