@@ -1,14 +1,18 @@
 // Device code of the flash-attention backward over a raw K/V cache (sm_103a).
 //
-// Pipeline (all on one stream, see fa_back.cu):
+// Pipeline (all on one stream, see fa_back.cu; the plan level depends on the workspace):
 //   k_row_stats  -> per-block max |x| and max row norm of Q, dO, K^ and V^
 //   k_vsum       -> per-chunk column sums of V^ (for its column mean r)
 //   k_finalize   -> power-of-two operand scales, r, the dS multiplier
 //   k_convert    -> Q, dO as scaled binary16 rows packed per KV head (row r = i*G + g)
-//   k_rows<LSE>  -> per (row tile, key split): running max / sum / sum of p*dP
+//   k_predecode  -> binary16 K', V' copies of the cache (levels 2 and 1)
+//   k_rows3/k_rows2 <LSE> -> per (row tile, key split): running max / sum / sum of p*dP
+//                            (TMA-fed from the copies, or decoding raw rows in the CTA at level 0)
 //   k_lse_merge  -> lse, delta outputs; log2-domain lse and shifted delta for the gradient passes
-//   k_rows<DQ>   -> dQ = scale * dS K^ per row tile (split over keys, merged in fixed order)
-//   k_cols       -> dK^T = scale * Q^T dS and dV^T = dO^T P per key tile
+//   k_cols2      -> dK^T = scale * Q^T dS and dV^T = dO^T P per key tile; stores dS (level 2)
+//   k_dq_gemm    -> dQ = scale * dS K' per row tile over the stored dS (level 2), or
+//   k_rows3/k_rows2 <DQ> -> dQ recomputing S, dP, dS per row tile (levels 1, 0);
+//                           both split over keys and merged in fixed order (k_dq_reduce)
 //
 // Arithmetic (documented in the header of fa_back.cu): every tensor-core product is
 // binary16 x binary16 -> f32 (tcgen05.mma kind::f16).  Inputs are multiplied by powers of two
