@@ -350,9 +350,16 @@ static cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& 
   CUtensorMap tmS;
   std::memset(&tmS, 0, sizeof(tmS));
   if (P.dsq && !make_map(&tmS, p.ds, 64, 128, p.Hkv * P.nQT * p.ldds)) return cudaErrorInvalidValue;
+  // the binary16 K'/V' copies as key tiles of the dK/dV pass (levels 2 and 1)
+  CUtensorMap tkc, tvc;
+  std::memset(&tkc, 0, sizeof(tkc));
+  tvc = tkc;
+  if (P.pre && (!make_map(&tkc, p.kd, 64, p.M, p.Hkv * (D / 64), BK) ||
+                !make_map(&tvc, p.vd, 64, p.M, p.Hkv * (Dv / 64), BK)))
+    return cudaErrorInvalidValue;
   if (P.nKT > 0) {
     if ((e = set_smem(k_cols2<D, Dv, BK>, CC::SMEM)) != cudaSuccess) return e;
-    k_cols2<D, Dv, BK><<<dim3(P.nKT, p.Hkv), 384, CC::SMEM, s>>>(tmQ, tmO, tmS, p);
+    k_cols2<D, Dv, BK><<<dim3(P.nKT, p.Hkv), 384, CC::SMEM, s>>>(tmQ, tmO, tmS, tkc, tvc, p);
     rec.mark(KS_COLS);
   }
   if (P.dsq) {

@@ -1670,8 +1670,9 @@ __global__ void __launch_bounds__(256) k_dq_reduce(Params p) {
 // ------------------------------------------------------------------------------------------------
 // key-tile pass: dK and dV
 //
-// A CTA owns BK keys of one KV head: their K' and V' tiles are decoded once into shared memory,
-// then the CTA walks the 128-row query tiles that can see them.  Per query tile:
+// A CTA owns BK keys of one KV head: their K' and V' tiles arrive once in shared memory (by TMA
+// from the binary16 copies where the plan has them, else decoded here from the raw cache), then
+// the CTA walks the 128-row query tiles that can see them.  Per query tile:
 //   dP = dO V'^T, S = Q K'^T              (M = 128 rows, N = BK keys)
 //   P                                     (softmax warps, written as binary16 [row][key])
 //   dV^T += dO^T P, while the softmax forms dS = P * (dP - delta)
@@ -1680,7 +1681,7 @@ __global__ void __launch_bounds__(256) k_dq_reduce(Params p) {
 // released when the last product reading it completes, so the next tile's loads overlap this
 // tile's final products without a second buffer.
 // Warp roles (12 warps): 0 producer, 1 MMA issuer / tensor-memory owner, 4-11 softmax and
-// epilogue, every warp decodes K' and V' at the start.  Where the plan keeps dS for a separate
+// epilogue; without the binary16 copies every warp decodes K' and V' at the start.  Where the plan keeps dS for a separate
 // dQ product (p.ds), warp 2 stores each tile's dS panels to it with TMA, and the dS buffer is
 // released only once both the gradient products and that store have read it.
 
@@ -1708,13 +1709,16 @@ enum {
   C_DS_FULL,
   C_DS_EMPTY,
   C_DONE,
+  C_KV_FULL,  // K'/V' tiles loaded from the binary16 copies (levels 2 and 1)
   C_COUNT
 };
+static_assert(8 * C_COUNT + 8 <= 256, "dK/dV pass barrier area");
 
 template <int D, int Dv, int BK>
 __global__ void __launch_bounds__(384, 1)
     k_cols2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
-            const __grid_constant__ CUtensorMap tmS, Params p) {
+            const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmKd,
+            const __grid_constant__ CUtensorMap tmVd, Params p) {
   using C = Cols2Cfg<D, Dv, BK>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -1753,11 +1757,13 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&bar[C_DS_FULL], 8);
     mbar_init(&bar[C_DS_EMPTY], p.ds ? 2 : 1);
     mbar_init(&bar[C_DONE], 1);
+    mbar_init(&bar[C_KV_FULL], 1);
     *s_abort = 0;
     fence_mbar_init();
   }
   const Stats st = *p.st;
-  if (nq > 0) {  // K' and V' once, by every thread
+  const bool kv_copies = p.kd != nullptr;  // K'/V' by TMA from the binary16 copies, else decoded here
+  if (nq > 0 && !kv_copies) {  // K' and V' once, by every thread
     decode_tile<D, BK, 384>(p.k, p.k_type, p.rbk, hk, p.Hkv, j0, p.M, sK, st.sK, nullptr, tid);
     decode_tile<Dv, BK, 384>(p.v, p.v_type, p.rbv, hk, p.Hkv, j0, p.M, sV, st.sV, p.rsh + (size_t)hk * Dv, tid);
     fence_proxy_async_smem();
@@ -1773,6 +1779,14 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmO);
+      if (nq > 0 && kv_copies) {  // the key tile's K' and V' panels (same values as decode_tile's)
+        mbar_arrive_expect_tx(&bar[C_KV_FULL], (uint32_t)(C::KB + C::VB));
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) tma_load_3d(sK + c * BK * 128, &tmKd, &bar[C_KV_FULL], 0, j0, hk * (D / 64) + c);
+#pragma unroll
+        for (int c = 0; c < Dv / 64; ++c)
+          tma_load_3d(sV + c * BK * 128, &tmVd, &bar[C_KV_FULL], 0, j0, hk * (Dv / 64) + c);
+      }
       for (int t = 0; t < nq; ++t) {
         const int r0 = (qt_begin + t) * 128;
         // dO first: the dP product comes first, and the dV product frees its panels first
@@ -1803,10 +1817,11 @@ __global__ void __launch_bounds__(384, 1)
                      dk0 = sdesc_sw128(smem_u32(sK), 16, 1024), dv0 = sdesc_sw128(smem_u32(sV), 16, 1024),
                      dqt = sdesc_sw128(smem_u32(sQ), LBO_Q, 1024), dot = sdesc_sw128(smem_u32(sO), LBO_O, 1024),
                      ds0 = sdesc_sw128(smem_u32(sS), 128 * 128, 1024), dp0 = sdesc_sw128(smem_u32(sP), 128 * 128, 1024);
+      const bool nq_ok = !kv_copies || wait(&bar[C_KV_FULL], 0);
       // Per query tile: dP, then S (so the Q panels, released last, have dP's time to arrive),
       // then dV^T once P is written and dK^T once dS is: the softmax's dS arithmetic overlaps
       // the dV^T product.
-      for (int t = 0; t < nq; ++t) {
+      for (int t = 0; nq_ok && t < nq; ++t) {
         bool ok = true;
         for (int c = 0; ok && c < C::NOP; ++c) {
           if (!(ok = wait(&bar[C_O_FULL + c], t & 1))) break;
