@@ -39,6 +39,9 @@ def lib():
     L.fa_back_workspace_size_min.argtypes = [i] * 6
     L.fa_back.restype = i
     L.fa_back.argtypes = [vp, vp, i, vp, i, vp, i, vp, f, i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.fa_back_with_stats.restype = i
+    L.fa_back_with_stats.argtypes = [vp, vp, i, vp, i, vp, i, vp, vp, vp, f, i, i, i, i, i, i, i, vp, vp, vp, vp, sz,
+                                     vp]
     L.fa_back_get_error.restype = i
     L.fa_back_get_error.argtypes = []
     L.fa_back_status_string.restype = ctypes.c_char_p
@@ -72,6 +75,13 @@ def fa_back(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, 
     """Direct call of the C entry point; pointers are integers (device addresses) or None."""
     return int(lib().fa_back(q, k, k_type, v, v_type, mask, mask_heads, dO, float(scale), N, M, H, Hkv, D, Dv,
                              int(causal), dQ, dK, dV, lse, delta, workspace, workspace_bytes, stream))
+
+
+def fa_back_with_stats(q, k, k_type, v, v_type, mask, mask_heads, dO, lse, delta, scale, N, M, H, Hkv, D, Dv,
+                       causal, dQ, dK, dV, workspace, workspace_bytes, stream) -> int:
+    return int(lib().fa_back_with_stats(q, k, k_type, v, v_type, mask, mask_heads, dO, lse, delta, float(scale), N,
+                                        M, H, Hkv, D, Dv, int(causal), dQ, dK, dV, workspace, workspace_bytes,
+                                        stream))
 
 
 def fa_back_get_error() -> int:

@@ -38,13 +38,16 @@ def backward(q: torch.Tensor, k: torch.Tensor, k_type: int, v: torch.Tensor, v_t
              *, H: int, Hkv: int, D: int, Dv: int, M: int, scale: float, causal: bool = False,
              mask: Optional[torch.Tensor] = None, mask_heads: int = 0, out: Optional[dict] = None,
              workspace: Optional[Workspace] = None, stream: Optional[torch.cuda.Stream] = None,
-             workspace_bytes: Optional[int] = None) -> dict:
+             workspace_bytes: Optional[int] = None, lse: Optional[torch.Tensor] = None,
+             delta: Optional[torch.Tensor] = None) -> dict:
     """Run the backward on device tensors.
 
     q [N][H][D] f32, dO [N][H][Dv] f32, k/v uint8 raw cache rows [M][Hkv][row], mask int16/uint16
     binary16 bits [Hm][N][M] or None.  Returns {"dQ", "dK", "dV", "lse", "delta"} (f32 tensors).
     workspace_bytes (default fa_back_workspace_size) is the workspace given to fa_back, which
-    runs the fastest plan that fits it (at least fa_back_workspace_size_min).
+    runs the fastest plan that fits it (at least fa_back_workspace_size_min).  Given the forward's
+    row statistics lse and delta ([N][H] f32), fa_back_with_stats runs instead and the result
+    holds dQ, dK and dV only.
     """
     N = q.shape[0]
     dev = q.device
@@ -56,15 +59,26 @@ def backward(q: torch.Tensor, k: torch.Tensor, k_type: int, v: torch.Tensor, v_t
             "lse": torch.empty((N, H), dtype=torch.float32, device=dev),
             "delta": torch.empty((N, H), dtype=torch.float32, device=dev),
         }
-    for t in (q, k, v, dO, mask, *out.values()):
+    given = lse is not None or delta is not None
+    if given and (lse is None or delta is None):
+        raise FaBackError("lse and delta are given together")
+    if given:
+        out.pop("lse", None)
+        out.pop("delta", None)
+    for t in (q, k, v, dO, mask, lse, delta, *out.values()):
         if t is not None and not t.is_contiguous():
             raise FaBackError("tensors must be contiguous")
     ws_bytes = nat.fa_back_workspace_size(N, M, H, Hkv, D, Dv) if workspace_bytes is None else int(workspace_bytes)
     ws = (workspace or Workspace(dev)).get(ws_bytes)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
-    rc = nat.fa_back(_ptr(q), _ptr(k), k_type, _ptr(v), v_type, _ptr(mask), mask_heads, _ptr(dO), scale,
-                     N, M, H, Hkv, D, Dv, causal, _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]),
-                     _ptr(out["lse"]), _ptr(out["delta"]), ws.data_ptr(),
-                     ws.numel() if workspace_bytes is None else ws_bytes, s.cuda_stream)
+    nbytes = ws.numel() if workspace_bytes is None else ws_bytes
+    if given:
+        rc = nat.fa_back_with_stats(_ptr(q), _ptr(k), k_type, _ptr(v), v_type, _ptr(mask), mask_heads, _ptr(dO),
+                                    _ptr(lse), _ptr(delta), scale, N, M, H, Hkv, D, Dv, causal, _ptr(out["dQ"]),
+                                    _ptr(out["dK"]), _ptr(out["dV"]), ws.data_ptr(), nbytes, s.cuda_stream)
+    else:
+        rc = nat.fa_back(_ptr(q), _ptr(k), k_type, _ptr(v), v_type, _ptr(mask), mask_heads, _ptr(dO), scale,
+                         N, M, H, Hkv, D, Dv, causal, _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]),
+                         _ptr(out["lse"]), _ptr(out["delta"]), ws.data_ptr(), nbytes, s.cuda_stream)
     _check(rc)
     return out

@@ -172,10 +172,10 @@ constexpr int kProfCalls = 256, kProfSlots = 16;
 // (the read-out measures each kernel from the marker recorded before it)
 static const char* const kKernelNames[kProfSlots] = {
     "k_row_stats", "k_vsum", "k_finalize", "k_convert", "k_predecode", "k_rows_lse", "k_lse_merge", "k_rows_dq",
-    "k_dq_reduce", "k_cols", "k_dq_gemm", "", "", "", "", ""};
+    "k_dq_reduce", "k_cols", "k_dq_gemm", "k_stats_in", "", "", "", ""};
 enum {
   KS_STATS = 0, KS_VSUM, KS_FINAL, KS_CONVERT, KS_PREDECODE, KS_ROWS_LSE, KS_MERGE, KS_ROWS_DQ, KS_DQ_REDUCE,
-  KS_COLS, KS_DQ_GEMM, KS_N
+  KS_COLS, KS_DQ_GEMM, KS_STATS_IN, KS_N
 };
 
 struct Profiler {
@@ -281,10 +281,12 @@ static cudaError_t rows_pre(const Params& pl, const Params& pq, const Plan& P, c
   const long units = (long)pl.M * pl.Hkv * ((D + Dv) / 8);
   k_predecode<<<(unsigned)std::min<long>((units + 255) / 256, 16L * P.nsm), 256, 0, s>>>(pl);
   rec.mark(KS_PREDECODE);
-  k_rows3<D, Dv, BKL, 0><<<grid, FL::NT, FL::SMEM, s>>>(tmQ, tkl, tvl, pl);
-  rec.mark(KS_ROWS_LSE);
-  k_lse_merge<<<(unsigned)(((long)pl.Hkv * P.R + 255) / 256), 256, 0, s>>>(pl);
-  rec.mark(KS_MERGE);
+  if (!pl.lse_in) {  // else the per-row values come from the given lse and delta
+    k_rows3<D, Dv, BKL, 0><<<grid, FL::NT, FL::SMEM, s>>>(tmQ, tkl, tvl, pl);
+    rec.mark(KS_ROWS_LSE);
+    k_lse_merge<<<(unsigned)(((long)pl.Hkv * P.R + 255) / 256), 256, 0, s>>>(pl);
+    rec.mark(KS_MERGE);
+  }
   if (!P.dsq) {  // else dQ comes from the stored dS after the dK/dV pass
     k_rows3<D, Dv, BK, 1><<<grid, FQ::NT, FQ::SMEM, s>>>(tmQ, tkq, tvq, pq);
     rec.mark(KS_ROWS_DQ);
@@ -320,10 +322,12 @@ static cudaError_t rows_raw(Params pl, Params pq, const Plan& P, const CUtensorM
         !make_raw_map(&tkq, pq.k, pq.rbk, pq.Hkv, pq.M, pq.ke) || !make_raw_map(&tvq, pq.v, pq.rbv, pq.Hkv, pq.M, pq.ke))
       return cudaErrorInvalidValue;
   }
-  k_rows2<D, Dv, BKL, 0><<<grid, RL::NT, sm_l, s>>>(tmQ, tkl, tvl, pl);
-  rec.mark(KS_ROWS_LSE);
-  k_lse_merge<<<(unsigned)(((long)pl.Hkv * P.R + 255) / 256), 256, 0, s>>>(pl);
-  rec.mark(KS_MERGE);
+  if (!pl.lse_in) {
+    k_rows2<D, Dv, BKL, 0><<<grid, RL::NT, sm_l, s>>>(tmQ, tkl, tvl, pl);
+    rec.mark(KS_ROWS_LSE);
+    k_lse_merge<<<(unsigned)(((long)pl.Hkv * P.R + 255) / 256), 256, 0, s>>>(pl);
+    rec.mark(KS_MERGE);
+  }
   k_rows2<D, Dv, BK, 1><<<grid, RQ::NT, sm_q, s>>>(tmQ, tkq, tvq, pq);
   rec.mark(KS_ROWS_DQ);
   return cudaSuccess;
@@ -434,14 +438,27 @@ extern "C" fa_status fa_back(const float* q, const void* k, int k_type, const vo
                              float* lse, float* delta, void* workspace, size_t workspace_bytes, void* stream) {
   // the plan is the fastest one whose workspace fits the caller's
   return fab_back_capped(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal, dQ,
-                         dK, dV, lse, delta, workspace, workspace_bytes, stream, workspace_bytes);
+                         dK, dV, lse, delta, workspace, workspace_bytes, stream, workspace_bytes, nullptr, nullptr);
+}
+
+extern "C" fa_status fa_back_with_stats(const float* q, const void* k, int k_type, const void* v, int v_type,
+                                        const uint16_t* mask, int mask_heads, const float* dO, const float* lse,
+                                        const float* delta, float scale, int N, int M, int H, int Hkv, int D, int Dv,
+                                        int causal, float* dQ, float* dK, float* dV, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+  if (N > 0 && (!lse || !delta)) return FA_ERR_NULL;
+  if ((lse && (reinterpret_cast<uintptr_t>(lse) & 15)) || (delta && (reinterpret_cast<uintptr_t>(delta) & 15)))
+    return FA_ERR_ALIGN;
+  return fab_back_capped(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal, dQ,
+                         dK, dV, nullptr, nullptr, workspace, workspace_bytes, stream, workspace_bytes, lse, delta);
 }
 
 extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, const void* v, int v_type,
                                      const uint16_t* mask, int mask_heads, const float* dO, float scale, int N,
                                      int M, int H, int Hkv, int D, int Dv, int causal, float* dQ, float* dK,
                                      float* dV, float* lse, float* delta, void* workspace, size_t workspace_bytes,
-                                     void* stream, size_t ws_cap) {
+                                     void* stream, size_t ws_cap, const float* lse_in, const float* delta_in) {
+  const bool given = lse_in != nullptr;  // fa_back_with_stats: no lse/delta outputs
   // ---- argument checks (nothing is enqueued on failure)
   if (k_type < FA_F32 || k_type > FA_Q4_0 || v_type < FA_F32 || v_type > FA_Q4_0) return FA_ERR_TYPE;
   if (N < 0 || M < 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || Hkv > 256) return FA_ERR_SHAPE;
@@ -451,7 +468,8 @@ extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, 
   const long rbk = fa_row_bytes(k_type, D), rbv = fa_row_bytes(v_type, Dv);
   if (rbk <= 0 || rbv <= 0) return FA_ERR_SHAPE;
   const bool needQ = N > 0, needK = M > 0;
-  if ((needQ && (!q || !dO || !dQ || !lse || !delta)) || (needK && (!k || !v || !dK || !dV))) return FA_ERR_NULL;
+  if ((needQ && (!q || !dO || !dQ || (!given && (!lse || !delta)))) || (needK && (!k || !v || !dK || !dV)))
+    return FA_ERR_NULL;
   const void* ptrs16[] = {q, dO, dQ, dK, dV, lse, delta, k, v, mask};
   for (const void* pp : ptrs16)
     if (pp && !aligned(pp, 16)) return FA_ERR_ALIGN;
@@ -472,8 +490,8 @@ extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, 
     };
     fill(dK, nkd, 0.f);
     fill(dV, nkv, 0.f);
-    fill(lse, nq, -std::numeric_limits<float>::infinity());
-    fill(delta, nq, 0.f);
+    if (lse) fill(lse, nq, -std::numeric_limits<float>::infinity());
+    if (delta) fill(delta, nq, 0.f);
     fill(dQ, nq * D, 0.f);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
   }
@@ -510,6 +528,7 @@ extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, 
   p.vd = P.pre ? reinterpret_cast<__half*>(ws + P.off_vd) : nullptr;
   p.ds = P.dsq ? reinterpret_cast<__half*>(ws + P.off_ds) : nullptr;
   p.ldds = P.ldds;
+  p.lse_in = lse_in, p.delta_in = delta_in;
   p.raw_bulk = (rbk % 16 == 0 && rbv % 16 == 0 && rbk <= 2048 && rbv <= 2048) ? 1 : 0;
   p.rbk_pad = (int)((rbk + 15) / 16 * 16);
   p.rbv_pad = (int)((rbv + 15) / 16 * 16);
@@ -528,6 +547,10 @@ extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, 
   rec.mark(KS_FINAL);
   k_convert<<<(unsigned)std::min<long>(((long)N * H + 7) / 8, 8L * nsm), 256, 0, s>>>(p);
   rec.mark(KS_CONVERT);
+  if (given) {
+    k_stats_in<<<(unsigned)(((long)Hkv * P.R + 255) / 256), 256, 0, s>>>(p);
+    rec.mark(KS_STATS_IN);
+  }
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   return pick(D, Dv)(p, P, tmQ, tmO, s, rec) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -83,6 +83,8 @@ struct Params {
                   // [128 rows][64 keys] tiles, tile (hk, row tile qt, key tile kt64) at
                   // (hk * nQT + qt) * ldds + kt64
   int ldds;       // 64-key tiles per row tile (whole gradient-pass key tiles)
+  const float* lse_in;    // [N][H] given row lse (natural log; fa_back_with_stats), or null
+  const float* delta_in;  // [N][H] given row delta = rowsum(dO o O), or null
   // raw K/V staging of the row passes
   int raw_bulk;        // 1: rows are 16-byte multiples, copied by bulk async copies; 0: 4-byte async copies
   int rbk_pad, rbv_pad;  // raw row strides in shared memory (16-byte multiples)
@@ -1648,6 +1650,26 @@ __global__ void __launch_bounds__(256) k_lse_merge(Params p) {
     p.lse[(size_t)i * p.H + h] = -CUDART_INF_F;
     p.delta[(size_t)i * p.H + h] = 0.f;
   }
+}
+
+// The per-row values of the gradient passes from a given lse and delta (instead of the LSE
+// pass): lse2 = lse / ln 2 and the shifted delta in accumulator units, (delta - dO_i . r) sdO sV
+// (the gradient passes take dP' - delta' with dP' = dO' . V', V' shifted by r).  A row whose lse
+// is -inf (or not finite) has no allowed key.
+__global__ void __launch_bounds__(256) k_stats_in(Params p) {
+  const long idx = (long)blockIdx.x * 256 + threadIdx.x;
+  if (idx >= (long)p.Hkv * p.R) return;
+  const int hk = (int)(idx / p.R), r = (int)(idx % p.R);
+  const int i = r / p.G, h = hk * p.G + r % p.G;
+  const float lse = p.lse_in[(size_t)i * p.H + h];
+  if (!(lse > -CUDART_INF_F) || !isfinite(lse)) {
+    p.lse2[idx] = -CUDART_INF_F;
+    p.dlt[idx] = 0.f;
+    return;
+  }
+  const Stats* st = p.st;
+  p.lse2[idx] = lse * kLog2e;
+  p.dlt[idx] = (p.delta_in[(size_t)i * p.H + h] - p.dOr[idx]) * (st->sdO * st->sV);
 }
 
 // dQ = sum of the split partials, in split order.

@@ -104,6 +104,21 @@ fa_status fa_back(const float* q, const void* k, int k_type, const void* v, int 
                   int H, int Hkv, int D, int Dv, int causal, float* dQ, float* dK, float* dV,
                   float* lse, float* delta, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * fa_back() for a caller that already has the row statistics of the forward pass: lse [N][H]
+ * (natural log, -inf for a row with no allowed key) and delta [N][H] = rowsum(dO o O) with O the
+ * forward output.  The backward then skips its LSE/D pass (the QK^T and dO V^T products over every
+ * pair that only serve those statistics) and writes dQ, dK and dV only; every other argument is
+ * as for fa_back().  lse and delta are read, 16-byte aligned, and must come from the same
+ * Q, K, V, mask, scale and causal setting (the gradients are exact for the statistics given).
+ * With N > 0, NULL lse or delta is FA_ERR_NULL.
+ */
+fa_status fa_back_with_stats(const float* q, const void* k, int k_type, const void* v, int v_type,
+                             const uint16_t* mask, int mask_heads, const float* dO, const float* lse,
+                             const float* delta, float scale, int N, int M, int H, int Hkv, int D, int Dv,
+                             int causal, float* dQ, float* dK, float* dV, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
 /* Sticky device-side status of the kernels enqueued so far on the current device
  * (FA_OK or FA_ERR_TIMEOUT).  Synchronises the device, then clears the word. */
 fa_status fa_back_get_error(void);

@@ -152,3 +152,60 @@ def test_long_context_sampled(fb):
         assert np.max(np.abs(sk)) <= 1e-3 * scale_k
         want = p.dO[:, hk * p.G:(hk + 1) * p.G].astype(np.float64).sum(axis=(0, 1))
         assert nmse(got["dV"][:, hk].astype(np.float64).sum(axis=0), want) <= NMSE_TOL
+
+
+# fa_back_with_stats: the row statistics (lse, delta) given, as from a forward pass.  They are
+# the oracle's, so dQ, dK and dV are checked against the oracle at the same bar; the LSE pass
+# must not run.
+def with_stats(fb, p, workspace_bytes=None):
+    import oracle
+    ref = oracle.fa_back(p)
+    t = synth.device.to_torch(p, "cuda")
+    lse = torch.tensor(np.asarray(ref["lse"], dtype=np.float32), device="cuda").contiguous()
+    delta = torch.tensor(np.asarray(ref["delta"], dtype=np.float32), device="cuda").contiguous()
+    fb.fa_back_profile(True)
+    out = fb.backward(t["q"], t["k"], p.k_type, t["v"], p.v_type, t["dO"], H=p.H, Hkv=p.Hkv, D=p.D, Dv=p.Dv,
+                      M=p.M, scale=p.scale, causal=p.causal, mask=t["mask"], mask_heads=p.mask_heads,
+                      workspace_bytes=workspace_bytes, lse=lse, delta=delta)
+    torch.cuda.synchronize()
+    fb.fa_back_profile(False)
+    launched = {k for k, v in fb.fa_back_profile_read().items() if v[1] > 0}
+    assert "k_stats_in" in launched and "k_rows_lse" not in launched, launched
+    assert fb.fa_back_get_error() == 0
+    assert set(out) == {"dQ", "dK", "dV"}
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    res = {n: nmse(got[n], ref[n]) for n in ("dQ", "dK", "dV")}
+    assert all(v <= NMSE_TOL for v in res.values()), res
+    dead = ~np.isfinite(ref["lse"])
+    assert np.all(got["dQ"][dead] == 0.0)
+    return res
+
+
+@pytest.mark.parametrize("cfg", ["1", "1c", "3"])
+def test_with_stats_configs(fb, cfg):
+    print(cfg, with_stats(fb, synth.from_config(cfg)))
+
+
+@pytest.mark.parametrize("name", ["n_gt_m_causal", "finite_mask_hm1", "d256_dv128", "ragged_f16_causal"])
+def test_with_stats_edge_cases(fb, name):
+    p = synth.make_problem(name, seed=2000 + sorted(EDGE).index(name), **EDGE[name])
+    print(name, with_stats(fb, p))
+
+
+def test_with_stats_minimum_workspace(fb):
+    p = synth.from_config("3")
+    print(with_stats(fb, p, fb.fa_back_workspace_size_min(p.N, p.M, p.H, p.Hkv, p.D, p.Dv)))
+
+
+def test_with_stats_matches_fa_back_given_its_own_statistics(fb):
+    """Feeding fa_back's own lse/delta outputs back gives fa_back's gradients (up to the rounding
+    of lse and delta to f32)."""
+    p = synth.from_config("3")
+    t = synth.device.to_torch(p, "cuda")
+    kw = dict(H=p.H, Hkv=p.Hkv, D=p.D, Dv=p.Dv, M=p.M, scale=p.scale, causal=p.causal, mask=t["mask"],
+              mask_heads=p.mask_heads)
+    a = fb.backward(t["q"], t["k"], p.k_type, t["v"], p.v_type, t["dO"], **kw)
+    b = fb.backward(t["q"], t["k"], p.k_type, t["v"], p.v_type, t["dO"], lse=a["lse"], delta=a["delta"], **kw)
+    torch.cuda.synchronize()
+    for n in ("dQ", "dK", "dV"):
+        assert nmse(b[n].cpu().numpy(), a[n].cpu().numpy()) <= 1e-9, n
