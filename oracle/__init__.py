@@ -6,5 +6,5 @@ It wraps ``fa_oracle.c`` (plain C, double precision, one thread per core),
 which is compiled here with gcc and shares no code with the CUDA path.
 """
 from .oracle import (  # noqa: F401
-    build, lib_path, half_to_double, dequant, fa_back, default_threads,
+    build, lib_path, half_to_double, dequant, fa_back, fa_forward, default_threads,
 )

@@ -24,6 +24,11 @@
  *   dK[j,hk]= scale * sum_{h in group(hk)} sum_i dS_ij * Q[i,h]
  *   dV[j,hk]= sum_{h in group(hk)} sum_i p_ij * dO[i,h]
  *
+ * The forward output, for oracle_fa_forward (the attention the backward
+ * differentiates; 0 for a row without an allowed key):
+ *
+ *   O[i,h]  = sum_j p_ij * V^[j,hk]
+ *
  * K^ and V^ are the cache rows decoded exactly as the block formats define
  * them (a q8_0 block: binary16 scale d, then 32 int8 codes, value code*d;
  * a q4_0 block: binary16 scale d, then 16 bytes whose low nibble is element
@@ -120,6 +125,7 @@ typedef struct {
   int nkeys;
   /* outputs */
   double *lse, *delta, *dQ, *dK, *dV;
+  double* O; /* [N][H][Dv] forward output, or NULL */
   /* scheduling */
   int phase, nitems;
   int next;
@@ -212,6 +218,7 @@ static void phase1_item(Job* J, int item, double* S, double* DP, double* qt, dou
       J->lse[o] = -INFINITY;
       J->delta[o] = 0.0;
       if (qi >= 0) memset(J->dQ + (qi * H + h) * (int64_t)D, 0, sizeof(double) * D);
+      if (J->O) memset(J->O + o * Dv, 0, sizeof(double) * Dv);
       continue;
     }
     double sum = 0.0;
@@ -223,6 +230,16 @@ static void phase1_item(Job* J, int item, double* S, double* DP, double* qt, dou
       if (s[j] != -INFINITY) delta += exp(s[j] - lse) * dp[j];
     J->lse[o] = lse;
     J->delta[o] = delta;
+    if (J->O) {
+      double* out = J->O + o * Dv;
+      for (int c = 0; c < Dv; ++c) out[c] = 0.0;
+      for (int j = 0; j < M; ++j) {
+        if (s[j] == -INFINITY) continue;
+        const double p = exp(s[j] - lse);
+        const double* v = J->Vh + ((int64_t)j * Hkv + (h / G)) * Dv;
+        for (int c = 0; c < Dv; ++c) out[c] += p * v[c];
+      }
+    }
     if (qi >= 0) {
       double* out = J->dQ + (qi * H + h) * (int64_t)D;
       for (int c = 0; c < D; ++c) out[c] = 0.0;
@@ -357,11 +374,11 @@ int oracle_default_threads(void) {
  * Outputs: lse, delta [N][H]; dQ [n_dq][H][D]; dK [n_keys][Hkv][D]; dV [n_keys][Hkv][Dv].
  * Returns 0 on success, 1 on a bad argument, 2 when memory runs out.
  */
-int oracle_fa_back(const float* q, const uint8_t* k, int k_type, const uint8_t* v, int v_type,
-                   const uint16_t* mask, int mask_heads, const float* dO, double scale, int N, int M, int H,
-                   int Hkv, int D, int Dv, int causal, const int64_t* dq_rows, int n_dq_rows,
-                   const int64_t* dkv_keys, int n_dkv_keys, double* lse, double* delta, double* dQ, double* dK,
-                   double* dV, int nthreads) {
+static int run_oracle(const float* q, const uint8_t* k, int k_type, const uint8_t* v, int v_type,
+                      const uint16_t* mask, int mask_heads, const float* dO, double scale, int N, int M, int H,
+                      int Hkv, int D, int Dv, int causal, const int64_t* dq_rows, int n_dq_rows,
+                      const int64_t* dkv_keys, int n_dkv_keys, double* lse, double* delta, double* dQ, double* dK,
+                      double* dV, double* O, int nthreads) {
   if (!q || !k || !v || !dO || !lse || !delta) return 1;
   if (N < 0 || M < 0 || H <= 0 || Hkv <= 0 || D <= 0 || Dv <= 0 || H % Hkv) return 1;
   if (mask && mask_heads != 1 && mask_heads != H) return 1;
@@ -372,7 +389,7 @@ int oracle_fa_back(const float* q, const uint8_t* k, int k_type, const uint8_t* 
   pthread_mutex_init(&J.mu, NULL);
   J.N = N, J.M = M, J.H = H, J.Hkv = Hkv, J.D = D, J.Dv = Dv, J.G = H / Hkv, J.causal = causal;
   J.scale = scale, J.mask = mask, J.Hm = mask ? mask_heads : 1;
-  J.lse = lse, J.delta = delta, J.dQ = dQ, J.dK = dK, J.dV = dV;
+  J.lse = lse, J.delta = delta, J.dQ = dQ, J.dK = dK, J.dV = dV, J.O = O;
   int rc = 0;
   double* Qd = (double*)malloc(sizeof(double) * ((int64_t)N * H * D + 1));
   double* dOd = (double*)malloc(sizeof(double) * ((int64_t)N * H * Dv + 1));
@@ -429,5 +446,32 @@ done:
   free(dq_index);
   free(keys);
   pthread_mutex_destroy(&J.mu);
+  return rc;
+}
+
+int oracle_fa_back(const float* q, const uint8_t* k, int k_type, const uint8_t* v, int v_type,
+                   const uint16_t* mask, int mask_heads, const float* dO, double scale, int N, int M, int H,
+                   int Hkv, int D, int Dv, int causal, const int64_t* dq_rows, int n_dq_rows,
+                   const int64_t* dkv_keys, int n_dkv_keys, double* lse, double* delta, double* dQ, double* dK,
+                   double* dV, int nthreads) {
+  return run_oracle(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal, dq_rows,
+                    n_dq_rows, dkv_keys, n_dkv_keys, lse, delta, dQ, dK, dV, NULL, nthreads);
+}
+
+/*
+ * Forward: lse [N][H] and O [N][H][Dv] of the same attention (no gradients).  The backward's
+ * first phase is run with a zero dO, whose delta is discarded.  Same return codes.
+ */
+int oracle_fa_forward(const float* q, const uint8_t* k, int k_type, const uint8_t* v, int v_type,
+                      const uint16_t* mask, int mask_heads, double scale, int N, int M, int H, int Hkv, int D,
+                      int Dv, int causal, double* lse, double* O, int nthreads) {
+  if (!lse || !O || N < 0 || H <= 0 || Dv <= 0) return 1;
+  float* dO = (float*)calloc((size_t)N * H * Dv + 1, sizeof(float));
+  double* delta = (double*)malloc(sizeof(double) * ((size_t)N * H + 1));
+  int rc = (!dO || !delta) ? 2
+                           : run_oracle(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv,
+                                        causal, NULL, 0, NULL, 0, lse, delta, NULL, NULL, NULL, O, nthreads);
+  free(dO);
+  free(delta);
   return rc;
 }

@@ -65,6 +65,10 @@ def _declare(L):
         + [ctypes.c_int] * 7
         + [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
         + [ctypes.c_void_p] * 5 + [ctypes.c_int])
+    L.oracle_fa_forward.restype = ctypes.c_int
+    L.oracle_fa_forward.argtypes = (
+        [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+         ctypes.c_double] + [ctypes.c_int] * 7 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int])
 
 
 def _ptr(a: Optional[np.ndarray]):
@@ -124,3 +128,21 @@ def fa_back(p, dq_rows: Optional[Sequence[int]] = None, dkv_keys: Optional[Seque
     if rc:
         raise RuntimeError("oracle_fa_back failed with code %d" % rc)
     return {"lse": lse, "delta": delta, "dQ": dQ, "dK": dK, "dV": dV}
+
+
+def fa_forward(p, nthreads: int = 0, lib=None) -> dict:
+    """Forward of a synth.Problem (dO unused): float64 lse [N][H] and O [N][H][Dv]."""
+    L = lib if lib is not None else _load()
+    N, M, H, Hkv, D, Dv = p.N, p.M, p.H, p.Hkv, p.D, p.Dv
+    q = np.ascontiguousarray(p.q, dtype=np.float32)
+    k = np.ascontiguousarray(p.k, dtype=np.uint8)
+    v = np.ascontiguousarray(p.v, dtype=np.uint8)
+    mask = None if p.mask is None else np.ascontiguousarray(p.mask, dtype=np.uint16)
+    lse = np.empty((N, H), dtype=np.float64)
+    O = np.empty((N, H, Dv), dtype=np.float64)
+    rc = L.oracle_fa_forward(_ptr(q), _ptr(k), p.k_type, _ptr(v), p.v_type, _ptr(mask),
+                             p.mask_heads if mask is not None else 0, float(p.scale), N, M, H, Hkv, D, Dv,
+                             int(p.causal), _ptr(lse), _ptr(O), int(nthreads))
+    if rc:
+        raise RuntimeError("oracle_fa_forward failed with code %d" % rc)
+    return {"lse": lse, "O": O}

@@ -377,3 +377,43 @@ def test_empty_problems(oracle_lib):
     p = synth.make_problem("e1", N=4, M=0, H=2, Hkv=1, D=32, Dv=32, k_type="q8_0", v_type="q8_0", seed=1)
     got = oracle_lib.fa_back(p)
     assert np.all(got["lse"] == -np.inf) and np.all(got["delta"] == 0) and np.all(got["dQ"] == 0)
+
+
+# ------------------------------------------------------------------------------------------------
+# forward output O (oracle_fa_forward)
+
+@pytest.mark.parametrize("case", range(len(AUTOGRAD_CASES)))
+def test_forward_matches_torch(oracle_lib, case):
+    p = synth.make_problem(f"fw{case}", seed=300 + case, **AUTOGRAD_CASES[case])
+    ref = torch_reference(p)
+    got = oracle_lib.fa_forward(p)
+    assert rel_err(got["lse"], ref["lse"]) < 1e-12
+    assert rel_err(got["O"], ref["O"]) < 1e-12
+
+
+def test_forward_O_gives_the_backward_delta(oracle_lib):
+    """rowsum(dO o O) from the forward's O equals the backward's delta (formed as sum p * dP)."""
+    p = synth.make_problem("fwd_delta", N=24, M=300, H=8, Hkv=2, D=64, Dv=128, k_type="q4_0", v_type="q8_0",
+                           causal=True, mask="random", mask_p=0.1, full_rows=2, seed=71)
+    fw = oracle_lib.fa_forward(p)
+    bw = oracle_lib.fa_back(p, want_dq=False, want_dkv=False)
+    assert np.array_equal(fw["lse"], bw["lse"])
+    d = (p.dO.astype(np.float64) * fw["O"]).sum(-1)
+    assert rel_err(d, bw["delta"]) < 1e-12
+    dead = ~np.isfinite(fw["lse"])
+    assert dead.any() and np.all(fw["O"][dead] == 0.0)
+
+
+def test_forward_single_key_and_zero_queries(oracle_lib):
+    p = synth.make_problem("fw_m1", N=3, M=1, H=4, Hkv=2, D=32, Dv=64, k_type="q8_0", v_type="q4_0", seed=72)
+    vhat = np_decode(p.v, p.v_type, p.Dv)
+    got = oracle_lib.fa_forward(p)
+    for h in range(p.H):
+        assert np.array_equal(got["O"][:, h], np.broadcast_to(vhat[0, h // p.G], (p.N, p.Dv)))
+    p = synth.make_problem("fw_q0", N=4, M=10, H=4, Hkv=2, D=32, Dv=32, k_type="f16", v_type="q8_0", seed=73)
+    p.q[:] = 0.0
+    vhat = np_decode(p.v, p.v_type, p.Dv)
+    got = oracle_lib.fa_forward(p)
+    for h in range(p.H):
+        want = vhat[:, h // p.G].mean(axis=0)
+        assert rel_err(got["O"][:, h], np.broadcast_to(want, (p.N, p.Dv))) < 1e-14
