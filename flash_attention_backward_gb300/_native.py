@@ -42,6 +42,10 @@ def lib():
     L.fa_back_with_stats.restype = i
     L.fa_back_with_stats.argtypes = [vp, vp, i, vp, i, vp, i, vp, vp, vp, f, i, i, i, i, i, i, i, vp, vp, vp, vp, sz,
                                      vp]
+    L.fa_forward_workspace_size.restype = sz
+    L.fa_forward_workspace_size.argtypes = [i] * 6
+    L.fa_forward.restype = i
+    L.fa_forward.argtypes = [vp, vp, i, vp, i, vp, i, f, i, i, i, i, i, i, i, vp, vp, vp, sz, vp]
     L.fa_back_get_error.restype = i
     L.fa_back_get_error.argtypes = []
     L.fa_back_status_string.restype = ctypes.c_char_p
@@ -82,6 +86,16 @@ def fa_back_with_stats(q, k, k_type, v, v_type, mask, mask_heads, dO, lse, delta
     return int(lib().fa_back_with_stats(q, k, k_type, v, v_type, mask, mask_heads, dO, lse, delta, float(scale), N,
                                         M, H, Hkv, D, Dv, int(causal), dQ, dK, dV, workspace, workspace_bytes,
                                         stream))
+
+
+def fa_forward_workspace_size(N: int, M: int, H: int, Hkv: int, D: int, Dv: int) -> int:
+    return int(lib().fa_forward_workspace_size(N, M, H, Hkv, D, Dv))
+
+
+def fa_forward(q, k, k_type, v, v_type, mask, mask_heads, scale, N, M, H, Hkv, D, Dv, causal, O, lse,
+               workspace, workspace_bytes, stream) -> int:
+    return int(lib().fa_forward(q, k, k_type, v, v_type, mask, mask_heads, float(scale), N, M, H, Hkv, D, Dv,
+                                int(causal), O, lse, workspace, workspace_bytes, stream))
 
 
 def fa_back_get_error() -> int:

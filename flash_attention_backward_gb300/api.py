@@ -82,3 +82,23 @@ def backward(q: torch.Tensor, k: torch.Tensor, k_type: int, v: torch.Tensor, v_t
                          _ptr(out["lse"]), _ptr(out["delta"]), ws.data_ptr(), nbytes, s.cuda_stream)
     _check(rc)
     return out
+
+
+def forward(q: torch.Tensor, k: torch.Tensor, k_type: int, v: torch.Tensor, v_type: int, *, H: int, Hkv: int,
+            D: int, Dv: int, M: int, scale: float, causal: bool = False, mask: Optional[torch.Tensor] = None,
+            mask_heads: int = 0, workspace: Optional[Workspace] = None,
+            stream: Optional[torch.cuda.Stream] = None) -> dict:
+    """The forward over the raw cache: {"O": [N][H][Dv], "lse": [N][H]} (f32 tensors)."""
+    N = q.shape[0]
+    dev = q.device
+    out = {"O": torch.empty((N, H, Dv), dtype=torch.float32, device=dev),
+           "lse": torch.empty((N, H), dtype=torch.float32, device=dev)}
+    for t in (q, k, v, mask):
+        if t is not None and not t.is_contiguous():
+            raise FaBackError("tensors must be contiguous")
+    ws = (workspace or Workspace(dev)).get(nat.fa_forward_workspace_size(N, M, H, Hkv, D, Dv))
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    rc = nat.fa_forward(_ptr(q), _ptr(k), k_type, _ptr(v), v_type, _ptr(mask), mask_heads, scale, N, M, H, Hkv, D,
+                        Dv, causal, _ptr(out["O"]), _ptr(out["lse"]), ws.data_ptr(), ws.numel(), s.cuda_stream)
+    _check(rc)
+    return out

@@ -60,7 +60,9 @@ static void layout(Plan& P, int M, int Hkv, int D, int Dv) {
   P.off_lse2 = o; o = align256(o + sizeof(float) * (size_t)Hkv * P.R);
   P.off_dlt = o; o = align256(o + sizeof(float) * (size_t)Hkv * P.R);
   P.off_part = o; o = align256(o + sizeof(float) * 3 * (size_t)P.nsplit * Hkv * P.R);
-  P.off_dqpart = o; o = align256(o + (P.nsplit_dq > 1 ? sizeof(float) * (size_t)P.nsplit_dq * Hkv * P.R * D : 0));
+  // split partials of dQ (backward) or O (forward)
+  P.off_dqpart = o;
+  o = align256(o + (P.nsplit_dq > 1 ? sizeof(float) * (size_t)P.nsplit_dq * Hkv * P.R * (D > Dv ? D : Dv) : 0));
   P.off_q16 = o; o = align256(o + 2 * (size_t)Hkv * P.R * D);
   P.off_do16 = o; o = align256(o + 2 * (size_t)Hkv * P.R * Dv);
   P.off_bstat = o; o = align256(o + sizeof(float) * 8 * (size_t)P.nblk_stats);
@@ -172,10 +174,10 @@ constexpr int kProfCalls = 256, kProfSlots = 16;
 // (the read-out measures each kernel from the marker recorded before it)
 static const char* const kKernelNames[kProfSlots] = {
     "k_row_stats", "k_vsum", "k_finalize", "k_convert", "k_predecode", "k_rows_lse", "k_lse_merge", "k_rows_dq",
-    "k_dq_reduce", "k_cols", "k_dq_gemm", "k_stats_in", "", "", "", ""};
+    "k_dq_reduce", "k_cols", "k_dq_gemm", "k_stats_in", "k_fwd_lse", "k_fwd_o", "k_o_reduce", ""};
 enum {
   KS_STATS = 0, KS_VSUM, KS_FINAL, KS_CONVERT, KS_PREDECODE, KS_ROWS_LSE, KS_MERGE, KS_ROWS_DQ, KS_DQ_REDUCE,
-  KS_COLS, KS_DQ_GEMM, KS_STATS_IN, KS_N
+  KS_COLS, KS_DQ_GEMM, KS_STATS_IN, KS_FWD_LSE, KS_FWD_O, KS_O_REDUCE, KS_N
 };
 
 struct Profiler {
@@ -381,8 +383,60 @@ static cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& 
   return cudaGetLastError();
 }
 
+// Forward: lse by the LSE pass without dP (MODE 3), then O += P V' per row tile with P from that
+// lse (MODE 2), and the split reduce.  Plan level 1 (binary16 K'/V' copies, no stored dS).
+template <int D, int Dv>
+static cudaError_t run_forward(const Params& p, const Plan& P, const CUtensorMap& tmQ, const CUtensorMap&,
+                               cudaStream_t s, CallRec& rec) {
+  constexpr int BK = (D + Dv <= 256) ? 128 : 64;
+  constexpr int BKL = kBKLse;
+  using FL = Rows3Cfg<D, Dv, BKL, 3>;
+  using FO = Rows3Cfg<D, Dv, BK, 2>;
+  Params pl = p;
+  pl.nKT = (p.M + BKL - 1) / BKL;
+  pl.kt_per_split = p.kt_per_split / (BKL / BK);
+  const dim3 grid(P.nQT, p.Hkv, P.nsplit);
+  CUtensorMap tkl, tko, tvo;
+  if (!make_map(&tkl, p.kd, 64, p.M, p.Hkv * (D / 64), BKL) || !make_map(&tko, p.kd, 64, p.M, p.Hkv * (D / 64), BK) ||
+      !make_map(&tvo, p.vd, 64, p.M, p.Hkv * (Dv / 64), BK))
+    return cudaErrorInvalidValue;
+  cudaError_t e;
+  if ((e = set_smem(k_rows3<D, Dv, BKL, 3>, FL::SMEM)) != cudaSuccess) return e;
+  if ((e = set_smem(k_rows3<D, Dv, BK, 2>, FO::SMEM)) != cudaSuccess) return e;
+  const long units = (long)p.M * p.Hkv * ((D + Dv) / 8);
+  k_predecode<<<(unsigned)std::min<long>((units + 255) / 256, 16L * P.nsm), 256, 0, s>>>(p);
+  rec.mark(KS_PREDECODE);
+  k_rows3<D, Dv, BKL, 3><<<grid, FL::NT, FL::SMEM, s>>>(tmQ, tkl, tkl, pl);  // no V' (its map unused)
+  rec.mark(KS_FWD_LSE);
+  k_lse_merge<<<(unsigned)(((long)p.Hkv * P.R + 255) / 256), 256, 0, s>>>(pl);
+  rec.mark(KS_MERGE);
+  k_rows3<D, Dv, BK, 2><<<grid, FO::NT, FO::SMEM, s>>>(tmQ, tko, tvo, p);
+  rec.mark(KS_FWD_O);
+  if (P.nsplit > 1) {
+    k_o_reduce<<<(unsigned)(((long)p.Hkv * P.R * (Dv / 4) + 255) / 256), 256, 0, s>>>(p);
+    rec.mark(KS_O_REDUCE);
+  }
+  return cudaGetLastError();
+}
+
 using RunFn = cudaError_t (*)(const Params&, const Plan&, const CUtensorMap&, const CUtensorMap&, cudaStream_t,
                               CallRec&);
+
+static RunFn pick_fwd(int D, int Dv) {
+#define FAB_CASE(a, b) \
+  if (D == a && Dv == b) return run_forward<a, b>;
+  FAB_CASE(64, 64)
+  FAB_CASE(64, 128)
+  FAB_CASE(64, 256)
+  FAB_CASE(128, 64)
+  FAB_CASE(128, 128)
+  FAB_CASE(128, 256)
+  FAB_CASE(256, 64)
+  FAB_CASE(256, 128)
+  FAB_CASE(256, 256)
+#undef FAB_CASE
+  return nullptr;
+}
 
 static RunFn pick(int D, int Dv) {
 #define FAB_CASE(a, b) \
@@ -438,7 +492,26 @@ extern "C" fa_status fa_back(const float* q, const void* k, int k_type, const vo
                              float* lse, float* delta, void* workspace, size_t workspace_bytes, void* stream) {
   // the plan is the fastest one whose workspace fits the caller's
   return fab_back_capped(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal, dQ,
-                         dK, dV, lse, delta, workspace, workspace_bytes, stream, workspace_bytes, nullptr, nullptr);
+                         dK, dV, lse, delta, workspace, workspace_bytes, stream, workspace_bytes, nullptr, nullptr,
+                         nullptr);
+}
+
+extern "C" size_t fa_forward_workspace_size(int N, int M, int H, int Hkv, int D, int Dv) {
+  if (N < 0 || M < 0 || H <= 0 || Hkv <= 0 || H % Hkv) return 0;
+  int nsm = device_sms(nullptr, nullptr);
+  if (nsm <= 0) nsm = 152;
+  return plan_variant(N, M, H, Hkv, D, Dv, nsm, SIZE_MAX, 1).total;
+}
+
+extern "C" fa_status fa_forward(const float* q, const void* k, int k_type, const void* v, int v_type,
+                                const uint16_t* mask, int mask_heads, float scale, int N, int M, int H, int Hkv,
+                                int D, int Dv, int causal, float* O, float* lse, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  if (N > 0 && !O) return FA_ERR_NULL;
+  if (O && (reinterpret_cast<uintptr_t>(O) & 15)) return FA_ERR_ALIGN;
+  return fab_back_capped(q, k, k_type, v, v_type, mask, mask_heads, nullptr, scale, N, M, H, Hkv, D, Dv, causal,
+                         nullptr, nullptr, nullptr, lse, nullptr, workspace, workspace_bytes, stream, SIZE_MAX,
+                         nullptr, nullptr, O);
 }
 
 extern "C" fa_status fa_back_with_stats(const float* q, const void* k, int k_type, const void* v, int v_type,
@@ -450,15 +523,18 @@ extern "C" fa_status fa_back_with_stats(const float* q, const void* k, int k_typ
   if ((lse && (reinterpret_cast<uintptr_t>(lse) & 15)) || (delta && (reinterpret_cast<uintptr_t>(delta) & 15)))
     return FA_ERR_ALIGN;
   return fab_back_capped(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal, dQ,
-                         dK, dV, nullptr, nullptr, workspace, workspace_bytes, stream, workspace_bytes, lse, delta);
+                         dK, dV, nullptr, nullptr, workspace, workspace_bytes, stream, workspace_bytes, lse, delta,
+                         nullptr);
 }
 
 extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, const void* v, int v_type,
                                      const uint16_t* mask, int mask_heads, const float* dO, float scale, int N,
                                      int M, int H, int Hkv, int D, int Dv, int causal, float* dQ, float* dK,
                                      float* dV, float* lse, float* delta, void* workspace, size_t workspace_bytes,
-                                     void* stream, size_t ws_cap, const float* lse_in, const float* delta_in) {
+                                     void* stream, size_t ws_cap, const float* lse_in, const float* delta_in,
+                                     float* O) {
   const bool given = lse_in != nullptr;  // fa_back_with_stats: no lse/delta outputs
+  const bool forward = O != nullptr;     // fa_forward: lse and O only
   // ---- argument checks (nothing is enqueued on failure)
   if (k_type < FA_F32 || k_type > FA_Q4_0 || v_type < FA_F32 || v_type > FA_Q4_0) return FA_ERR_TYPE;
   if (N < 0 || M < 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || Hkv > 256) return FA_ERR_SHAPE;
@@ -468,8 +544,11 @@ extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, 
   const long rbk = fa_row_bytes(k_type, D), rbv = fa_row_bytes(v_type, Dv);
   if (rbk <= 0 || rbv <= 0) return FA_ERR_SHAPE;
   const bool needQ = N > 0, needK = M > 0;
-  if ((needQ && (!q || !dO || !dQ || (!given && (!lse || !delta)))) || (needK && (!k || !v || !dK || !dV)))
+  if (forward) {
+    if (needQ && (!q || !lse || (needK && (!k || !v)))) return FA_ERR_NULL;
+  } else if ((needQ && (!q || !dO || !dQ || (!given && (!lse || !delta)))) || (needK && (!k || !v || !dK || !dV))) {
     return FA_ERR_NULL;
+  }
   const void* ptrs16[] = {q, dO, dQ, dK, dV, lse, delta, k, v, mask};
   for (const void* pp : ptrs16)
     if (pp && !aligned(pp, 16)) return FA_ERR_ALIGN;
@@ -477,7 +556,8 @@ extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, 
   const int nsm = device_sms(&major, &minor);
   if (nsm <= 0) return FA_ERR_CUDA;
   if (major != 10 || minor != 3) return FA_ERR_DEVICE;
-  const Plan P = make_plan(N, M, H, Hkv, D, Dv, nsm, ws_cap);
+  // the forward runs plan level 1 (K'/V' copies, no stored dS)
+  const Plan P = forward ? plan_variant(N, M, H, Hkv, D, Dv, nsm, SIZE_MAX, 1) : make_plan(N, M, H, Hkv, D, Dv, nsm, ws_cap);
   if (!workspace || workspace_bytes < P.total) return FA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return FA_ERR_ALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -485,13 +565,14 @@ extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, 
   // ---- degenerate shapes: every output element is still written
   if (N == 0 || M == 0) {
     const long nq = (long)N * H, nkd = (long)M * Hkv * D, nkv = (long)M * Hkv * Dv;
-    auto fill = [&](float* x, long n, float val) {
-      if (n > 0) k_fill<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(x, n, val);
+    auto fill = [&](float* x, long n, float val) {  // outputs the call does not have are null
+      if (x && n > 0) k_fill<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(x, n, val);
     };
     fill(dK, nkd, 0.f);
     fill(dV, nkv, 0.f);
     if (lse) fill(lse, nq, -std::numeric_limits<float>::infinity());
     if (delta) fill(delta, nq, 0.f);
+    if (O) fill(O, nq * Dv, 0.f);
     fill(dQ, nq * D, 0.f);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
   }
@@ -529,6 +610,7 @@ extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, 
   p.ds = P.dsq ? reinterpret_cast<__half*>(ws + P.off_ds) : nullptr;
   p.ldds = P.ldds;
   p.lse_in = lse_in, p.delta_in = delta_in;
+  p.o_out = O;
   p.raw_bulk = (rbk % 16 == 0 && rbv % 16 == 0 && rbk <= 2048 && rbv <= 2048) ? 1 : 0;
   p.rbk_pad = (int)((rbk + 15) / 16 * 16);
   p.rbv_pad = (int)((rbv + 15) / 16 * 16);
@@ -552,7 +634,7 @@ extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, 
     rec.mark(KS_STATS_IN);
   }
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  return pick(D, Dv)(p, P, tmQ, tmO, s, rec) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return (forward ? pick_fwd(D, Dv) : pick(D, Dv))(p, P, tmQ, tmO, s, rec) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 extern "C" fa_status fa_back_selftest_timeout(unsigned long long limit_ns, void* stream) {

@@ -119,6 +119,20 @@ fa_status fa_back_with_stats(const float* q, const void* k, int k_type, const vo
                              int causal, float* dQ, float* dK, float* dV, void* workspace,
                              size_t workspace_bytes, void* stream);
 
+/*
+ * The forward of the same attention over the raw cache: O [N][H][Dv] = softmax(scale * q k^T +
+ * mask, causal tail) v and lse [N][H] (natural log), f32.  A row without an allowed key gets
+ * O = 0 and lse = -inf.  Arguments as for fa_back(); O and lse are written, 16-byte aligned.
+ * The lse it writes, with delta = rowsum(dO o O), is what fa_back_with_stats() takes.
+ * Computation: the LSE pass without its dP product, then O += P v' per row tile with P from
+ * that lse (binary16 operands as in the backward), key splits reduced in a fixed order.
+ */
+size_t fa_forward_workspace_size(int N, int M, int H, int Hkv, int D, int Dv);
+fa_status fa_forward(const float* q, const void* k, int k_type, const void* v, int v_type,
+                     const uint16_t* mask, int mask_heads, float scale, int N, int M, int H, int Hkv,
+                     int D, int Dv, int causal, float* O, float* lse, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
 /* Sticky device-side status of the kernels enqueued so far on the current device
  * (FA_OK or FA_ERR_TIMEOUT).  Synchronises the device, then clears the word. */
 fa_status fa_back_get_error(void);

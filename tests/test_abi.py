@@ -28,7 +28,8 @@ def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
         ["fa_back", "fa_back_get_error", "fa_back_noalloc", "fa_back_profile", "fa_back_profile_read",
          "fa_back_selftest_timeout", "fa_back_status_string", "fa_back_workspace_size",
-         "fa_back_with_stats", "fa_back_workspace_size_min", "fa_row_bytes"])
+         "fa_back_with_stats", "fa_back_workspace_size_min", "fa_forward", "fa_forward_workspace_size",
+         "fa_row_bytes"])
 
 
 def test_every_declared_symbol_is_exported(L):
@@ -98,3 +99,14 @@ def test_with_stats_rejects_missing_or_misaligned_statistics(L):
     assert fb.STATUS[fb.fa_back_with_stats(**dict(a, lse=None))] == "FA_ERR_NULL"
     assert fb.STATUS[fb.fa_back_with_stats(**dict(a, delta=None))] == "FA_ERR_NULL"
     assert fb.STATUS[fb.fa_back_with_stats(**dict(a, lse=0x8004))] == "FA_ERR_ALIGN"
+
+
+def test_forward_workspace_and_argument_errors(L):
+    assert 0 < fb.fa_forward_workspace_size(64, 512, 8, 2, 128, 128) < fb.fa_back_workspace_size(64, 512, 8, 2, 128, 128)
+    a = dict(q=0x1000, k=0x2000, k_type=2, v=0x3000, v_type=2, mask=None, mask_heads=0, scale=0.1, N=8, M=32, H=4,
+             Hkv=2, D=128, Dv=128, causal=0, O=0x5000, lse=0x8000, workspace=0x10000, workspace_bytes=1 << 30,
+             stream=None)
+    assert fb.STATUS[fb.fa_forward(**dict(a, O=None))] == "FA_ERR_NULL"
+    assert fb.STATUS[fb.fa_forward(**dict(a, lse=None))] == "FA_ERR_NULL"
+    assert fb.STATUS[fb.fa_forward(**dict(a, O=0x5004))] == "FA_ERR_ALIGN"
+    assert fb.STATUS[fb.fa_forward(**dict(a, D=96, Dv=96))] == "FA_ERR_UNSUPPORTED"
