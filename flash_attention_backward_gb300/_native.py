@@ -42,6 +42,9 @@ def lib():
     L.fa_back_with_stats.restype = i
     L.fa_back_with_stats.argtypes = [vp, vp, i, vp, i, vp, i, vp, vp, vp, f, i, i, i, i, i, i, i, vp, vp, vp, vp, sz,
                                      vp]
+    L.fa_back_batched.restype = i
+    L.fa_back_batched.argtypes = [i, vp, vp, i, vp, i, vp, i, i, vp, f, i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp,
+                                  sz, vp]
     L.fa_forward_workspace_size.restype = sz
     L.fa_forward_workspace_size.argtypes = [i] * 6
     L.fa_forward.restype = i
@@ -86,6 +89,13 @@ def fa_back_with_stats(q, k, k_type, v, v_type, mask, mask_heads, dO, lse, delta
     return int(lib().fa_back_with_stats(q, k, k_type, v, v_type, mask, mask_heads, dO, lse, delta, float(scale), N,
                                         M, H, Hkv, D, Dv, int(causal), dQ, dK, dV, workspace, workspace_bytes,
                                         stream))
+
+
+def fa_back_batched(B, q, k, k_type, v, v_type, mask, mask_heads, mask_per_batch, dO, scale, N, M, H, Hkv, D, Dv,
+                    causal, dQ, dK, dV, lse, delta, workspace, workspace_bytes, stream) -> int:
+    return int(lib().fa_back_batched(B, q, k, k_type, v, v_type, mask, mask_heads, int(mask_per_batch), dO,
+                                     float(scale), N, M, H, Hkv, D, Dv, int(causal), dQ, dK, dV, lse, delta,
+                                     workspace, workspace_bytes, stream))
 
 
 def fa_forward_workspace_size(N: int, M: int, H: int, Hkv: int, D: int, Dv: int) -> int:

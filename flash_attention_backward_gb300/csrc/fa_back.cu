@@ -496,6 +496,32 @@ extern "C" fa_status fa_back(const float* q, const void* k, int k_type, const vo
                          nullptr);
 }
 
+extern "C" fa_status fa_back_batched(int B, const float* q, const void* k, int k_type, const void* v, int v_type,
+                                     const uint16_t* mask, int mask_heads, int mask_per_batch, const float* dO,
+                                     float scale, int N, int M, int H, int Hkv, int D, int Dv, int causal, float* dQ,
+                                     float* dK, float* dV, float* lse, float* delta, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  if (B < 0) return FA_ERR_SHAPE;
+  const long rbk = fa_row_bytes(k_type, D), rbv = fa_row_bytes(v_type, Dv);
+  if (rbk <= 0 || rbv <= 0) return FA_ERR_SHAPE;
+  if (N < 0 || M < 0 || H <= 0 || Hkv <= 0) return FA_ERR_SHAPE;
+  const long hm = mask ? (mask_heads > 0 ? mask_heads : 1) : 0;
+  // one problem after another on the stream, sharing the workspace; batch b's slices start
+  // b problems into each tensor
+  for (int b = 0; b < B; ++b) {
+    const size_t nq = (size_t)b * N * H, nk = (size_t)b * M * Hkv;
+    const fa_status rc = fa_back(
+        q ? q + nq * D : nullptr, k ? static_cast<const uint8_t*>(k) + nk * rbk : nullptr, k_type,
+        v ? static_cast<const uint8_t*>(v) + nk * rbv : nullptr, v_type,
+        mask ? mask + (mask_per_batch ? (size_t)b * hm * N * M : 0) : nullptr, mask_heads, dO ? dO + nq * Dv : nullptr,
+        scale, N, M, H, Hkv, D, Dv, causal, dQ ? dQ + nq * D : nullptr, dK ? dK + nk * D : nullptr,
+        dV ? dV + nk * Dv : nullptr, lse ? lse + nq : nullptr, delta ? delta + nq : nullptr, workspace,
+        workspace_bytes, stream);
+    if (rc != FA_OK) return rc;
+  }
+  return FA_OK;
+}
+
 extern "C" size_t fa_forward_workspace_size(int N, int M, int H, int Hkv, int D, int Dv) {
   if (N < 0 || M < 0 || H <= 0 || Hkv <= 0 || H % Hkv) return 0;
   int nsm = device_sms(nullptr, nullptr);

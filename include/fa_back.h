@@ -133,6 +133,20 @@ fa_status fa_forward(const float* q, const void* k, int k_type, const void* v, i
                      int D, int Dv, int causal, float* O, float* lse, void* workspace,
                      size_t workspace_bytes, void* stream);
 
+/*
+ * B independent backwards of the same shape (a leading batch dimension, ggml's ne[3]): q, dO,
+ * dQ [B][N][H][·]; k, v, dK, dV [B][M][Hkv][·]; lse, delta [B][N][H]; the mask [B][Hm][N][M]
+ * when mask_per_batch != 0, else one [Hm][N][M] shared by every batch.  All tensors contiguous.
+ * Batch b runs as fa_back() on its slices, one after another on `stream`, sharing the workspace
+ * (fa_back_workspace_size() of one problem suffices); every slice must meet fa_back()'s
+ * alignment.  The first failing batch's status is returned (earlier batches are enqueued).
+ */
+fa_status fa_back_batched(int B, const float* q, const void* k, int k_type, const void* v, int v_type,
+                          const uint16_t* mask, int mask_heads, int mask_per_batch, const float* dO,
+                          float scale, int N, int M, int H, int Hkv, int D, int Dv, int causal, float* dQ,
+                          float* dK, float* dV, float* lse, float* delta, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
 /* Sticky device-side status of the kernels enqueued so far on the current device
  * (FA_OK or FA_ERR_TIMEOUT).  Synchronises the device, then clears the word. */
 fa_status fa_back_get_error(void);

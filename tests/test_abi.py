@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
-        ["fa_back", "fa_back_get_error", "fa_back_noalloc", "fa_back_profile", "fa_back_profile_read",
+        ["fa_back", "fa_back_batched", "fa_back_get_error", "fa_back_noalloc", "fa_back_profile", "fa_back_profile_read",
          "fa_back_selftest_timeout", "fa_back_status_string", "fa_back_workspace_size",
          "fa_back_with_stats", "fa_back_workspace_size_min", "fa_forward", "fa_forward_workspace_size",
          "fa_row_bytes"])
@@ -110,3 +110,9 @@ def test_forward_workspace_and_argument_errors(L):
     assert fb.STATUS[fb.fa_forward(**dict(a, lse=None))] == "FA_ERR_NULL"
     assert fb.STATUS[fb.fa_forward(**dict(a, O=0x5004))] == "FA_ERR_ALIGN"
     assert fb.STATUS[fb.fa_forward(**dict(a, D=96, Dv=96))] == "FA_ERR_UNSUPPORTED"
+
+
+def test_batched_rejects_a_negative_batch(L):
+    rc = fb.fa_back_batched(-1, 0x1000, 0x2000, 2, 0x3000, 2, None, 0, 0, 0x4000, 0.1, 8, 32, 4, 2, 128, 128, 0,
+                            0x5000, 0x6000, 0x7000, 0x8000, 0x9000, 0x10000, 1 << 30, None)
+    assert fb.STATUS[rc] == "FA_ERR_SHAPE"

@@ -209,3 +209,52 @@ def test_with_stats_matches_fa_back_given_its_own_statistics(fb):
     torch.cuda.synchronize()
     for n in ("dQ", "dK", "dV"):
         assert nmse(b[n].cpu().numpy(), a[n].cpu().numpy()) <= 1e-9, n
+
+
+def _stack(problems, key):
+    arrs = [getattr(q, key) for q in problems]
+    return None if arrs[0] is None else np.ascontiguousarray(np.stack(arrs))
+
+
+def run_batched(fb, problems, mask_per_batch):
+    p0 = problems[0]
+    B = len(problems)
+    dev = lambda a, dt=None: None if a is None else torch.from_numpy(a).to("cuda")
+    q, k, v, dO = (dev(_stack(problems, n)) for n in ("q", "k", "v", "dO"))
+    mask = dev(_stack(problems, "mask")) if mask_per_batch else dev(p0.mask)
+    out = {"dQ": torch.empty((B, p0.N, p0.H, p0.D), device="cuda"),
+           "dK": torch.empty((B, p0.M, p0.Hkv, p0.D), device="cuda"),
+           "dV": torch.empty((B, p0.M, p0.Hkv, p0.Dv), device="cuda"),
+           "lse": torch.empty((B, p0.N, p0.H), device="cuda"), "delta": torch.empty((B, p0.N, p0.H), device="cuda")}
+    need = fb.fa_back_workspace_size(p0.N, p0.M, p0.H, p0.Hkv, p0.D, p0.Dv)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    rc = fb.fa_back_batched(B, q.data_ptr(), k.data_ptr(), p0.k_type, v.data_ptr(), p0.v_type,
+                            None if mask is None else mask.data_ptr(), p0.mask_heads, int(mask_per_batch),
+                            dO.data_ptr(), p0.scale, p0.N, p0.M, p0.H, p0.Hkv, p0.D, p0.Dv, int(p0.causal),
+                            *[out[n].data_ptr() for n in ("dQ", "dK", "dV", "lse", "delta")], ws.data_ptr(), need,
+                            torch.cuda.current_stream().cuda_stream)
+    assert fb.STATUS[rc] == "FA_OK"
+    torch.cuda.synchronize()
+    assert fb.fa_back_get_error() == 0
+    return {n: t.cpu().numpy() for n, t in out.items()}
+
+
+def test_batched_slices_match_the_oracle(fb):
+    import oracle
+    shape = dict(N=64, M=512, H=8, Hkv=2, D=128, Dv=128, k_type="q8_0", v_type="q8_0", causal=True)
+    problems = [synth.make_problem(f"b{b}", seed=6100 + b, **shape) for b in range(3)]
+    got = run_batched(fb, problems, False)
+    for b, p in enumerate(problems):
+        ref = oracle.fa_back(p)
+        print(b, check_components({n: got[n][b] for n in got}, ref))
+
+
+def test_batched_per_batch_mask_equals_separate_calls(fb):
+    shape = dict(N=40, M=333, H=4, Hkv=2, D=128, Dv=128, k_type="q4_0", v_type="q8_0", mask="random", mask_p=0.1,
+                 full_rows=2, mask_heads=4)
+    problems = [synth.make_problem(f"bm{b}", seed=6200 + b, **shape) for b in range(2)]
+    got = run_batched(fb, problems, True)
+    for b, p in enumerate(problems):
+        one = run_gpu(fb, p)
+        for n in one:
+            assert np.array_equal(got[n][b], one[n], equal_nan=True), (b, n)
