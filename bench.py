@@ -188,13 +188,31 @@ def read_traffic(p) -> dict:
 
 
 def init_dist():
+    """(dist, rank, world size) under torchrun, else (None, 0, 1).  NCCL where the GPUs are
+    visible; gloo on host cores only (the reference arm on a machine without GPUs)."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws > 1:
+        import torch
         import torch.distributed as dist
-        backend = "nccl"
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
         dist.init_process_group(backend=backend)
         return dist, dist.get_rank(), ws
     return None, 0, 1
+
+
+def max_over_ranks(dist, values, device=None):
+    """Each value's maximum over all ranks (the slowest rank's time); unchanged for one process."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    x = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(x, op=dist.ReduceOp.MAX)
+    return [float(v) for v in x.tolist()]
+
+
+def job_tflops(world: int, flops_per_replica: float, ms: float) -> float:
+    """Whole-job rate: every replica's work over the slowest rank's time per step."""
+    return world * flops_per_replica / (ms * 1e-3) / 1e12
 
 
 def run_reference(args):
@@ -285,11 +303,7 @@ def run_ours(args):
         clk.mark_end()
     fb.fa_back_profile(False)
     kern = fb.fa_back_profile_read()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if dist is not None:
-        x = torch.tensor([ms], device=dev)
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        ms = float(x.item())
+    ms, = max_over_ranks(dist, [ev0.elapsed_time(ev1) / args.steps], dev)
     clocks = clk.summary()
     launches = sum(c for _, c in kern.values())
 
@@ -316,10 +330,11 @@ def run_ours(args):
                                      M=p.M, scale=p.scale, causal=p.causal, mask=t["mask"],
                                      mask_heads=p.mask_heads, workspace=ws, stream=stream), n_var)
     assert fb.fa_back_get_error() == 0
+    ws_ms, fw_ms = max_over_ranks(dist, [ws_ms, fw_ms], dev)
     variants = {
-        "fa_back_with_stats": {"ms": ws_ms, "TFLOP/s": world * p.flops() / (ws_ms * 1e-3) / 1e12,
+        "fa_back_with_stats": {"ms": ws_ms, "TFLOP/s": job_tflops(world, p.flops(), ws_ms),
                                "note": "lse and delta given; the LSE/D pass is skipped; same F_alg"},
-        "fa_forward": {"ms": fw_ms, "TFLOP/s": 4.0 * p.D * p.H * p.visible_pairs() / (fw_ms * 1e-3) / 1e12,
+        "fa_forward": {"ms": fw_ms, "TFLOP/s": job_tflops(world, 4.0 * p.D * p.H * p.visible_pairs(), fw_ms),
                        "note": "O and lse; TFLOP/s of its two contractions (S, P V)"},
     }
 
@@ -374,14 +389,11 @@ def run_ours(args):
     e2e_ms = min(run_e2e(True), run_e2e(True))
     rc = fb.fa_back_get_error()
     assert rc == 0, fb.fa_back_status_string(rc)
-    if dist is not None:
-        x = torch.tensor([e2e_ms, e2e_serial_ms], device=dev)
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        e2e_ms, e2e_serial_ms = float(x[0].item()), float(x[1].item())
+    e2e_ms, e2e_serial_ms = max_over_ranks(dist, [e2e_ms, e2e_serial_ms], dev)
 
     flops = p.flops()
-    tflops = world * flops / (ms * 1e-3) / 1e12
-    e2e_tflops = world * flops / (e2e_ms * 1e-3) / 1e12
+    tflops = job_tflops(world, flops, ms)
+    e2e_tflops = job_tflops(world, flops, e2e_ms)
     pk, pk_src = peaks()
     # binary16 runs at the bf16 rate; the kernels are timed inside a long step, so the sustained
     # figure is the denominator (the burst one is reported beside it)
@@ -410,7 +422,7 @@ def run_ours(args):
             "e2e": {"value": e2e_tflops, "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
                     "pipelining": "input copy, backward and result copy on three streams, double-buffered",
-                    "serial": {"value": world * flops / (e2e_serial_ms * 1e-3) / 1e12, "ms_per_step": e2e_serial_ms}}}
+                    "serial": {"value": job_tflops(world, flops, e2e_serial_ms), "ms_per_step": e2e_serial_ms}}}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(p)
     if rank == 0:
