@@ -258,3 +258,16 @@ def test_batched_per_batch_mask_equals_separate_calls(fb):
         one = run_gpu(fb, p)
         for n in one:
             assert np.array_equal(got[n][b], one[n], equal_nan=True), (b, n)
+
+
+def test_golden_worked_example(fb):
+    """The CUDA path against the hand-worked example under tests/golden/ (GQA, causal tail, an
+    additive and a -inf mask entry, a row without keys, a single-key row), embedded in D = Dv = 64
+    with zero components after the worked ones."""
+    import golden_io
+    fix = golden_io.load("gqa_causal_mask_worked_example.txt")
+    p = golden_io.worked_problem(fix, 64)
+    want = golden_io.worked_expected(fix, 64)
+    got = run_gpu(fb, p)
+    print(check_components(got, want))
+    assert np.all(got["dQ"][~np.isfinite(want["lse"])] == 0.0)
