@@ -12,7 +12,16 @@ STATUS = {0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_TYPE", 3: "FA_ERR_SHAPE", 4: 
           5: "FA_ERR_UNSUPPORTED", 6: "FA_ERR_DEVICE", 7: "FA_ERR_CUDA", 8: "FA_ERR_TIMEOUT",
           9: "FA_ERR_WORKSPACE"}
 
+FA_MASK_F16, FA_MASK_BITS = 0, 1
+
 _lib = None
+
+
+class fa_strides(ctypes.Structure):
+    """struct fa_strides of the header: element strides of Q and dO, byte strides of the K and V
+    rows, word strides of the mask."""
+    _fields_ = [(n, ctypes.c_int64) for n in ("q_row", "q_head", "q_comp", "do_row", "do_head", "do_comp",
+                                             "k_cell", "k_head", "v_cell", "v_head", "mask_head", "mask_row")]
 
 
 class NativeLibraryMissing(RuntimeError):
@@ -45,6 +54,11 @@ def lib():
     L.fa_back_batched.restype = i
     L.fa_back_batched.argtypes = [i, vp, vp, i, vp, i, vp, i, i, vp, f, i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp,
                                   sz, vp]
+    L.fa_back_strided_workspace_size.restype = sz
+    L.fa_back_strided_workspace_size.argtypes = [i] * 9
+    L.fa_back_strided.restype = i
+    L.fa_back_strided.argtypes = [vp, vp, i, vp, i, vp, i, i, vp, ctypes.POINTER(fa_strides), f, i, i, i, i, i, i, i,
+                                  vp, vp, vp, vp, vp, vp, sz, vp]
     L.fa_forward_workspace_size.restype = sz
     L.fa_forward_workspace_size.argtypes = [i] * 6
     L.fa_forward.restype = i
@@ -96,6 +110,20 @@ def fa_back_batched(B, q, k, k_type, v, v_type, mask, mask_heads, mask_per_batch
     return int(lib().fa_back_batched(B, q, k, k_type, v, v_type, mask, mask_heads, int(mask_per_batch), dO,
                                      float(scale), N, M, H, Hkv, D, Dv, int(causal), dQ, dK, dV, lse, delta,
                                      workspace, workspace_bytes, stream))
+
+
+def fa_back_strided_workspace_size(N: int, M: int, H: int, Hkv: int, D: int, Dv: int, k_type: int, v_type: int,
+                                   mask_heads: int) -> int:
+    return int(lib().fa_back_strided_workspace_size(N, M, H, Hkv, D, Dv, k_type, v_type, mask_heads))
+
+
+def fa_back_strided(q, k, k_type, v, v_type, mask, mask_format, mask_heads, dO, strides, scale, N, M, H, Hkv, D, Dv,
+                    causal, dQ, dK, dV, lse, delta, workspace, workspace_bytes, stream) -> int:
+    """strides: an fa_strides, or None for a NULL pointer."""
+    st = None if strides is None else ctypes.byref(strides)
+    return int(lib().fa_back_strided(q, k, k_type, v, v_type, mask, mask_format, mask_heads, dO, st, float(scale), N,
+                                     M, H, Hkv, D, Dv, int(causal), dQ, dK, dV, lse, delta, workspace,
+                                     workspace_bytes, stream))
 
 
 def fa_forward_workspace_size(N: int, M: int, H: int, Hkv: int, D: int, Dv: int) -> int:

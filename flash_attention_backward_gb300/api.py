@@ -102,3 +102,54 @@ def forward(q: torch.Tensor, k: torch.Tensor, k_type: int, v: torch.Tensor, v_ty
                         Dv, causal, _ptr(out["O"]), _ptr(out["lse"]), ws.data_ptr(), ws.numel(), s.cuda_stream)
     _check(rc)
     return out
+
+
+def backward_strided(q: torch.Tensor, k: torch.Tensor, k_type: int, v: torch.Tensor, v_type: int, dO: torch.Tensor,
+                     *, H: int, Hkv: int, D: int, Dv: int, M: int, scale: float, causal: bool = False,
+                     mask: Optional[torch.Tensor] = None, mask_heads: int = 0, mask_bits: bool = False,
+                     out: Optional[dict] = None, workspace: Optional[Workspace] = None,
+                     stream: Optional[torch.cuda.Stream] = None, workspace_bytes: Optional[int] = None) -> dict:
+    """fa_back_strided on device tensors that may be views.
+
+    q [N][H][D] and dO [N][H][Dv] f32 with any non-negative strides; k, v uint8 [M][Hkv][row] with
+    each row contiguous (last stride 1, the other two even); mask [Hm][N][M] binary16 bits
+    (int16/uint16/float16) with the keys contiguous, or, with mask_bits, int32 words
+    [Hm][N][ceil(M/32)] whose bit j % 32 of word j / 32 is set where key j is allowed.  The
+    outputs are contiguous, as for backward().
+    """
+    N = q.shape[0]
+    dev = q.device
+    if out is None:
+        out = {
+            "dQ": torch.empty((N, H, D), dtype=torch.float32, device=dev),
+            "dK": torch.empty((M, Hkv, D), dtype=torch.float32, device=dev),
+            "dV": torch.empty((M, Hkv, Dv), dtype=torch.float32, device=dev),
+            "lse": torch.empty((N, H), dtype=torch.float32, device=dev),
+            "delta": torch.empty((N, H), dtype=torch.float32, device=dev),
+        }
+    for t in out.values():
+        if not t.is_contiguous():
+            raise FaBackError("outputs must be contiguous")
+    for name, t in (("k", k), ("v", v)):
+        if t.dim() != 3 or t.stride(2) != 1 or t.element_size() != 1:
+            raise FaBackError(f"{name}: uint8 [M][Hkv][row] with contiguous rows expected")
+    if mask is not None and (mask.dim() != 3 or mask.stride(2) != 1):
+        raise FaBackError("mask: [Hm][N][keys or words] with the last dimension contiguous expected")
+    for name, t in (("q", q), ("dO", dO)):
+        if t.dim() != 3:
+            raise FaBackError(f"{name}: [N][H][D] expected")
+    st = nat.fa_strides(q_row=q.stride(0), q_head=q.stride(1), q_comp=q.stride(2),
+                        do_row=dO.stride(0), do_head=dO.stride(1), do_comp=dO.stride(2),
+                        k_cell=k.stride(0), k_head=k.stride(1), v_cell=v.stride(0), v_head=v.stride(1),
+                        mask_head=0 if mask is None else mask.stride(0), mask_row=0 if mask is None else mask.stride(1))
+    Hm = mask_heads if mask is not None else 0
+    need = nat.fa_back_strided_workspace_size(N, M, H, Hkv, D, Dv, k_type, v_type, Hm)
+    ws_bytes = need if workspace_bytes is None else int(workspace_bytes)
+    ws = (workspace or Workspace(dev)).get(ws_bytes)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    fmt = nat.FA_MASK_BITS if mask_bits else nat.FA_MASK_F16
+    rc = nat.fa_back_strided(_ptr(q), _ptr(k), k_type, _ptr(v), v_type, _ptr(mask), fmt, mask_heads, _ptr(dO), st,
+                             scale, N, M, H, Hkv, D, Dv, causal, _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]),
+                             _ptr(out["lse"]), _ptr(out["delta"]), ws.data_ptr(), ws_bytes, s.cuda_stream)
+    _check(rc)
+    return out

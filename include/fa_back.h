@@ -147,6 +147,61 @@ fa_status fa_back_batched(int B, const float* q, const void* k, int k_type, cons
                           float* dK, float* dV, float* lse, float* delta, void* workspace,
                           size_t workspace_bytes, void* stream);
 
+/*
+ * Input strides for fa_back_strided().  The operator keeps its outer strides and its q / dO
+ * component strides ("CUDA: FLASH_ATTN_BACK kernels", CambrianTech/llama.cpp pull request 63,
+ * PR description), so each input may be a view:
+ *   Q  element (i, h, c) at q[i*q_row + h*q_head + c*q_comp]       (f32 elements)
+ *   dO element (i, h, c) at dO[i*do_row + h*do_head + c*do_comp]   (f32 elements)
+ *   K  row (j, hk) starts at (const char*)k + j*k_cell + hk*k_head  (bytes; a row's fa_row_bytes
+ *      bytes are contiguous, since a block is the format's unit; v likewise with v_cell, v_head)
+ *   mask element (j, i, hm) at word hm*mask_head + i*mask_row + j    (FA_MASK_F16: binary16 words)
+ *      or bit j % 32 of word hm*mask_head + i*mask_row + j / 32      (FA_MASK_BITS: 32-bit words)
+ * Every stride is >= 0 (0 repeats one element, a broadcast view); the K and V byte strides are
+ * even.  The contiguous layouts of fa_back() are q_row = H*D, q_head = D, q_comp = 1,
+ * k_cell = Hkv*fa_row_bytes(k_type, D), k_head = fa_row_bytes(k_type, D), mask_head = N*M (F16)
+ * and mask_row = M.
+ */
+typedef struct fa_strides {
+  int64_t q_row, q_head, q_comp;
+  int64_t do_row, do_head, do_comp;
+  int64_t k_cell, k_head;
+  int64_t v_cell, v_head;
+  int64_t mask_head, mask_row;
+} fa_strides;
+
+/* Mask formats of fa_back_strided().  FA_MASK_F16: binary16 additive values, as for fa_back().
+ * FA_MASK_BITS: one bit per (query, key), set = the key is allowed (adds +0), clear = masked
+ * (-inf); the mask the raw-cache forward of torad-labs/llama.cpp pull request 71 reads is
+ * bit-packed, and this is the plainest reading of one, since that page gives no bit order. */
+#define FA_MASK_F16 0
+#define FA_MASK_BITS 1
+
+/* Workspace bytes of fa_back_strided() with fa_back()'s fastest plan: contiguous copies of Q, dO,
+ * K, V and (mask_heads > 0) a binary16 mask, each rounded up to 256 bytes, followed by
+ * fa_back_workspace_size().  0 for invalid arguments. */
+size_t fa_back_strided_workspace_size(int N, int M, int H, int Hkv, int D, int Dv, int k_type, int v_type,
+                                      int mask_heads);
+
+/*
+ * fa_back() on inputs given as views (strides in *strides) and with a binary16 or bit-packed
+ * mask (mask_format).  Each input is copied once, on `stream`, into a contiguous region at the
+ * front of the workspace (the mask's bits widened to binary16 0 / -inf), then fa_back() runs on
+ * those regions with the rest of the workspace, so its plan, results and determinism are those
+ * of fa_back() given workspace_bytes minus the copies.  The outputs are contiguous, laid out as
+ * for fa_back().  Pointers: q, dO 4-byte aligned; k, v 2-byte aligned; the mask 2-byte
+ * (FA_MASK_F16) or 4-byte (FA_MASK_BITS) aligned; outputs 16-byte aligned; workspace 256-byte
+ * aligned.  Errors as for fa_back(), plus: strides NULL is FA_ERR_NULL; a negative stride or an
+ * unknown mask_format is FA_ERR_SHAPE; an odd K/V byte stride is FA_ERR_ALIGN; a workspace
+ * smaller than the copies plus fa_back_workspace_size_min() is FA_ERR_WORKSPACE.  Every element a
+ * view addresses must lie inside memory the caller owns; the library cannot check that.
+ */
+fa_status fa_back_strided(const float* q, const void* k, int k_type, const void* v, int v_type,
+                          const void* mask, int mask_format, int mask_heads, const float* dO,
+                          const fa_strides* strides, float scale, int N, int M, int H, int Hkv, int D,
+                          int Dv, int causal, float* dQ, float* dK, float* dV, float* lse, float* delta,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
 /* Sticky device-side status of the kernels enqueued so far on the current device
  * (FA_OK or FA_ERR_TIMEOUT).  Synchronises the device, then clears the word. */
 fa_status fa_back_get_error(void);

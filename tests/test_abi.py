@@ -27,7 +27,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
         ["fa_back", "fa_back_batched", "fa_back_get_error", "fa_back_noalloc", "fa_back_profile", "fa_back_profile_read",
-         "fa_back_selftest_timeout", "fa_back_status_string", "fa_back_workspace_size",
+         "fa_back_selftest_timeout", "fa_back_status_string", "fa_back_strided", "fa_back_strided_workspace_size",
+         "fa_back_workspace_size",
          "fa_back_with_stats", "fa_back_workspace_size_min", "fa_forward", "fa_forward_workspace_size",
          "fa_row_bytes"])
 
@@ -116,3 +117,52 @@ def test_batched_rejects_a_negative_batch(L):
     rc = fb.fa_back_batched(-1, 0x1000, 0x2000, 2, 0x3000, 2, None, 0, 0, 0x4000, 0.1, 8, 32, 4, 2, 128, 128, 0,
                             0x5000, 0x6000, 0x7000, 0x8000, 0x9000, 0x10000, 1 << 30, None)
     assert fb.STATUS[rc] == "FA_ERR_SHAPE"
+
+
+def _strided_call(**kw):
+    st = fb.fa_strides(q_row=4 * 128, q_head=128, q_comp=1, do_row=4 * 128, do_head=128, do_comp=1, k_cell=2 * 136,
+                       k_head=136, v_cell=2 * 136, v_head=136, mask_head=8 * 32, mask_row=32)
+    for f in [f for f in kw if f in dict(fb.fa_strides._fields_)]:
+        setattr(st, f, kw.pop(f))
+    a = dict(q=0x1000, k=0x2000, k_type=2, v=0x3000, v_type=2, mask=None, mask_format=0, mask_heads=0, dO=0x4000,
+             strides=st, scale=0.1, N=8, M=32, H=4, Hkv=2, D=128, Dv=128, causal=0, dQ=0x5000, dK=0x6000, dV=0x7000,
+             lse=0x8000, delta=0x9000, workspace=0x10000, workspace_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return fb.STATUS[fb.fa_back_strided(**a)]
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(strides=None), "FA_ERR_NULL"),
+    (dict(q_comp=-1), "FA_ERR_SHAPE"),
+    (dict(k_head=-2), "FA_ERR_SHAPE"),
+    (dict(mask=0xA000, mask_heads=4, mask_format=2), "FA_ERR_SHAPE"),
+    (dict(mask=0xA000, mask_heads=3), "FA_ERR_SHAPE"),
+    (dict(k_type=7), "FA_ERR_TYPE"),
+    (dict(D=96, Dv=96), "FA_ERR_UNSUPPORTED"),
+    (dict(dO=None), "FA_ERR_NULL"),
+    (dict(q=0x1002), "FA_ERR_ALIGN"),
+    (dict(k=0x2001), "FA_ERR_ALIGN"),
+    (dict(v_cell=273), "FA_ERR_ALIGN"),
+    (dict(mask=0xA002, mask_heads=1, mask_format=1), "FA_ERR_ALIGN"),
+    (dict(dK=0x6008), "FA_ERR_ALIGN"),
+])
+def test_strided_argument_errors_are_reported_before_any_launch(L, kw, code):
+    assert _strided_call(**kw) == code
+
+
+def test_strided_accepts_views_that_fa_back_would_reject():
+    """Unaligned and strided views pass the host checks; with no GPU here the call then stops at
+    the device query (FA_ERR_CUDA), before anything is enqueued."""
+    assert _strided_call(q=0x1004, dO=0x4008, k=0x2002, k_cell=3 * 136, q_comp=2) in ("FA_ERR_CUDA", "FA_ERR_DEVICE")
+    assert _strided_call(mask=0xA002, mask_heads=4, mask_format=0) in ("FA_ERR_CUDA", "FA_ERR_DEVICE")
+
+
+def test_strided_workspace_is_the_copies_plus_fa_backs(L):
+    for N, M, H, Hkv, D, Dv, kt, vt, hm in [(64, 512, 8, 2, 128, 128, 2, 2, 0), (2048, 75520, 24, 4, 256, 256, 2, 2, 0),
+                                            (40, 333, 4, 2, 128, 128, 3, 2, 4), (5, 1, 2, 1, 64, 64, 0, 1, 1)]:
+        inner = fb.fa_back_workspace_size(N, M, H, Hkv, D, Dv)
+        got = fb.fa_back_strided_workspace_size(N, M, H, Hkv, D, Dv, kt, vt, hm)
+        copies = (4 * N * H * (D + Dv) + M * Hkv * (fb.fa_row_bytes(kt, D) + fb.fa_row_bytes(vt, Dv))
+                  + 2 * hm * N * M)
+        assert copies <= got - inner < copies + 5 * 256
+    assert fb.fa_back_strided_workspace_size(8, 32, 4, 2, 48, 48, 2, 2, 0) == 0  # not a whole q8_0 block
