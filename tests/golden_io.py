@@ -70,11 +70,13 @@ def worked_problem(fix: dict, D_pad: int = 0):
     dO = pad(indexed(inp, "dO", (N, H), Dv), Dvp).astype(np.float32)
     k = pad(indexed(inp, "k", (M, Hkv), D), Dp).astype(np.float32)
     v = pad(indexed(inp, "v", (M, Hkv), Dv), Dvp).astype(np.float32)
-    mask = indexed(inp, "mask", (Hm, N), M).astype(np.float16).view(np.uint16)
+    mask = None
+    if Hm > 0:
+        mask = np.ascontiguousarray(indexed(inp, "mask", (Hm, N), M).astype(np.float16).view(np.uint16))
     return synth.Problem(name="golden", N=N, M=M, H=H, Hkv=Hkv, D=Dp, Dv=Dvp, k_type=synth.TYPE_F32,
                          v_type=synth.TYPE_F32, causal=bool(int(inp["causal"])), scale=value(inp["scale"]),
                          q=q, k=np.ascontiguousarray(k).view(np.uint8), v=np.ascontiguousarray(v).view(np.uint8),
-                         dO=dO, mask=np.ascontiguousarray(mask), mask_heads=Hm)
+                         dO=dO, mask=mask, mask_heads=Hm)
 
 
 def worked_expected(fix: dict, D_pad: int = 0) -> dict:

@@ -10,12 +10,13 @@ import pytest
 import golden_io
 import synth
 
-WORKED = "gqa_causal_mask_worked_example.txt"
+WORKED_EXAMPLES = ["gqa_causal_mask_worked_example.txt", "gqa_two_kv_heads_worked_example.txt"]
 
 
 @pytest.mark.parametrize("D_pad", [0, 64])
-def test_worked_example_backward(oracle_lib, D_pad):
-    fix = golden_io.load(WORKED)
+@pytest.mark.parametrize("name", WORKED_EXAMPLES)
+def test_worked_example_backward(oracle_lib, name, D_pad):
+    fix = golden_io.load(name)
     p = golden_io.worked_problem(fix, D_pad)
     want = golden_io.worked_expected(fix, D_pad)
     got = oracle_lib.fa_back(p)
@@ -26,12 +27,14 @@ def test_worked_example_backward(oracle_lib, D_pad):
     assert np.allclose(got["lse"][live], want["lse"][live], rtol=0, atol=1e-7)
     for n in ("delta", "dQ", "dK", "dV"):
         assert np.allclose(got[n], want[n], rtol=0, atol=1e-7), (n, got[n], want[n])
-    # the fully masked row and the single-key row give exact zeros
-    assert np.all(got["dQ"][0] == 0.0) and got["delta"][0, 1] == 0.0
+    # a fully masked row gives exact zeros
+    dead = ~live
+    assert np.all(got["dQ"][dead] == 0.0) and np.all(got["delta"][dead] == 0.0)
 
 
-def test_worked_example_forward(oracle_lib):
-    fix = golden_io.load(WORKED)
+@pytest.mark.parametrize("name", WORKED_EXAMPLES)
+def test_worked_example_forward(oracle_lib, name):
+    fix = golden_io.load(name)
     p = golden_io.worked_problem(fix)
     want = golden_io.worked_expected(fix)
     got = oracle_lib.fa_forward(p)
@@ -39,20 +42,25 @@ def test_worked_example_forward(oracle_lib):
     live = np.isfinite(want["lse"])
     assert np.allclose(got["lse"][live], want["lse"][live], rtol=0, atol=1e-7)
     assert np.allclose(got["O"], want["O"], rtol=0, atol=1e-7)
-    assert np.all(got["O"][0, 1] == 0.0)
+    assert np.all(got["O"][~live] == 0.0)
 
 
-def test_worked_example_is_self_consistent():
-    """The fixture's own sums: delta = dO.O per live row, sum_j dK_j = 0, sum_j dV_j = the live
-    rows' dO summed (the working in the fixture, checked as arithmetic)."""
-    fix = golden_io.load(WORKED)
+@pytest.mark.parametrize("name", WORKED_EXAMPLES)
+def test_worked_example_is_self_consistent(name):
+    """The fixture's own sums: delta = dO.O per live row, sum_j dK_j = 0 and sum_j dV_j = the
+    live rows' dO summed over each KV head's group (the working in the fixture, checked as
+    arithmetic)."""
+    fix = golden_io.load(name)
     p = golden_io.worked_problem(fix)
     want = golden_io.worked_expected(fix)
     live = np.isfinite(want["lse"])
     dO = p.dO.astype(np.float64)
     assert np.allclose(np.sum(dO * want["O"], axis=-1)[live], want["delta"][live], atol=1e-12)
     assert np.allclose(want["dK"].sum(axis=0), 0.0, atol=1e-12)
-    assert np.allclose(want["dV"].sum(axis=0)[0], dO[live].sum(axis=0), atol=1e-12)
+    for hk in range(p.Hkv):
+        heads = slice(hk * p.G, (hk + 1) * p.G)
+        live_dO = dO[:, heads][live[:, heads]]
+        assert np.allclose(want["dV"].sum(axis=0)[hk], live_dO.sum(axis=0), atol=1e-12)
 
 
 @pytest.mark.parametrize("block,t", [("q8_0 ramp", synth.TYPE_Q8_0),

@@ -260,12 +260,13 @@ def test_batched_per_batch_mask_equals_separate_calls(fb):
             assert np.array_equal(got[n][b], one[n], equal_nan=True), (b, n)
 
 
-def test_golden_worked_example(fb):
-    """The CUDA path against the hand-worked example under tests/golden/ (GQA, causal tail, an
-    additive and a -inf mask entry, a row without keys, a single-key row), embedded in D = Dv = 64
-    with zero components after the worked ones."""
+@pytest.mark.parametrize("name", ["gqa_causal_mask_worked_example.txt", "gqa_two_kv_heads_worked_example.txt"])
+def test_golden_worked_example(fb, name):
+    """The CUDA path against the hand-worked examples under tests/golden/ (GQA with one and with
+    two KV heads, the causal tail, an additive and a -inf mask entry, a row without keys, a
+    single-key row), embedded in D = Dv = 64 with zero components after the worked ones."""
     import golden_io
-    fix = golden_io.load("gqa_causal_mask_worked_example.txt")
+    fix = golden_io.load(name)
     p = golden_io.worked_problem(fix, 64)
     want = golden_io.worked_expected(fix, 64)
     got = run_gpu(fb, p)

@@ -64,24 +64,22 @@ def test_planted_mistake_is_caught(problem, tmp_path, name):
     assert max(errs.values()) > 1e-6, (name, errs)
 
 
-# the hand-worked fixtures alone (tests/golden/) catch these; the GQA index mistake needs more
-# than one KV head, which the worked example does not have (the autograd pin above catches it)
-GOLDEN_CATCHES = sorted(set(MUTATIONS) - {"gqa_index_in_dq"})
-
-
-@pytest.mark.parametrize("name", GOLDEN_CATCHES)
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_planted_mistake_fails_the_golden_fixtures(tmp_path, name):
+    """The hand-worked fixtures under tests/golden/ alone reject every planted mistake."""
     import golden_io
     old, new = MUTATIONS[name]
     src = tmp_path / f"mut_{name}.c"
     src.write_text(open(SRC).read().replace(old, new))
     lib = orc.load(orc.compile_source(str(src), str(tmp_path / f"lib_{name}.so")))
-    fix = golden_io.load("gqa_causal_mask_worked_example.txt")
-    got = orc.fa_back(golden_io.worked_problem(fix), lib=lib)
-    want = golden_io.worked_expected(fix)
-    worst = max(float(np.max(np.abs(np.nan_to_num(got[k], nan=1e30, posinf=1e30, neginf=-1e30)
-                                    - np.nan_to_num(want[k], nan=1e30, posinf=1e30, neginf=-1e30))))
-                for k in ("lse", "delta", "dQ", "dK", "dV"))
+    worst = 0.0
+    for example in ("gqa_causal_mask_worked_example.txt", "gqa_two_kv_heads_worked_example.txt"):
+        fix = golden_io.load(example)
+        got = orc.fa_back(golden_io.worked_problem(fix), lib=lib)
+        want = golden_io.worked_expected(fix)
+        worst = max([worst] + [float(np.max(np.abs(np.nan_to_num(got[k], nan=1e30, posinf=1e30, neginf=-1e30)
+                                                   - np.nan_to_num(want[k], nan=1e30, posinf=1e30, neginf=-1e30))))
+                               for k in ("lse", "delta", "dQ", "dK", "dV")])
     blocks = golden_io.load("cache_blocks.txt")
     for block, t in (("q8_0 ramp", synth.TYPE_Q8_0), ("q4_0 nibble order", synth.TYPE_Q4_0)):
         raw = np.array([int(x, 16) for x in blocks[block]["bytes"].split()], dtype=np.uint8)
