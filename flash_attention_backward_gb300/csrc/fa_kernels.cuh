@@ -710,6 +710,8 @@ enum {
   B_ACC_FULL,
   B_Q_FULL,
   B_OPS_READY,
+  B_DRAIN0,  // the producer's dQ products, committed after an abort
+  B_DRAIN1,  // the issuer's S/dP products, committed after an abort
   B_COUNT
 };
 static_assert(8 * B_COUNT + 8 <= 512, "barrier area");
@@ -726,6 +728,26 @@ struct Waiter {
     return false;
   }
 };
+
+// ---- leaving after an abort.  A CTA that gave up on a wait still has to let its own
+// asynchronous work finish before it frees tensor memory and exits: loads still landing in its
+// shared memory, products still reading it.  These waits stop at a deadline too.
+
+// Waits for the phase of `bar` with the given parity until the global timer passes `deadline`.
+__device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, uint64_t deadline) {
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 255u && globaltimer_ns() > deadline) return false;
+  }
+}
+
+// The last loads of a ring of `nst` stages whose full barriers start at `full`, after `issued`
+// loads (load n fills stage n % nst and completes phase n / nst of its barrier).  An earlier load
+// of a stage has landed: the stage was consumed, and released, before it was refilled.
+__device__ __forceinline__ void drain_loads(uint64_t* full, int nst, int issued, uint64_t deadline) {
+  for (int n = issued > nst ? issued - nst : 0; n < issued; ++n)
+    mbar_wait_until(&full[n % nst], (uint32_t)(n / nst) & 1u, deadline);
+}
 
 template <int D, int Dv, int BK, int MODE>
 __global__ void __launch_bounds__(Rows2Cfg<D, Dv, BK, MODE>::NT, 1)
@@ -782,6 +804,8 @@ __global__ void __launch_bounds__(Rows2Cfg<D, Dv, BK, MODE>::NT, 1)
     mbar_init(&bar[B_ACC_FULL], 1);
     mbar_init(&bar[B_Q_FULL], 1);
     mbar_init(&bar[B_OPS_READY], C::NSOFT);
+    mbar_init(&bar[B_DRAIN0], 1);
+    mbar_init(&bar[B_DRAIN1], 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -791,6 +815,8 @@ __global__ void __launch_bounds__(Rows2Cfg<D, Dv, BK, MODE>::NT, 1)
   const uint32_t tbase = *tslot;
   const Waiter wait{s_abort, p.err};
   const Stats st = *p.st;
+  int n_kraw = 0, n_vraw = 0, n_dq = 0;  // producer: raw entries loaded, dQ products issued
+  bool s_issued = false;                 // issuer: any S product issued
   // dQ += dS(t) K'(t) (dQ pass; issued by the producer thread, beside the S/dP stream of warp 1)
   auto issue_dq = [&](int t) {
     if constexpr (MODE != 1) return;  // only the dQ pass has the accumulator and the dS panel
@@ -899,6 +925,7 @@ __global__ void __launch_bounds__(Rows2Cfg<D, Dv, BK, MODE>::NT, 1)
         __nanosleep(64);
       }
     }
+    n_kraw = ek, n_vraw = ev, n_dq = nd;
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0 && ntiles > 0) {
@@ -908,6 +935,7 @@ __global__ void __launch_bounds__(Rows2Cfg<D, Dv, BK, MODE>::NT, 1)
       // S(t) = Q K'^T into the tensor-memory slot of tile t
       auto issue_s = [&](int t) {
         const uint32_t tS = tbase + C::T_S + 2 * BK * (t % C::NSLOT);
+        s_issued = true;
         tc_fence_after();
         const uint64_t db = sdesc_sw128(smem_u32(sK + (t % C::KSTAGES) * C::KB), 16, 1024);
         const uint64_t da = sdesc_sw128(smem_u32(sQ), 16, 1024);
@@ -1183,6 +1211,23 @@ __global__ void __launch_bounds__(Rows2Cfg<D, Dv, BK, MODE>::NT, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (*s_abort) {  // the same value in every thread: nothing writes it after the barrier
+    const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
+    if (warp == 0 && lane == 0) {
+      drain_loads(&bar[B_KRAW_FULL], RK, n_kraw, deadline);
+      drain_loads(&bar[B_VRAW_FULL], RV, n_vraw, deadline);
+      if (MODE == 1 && ntiles > 0) mbar_wait_until(&bar[B_Q_FULL], 0, deadline);
+      if (n_dq > 0) {
+        mma_commit(&bar[B_DRAIN0]);
+        mbar_wait_until(&bar[B_DRAIN0], 0, deadline);
+      }
+    }
+    if (warp == 1 && lane == 0 && s_issued) {
+      mma_commit(&bar[B_DRAIN1]);
+      mbar_wait_until(&bar[B_DRAIN1], 0, deadline);
+    }
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, C::TCOLS);
@@ -1267,6 +1312,8 @@ enum {
   R3_ACC_FULL,
   R3_Q_FULL,
   R3_OPS_READY,
+  R3_DRAIN0,  // the producer's dQ / O products, committed after an abort
+  R3_DRAIN1,  // the issuer's S/dP products, committed after an abort
   R3_COUNT
 };
 static_assert(8 * R3_COUNT + 8 <= 512, "barrier area");
@@ -1318,6 +1365,8 @@ __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
     mbar_init(&bar[R3_ACC_FULL], 1);
     mbar_init(&bar[R3_Q_FULL], 1);
     mbar_init(&bar[R3_OPS_READY], C::NSOFT);
+    mbar_init(&bar[R3_DRAIN0], 1);
+    mbar_init(&bar[R3_DRAIN1], 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -1327,6 +1376,8 @@ __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
   const uint32_t tbase = *tslot;
   const Waiter wait{s_abort, p.err};
   const Stats st = *p.st;
+  int n_kload = 0, n_vload = 0, n_prod = 0;  // producer: K' and V' tiles loaded, products issued
+  bool s_issued = false;                     // issuer: any S product issued
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
@@ -1404,6 +1455,7 @@ __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
           }
         }
       }
+      n_kload = kt, n_vload = vt, n_prod = nd;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ S/dP issuer
@@ -1415,6 +1467,7 @@ __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
       for (int t = 0; ok && t < ntiles; ++t) {
         const int ks = t % C::KSTAGES, vs = t % C::VSTAGES;
         if (!wait(&bar[R3_K_FULL + ks], (t / C::KSTAGES) & 1) || !wait(&bar[R3_S_FREE], (t & 1) ^ 1)) break;
+        s_issued = true;
         tc_fence_after();
         const uint64_t db = sdesc_sw128(smem_u32(sK + ks * C::KB), 16, 1024);
         const uint64_t da = sdesc_sw128(smem_u32(sQ), 16, 1024);
@@ -1650,6 +1703,23 @@ __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (*s_abort) {  // the same value in every thread: nothing writes it after the barrier
+    const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
+    if (warp == 0 && lane == 0) {
+      drain_loads(&bar[R3_K_FULL], C::KSTAGES, n_kload, deadline);
+      drain_loads(&bar[R3_V_FULL], C::VSTAGES, n_vload, deadline);
+      if (C::ROWQ && ntiles > 0) mbar_wait_until(&bar[R3_Q_FULL], 0, deadline);
+      if (n_prod > 0) {
+        mma_commit(&bar[R3_DRAIN0]);
+        mbar_wait_until(&bar[R3_DRAIN0], 0, deadline);
+      }
+    }
+    if (warp == 1 && lane == 0 && s_issued) {
+      mma_commit(&bar[R3_DRAIN1]);
+      mbar_wait_until(&bar[R3_DRAIN1], 0, deadline);
+    }
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, C::TCOLS);
@@ -1855,6 +1925,7 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tbase = *tslot;
   const Waiter wait{s_abort, p.err};
+  int n_oload = 0, n_qload = 0;  // producer: dO and Q panels loaded
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
@@ -1877,11 +1948,13 @@ __global__ void __launch_bounds__(384, 1)
           if (!(ok = wait(&bar[C_O_EMPTY + c], (t & 1) ^ 1))) break;
           mbar_arrive_expect_tx(&bar[C_O_FULL + c], 128 * 128);
           tma_load_3d(sO + c * 128 * 128, &tmO, &bar[C_O_FULL + c], c * 64, r0, hk);
+          ++n_oload;
         }
         for (int c = 0; ok && c < C::NQP; ++c) {
           if (!(ok = wait(&bar[C_Q_EMPTY + c], (t & 1) ^ 1))) break;
           mbar_arrive_expect_tx(&bar[C_Q_FULL + c], 128 * 128);
           tma_load_3d(sQ + c * 128 * 128, &tmQ, &bar[C_Q_FULL + c], c * 64, r0, hk);
+          ++n_qload;
         }
         if (!ok) break;
       }
@@ -2118,6 +2191,17 @@ __global__ void __launch_bounds__(384, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (*s_abort) {  // the same value in every thread: nothing writes it after the barrier
+    const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
+    if (warp == 0 && lane == 0) {
+      if (nq > 0 && kv_copies) mbar_wait_until(&bar[C_KV_FULL], 0, deadline);
+      drain_loads(&bar[C_O_FULL], C::NOP, n_oload, deadline);
+      drain_loads(&bar[C_Q_FULL], C::NQP, n_qload, deadline);
+    }
+    // the issuer committed every product it issued to C_DONE before leaving its loop
+    if (warp == 1 && lane == 0 && nq > 0) mbar_wait_until(&bar[C_DONE], 0, deadline);
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, C::TCOLS);
@@ -2199,6 +2283,7 @@ __global__ void __launch_bounds__(256, 1)
   tc_fence_after();
   const uint32_t tbase = *tslot;
   const Waiter wait{s_abort, p.err};
+  int n_load = 0;  // producer: stages loaded
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
@@ -2218,6 +2303,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(b + c * (BK * 128), &tmK, &bar[G_FULL + s], 0, j0, hk * (D / 64) + c);
+        ++n_load;
       }
     }
   } else if (warp == 1) {
@@ -2273,6 +2359,13 @@ __global__ void __launch_bounds__(256, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (*s_abort) {  // the same value in every thread: nothing writes it after the barrier
+    const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
+    if (warp == 0 && lane == 0) drain_loads(&bar[G_FULL], C::NST, n_load, deadline);
+    // the issuer committed every product it issued to G_ACC before leaving its loop
+    if (warp == 1 && lane == 0 && ntiles > 0) mbar_wait_until(&bar[G_ACC], 0, deadline);
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, C::TCOLS);

@@ -37,7 +37,8 @@
  * Errors: argument errors are reported before anything is enqueued and leave the outputs
  * untouched.  A launch failure returns FA_ERR_CUDA.  A kernel that gives up on a bounded wait
  * records FA_ERR_TIMEOUT in a device word that fa_back_get_error() reads after the caller has
- * synchronised.
+ * synchronised; before it exits it waits (again bounded) for its own loads and tensor-core
+ * products still in flight and frees its tensor memory, so the context stays usable.
  *
  * Determinism: every output element has exactly one writer and every sum runs in a fixed
  * order, so repeated calls with the same inputs give bit-identical outputs.
