@@ -166,3 +166,26 @@ def test_strided_workspace_is_the_copies_plus_fa_backs(L):
                   + 2 * hm * N * M)
         assert copies <= got - inner < copies + 5 * 256
     assert fb.fa_back_strided_workspace_size(8, 32, 4, 2, 48, 48, 2, 2, 0) == 0  # not a whole q8_0 block
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    """No CPU fallback: without libfa_back.so every entry point raises NativeLibraryMissing."""
+    from flash_attention_backward_gb300 import _native
+    monkeypatch.setattr(_native, "LIB_PATH", str(tmp_path / "libfa_back.so"))
+    monkeypatch.setattr(_native, "_lib", None)
+    with pytest.raises(_native.NativeLibraryMissing):
+        _native.fa_back_workspace_size(8, 32, 4, 2, 128, 128)
+    with pytest.raises(_native.NativeLibraryMissing):
+        _native.fa_back(0x1000, 0x2000, 2, 0x3000, 2, None, 0, 0x4000, 0.1, 8, 32, 4, 2, 128, 128, 0, 0x5000,
+                        0x6000, 0x7000, 0x8000, 0x9000, 0x10000, 1 << 30, None)
+
+
+def test_product_path_imports_nothing_from_the_oracle():
+    """The package and its sources never name the oracle: the CPU oracle is test infrastructure."""
+    pkg = os.path.join(ROOT, "flash_attention_backward_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "fa_oracle" not in text and "liboracle" not in text, f
