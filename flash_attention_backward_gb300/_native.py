@@ -46,6 +46,8 @@ def lib():
     L.fa_back_workspace_size.argtypes = [i] * 6
     L.fa_back_workspace_size_min.restype = sz
     L.fa_back_workspace_size_min.argtypes = [i] * 6
+    L.fa_back_plan_info.restype = i
+    L.fa_back_plan_info.argtypes = [i] * 6 + [sz, vp, vp, vp]
     L.fa_back.restype = i
     L.fa_back.argtypes = [vp, vp, i, vp, i, vp, i, vp, f, i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, sz, vp]
     L.fa_back_with_stats.restype = i
@@ -89,6 +91,14 @@ def fa_back_workspace_size(N: int, M: int, H: int, Hkv: int, D: int, Dv: int) ->
 
 def fa_back_workspace_size_min(N: int, M: int, H: int, Hkv: int, D: int, Dv: int) -> int:
     return int(lib().fa_back_workspace_size_min(N, M, H, Hkv, D, Dv))
+
+
+def fa_back_plan_info(N: int, M: int, H: int, Hkv: int, D: int, Dv: int, workspace_bytes: int):
+    """(status, level, key_splits, plan_bytes) of the plan fa_back runs with this workspace."""
+    level, splits, nbytes = ctypes.c_int(-1), ctypes.c_int(0), ctypes.c_size_t(0)
+    rc = int(lib().fa_back_plan_info(N, M, H, Hkv, D, Dv, workspace_bytes, ctypes.byref(level), ctypes.byref(splits),
+                                     ctypes.byref(nbytes)))
+    return rc, level.value, splits.value, nbytes.value
 
 
 def fa_back(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal,

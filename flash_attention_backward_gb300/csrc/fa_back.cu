@@ -486,6 +486,20 @@ extern "C" size_t fa_back_workspace_size_min(int N, int M, int H, int Hkv, int D
   return fab_workspace_size_capped(N, M, H, Hkv, D, Dv, 0);
 }
 
+extern "C" fa_status fa_back_plan_info(int N, int M, int H, int Hkv, int D, int Dv, size_t workspace_bytes,
+                                       int* level, int* key_splits, size_t* plan_bytes) {
+  if (N < 0 || M < 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || Hkv > 256) return FA_ERR_SHAPE;
+  if (!pick(D, Dv)) return FA_ERR_UNSUPPORTED;
+  int nsm = device_sms(nullptr, nullptr);
+  if (nsm <= 0) nsm = 152;  // no device: the GB300's SM count
+  const Plan P = make_plan(N, M, H, Hkv, D, Dv, nsm, workspace_bytes);
+  if (workspace_bytes < P.total) return FA_ERR_WORKSPACE;
+  if (level) *level = P.dsq ? 2 : P.pre ? 1 : 0;
+  if (key_splits) *key_splits = P.nsplit;
+  if (plan_bytes) *plan_bytes = P.total;
+  return FA_OK;
+}
+
 extern "C" fa_status fa_back(const float* q, const void* k, int k_type, const void* v, int v_type,
                              const uint16_t* mask, int mask_heads, const float* dO, float scale, int N, int M,
                              int H, int Hkv, int D, int Dv, int causal, float* dQ, float* dK, float* dV,

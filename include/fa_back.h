@@ -93,6 +93,15 @@ size_t fa_back_workspace_size(int N, int M, int H, int Hkv, int D, int Dv);
  * workspace_bytes, so equal calls give bit-identical outputs. */
 size_t fa_back_workspace_size_min(int N, int M, int H, int Hkv, int D, int Dv);
 
+/* The plan fa_back() runs for this shape and workspace_bytes on the current device (an SM count
+ * of 152 when no device is visible): *level 2 (binary16 K'/V' copies and the stored dS), 1 (the
+ * copies only) or 0 (raw rows decoded in the passes), the number of key splits of its row
+ * passes, and the workspace bytes it uses.  Host only: nothing is enqueued.  FA_ERR_WORKSPACE
+ * when workspace_bytes is below fa_back_workspace_size_min(); FA_ERR_SHAPE / FA_ERR_UNSUPPORTED
+ * as for fa_back().  Any output pointer may be NULL. */
+fa_status fa_back_plan_info(int N, int M, int H, int Hkv, int D, int Dv, size_t workspace_bytes, int* level,
+                            int* key_splits, size_t* plan_bytes);
+
 /*
  * The backward.  scale multiplies q.k before the mask is added (the reading used for the
  * pages' tests is scale = 1/sqrt(D)).  causal != 0 applies the causal tail j <= M - N + i.

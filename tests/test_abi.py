@@ -26,7 +26,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
-        ["fa_back", "fa_back_batched", "fa_back_get_error", "fa_back_noalloc", "fa_back_profile", "fa_back_profile_read",
+        ["fa_back", "fa_back_batched", "fa_back_get_error", "fa_back_noalloc", "fa_back_plan_info", "fa_back_profile",
+         "fa_back_profile_read",
          "fa_back_selftest_timeout", "fa_back_status_string", "fa_back_strided", "fa_back_strided_workspace_size",
          "fa_back_workspace_size",
          "fa_back_with_stats", "fa_back_workspace_size_min", "fa_forward", "fa_forward_workspace_size",
@@ -189,3 +190,39 @@ def test_product_path_imports_nothing_from_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "fa_oracle" not in text and "liboracle" not in text, f
+
+
+PLAN_SHAPES = [(2048, 75520, 24, 4, 256, 256), (64, 512, 8, 2, 128, 128), (40, 17000, 4, 2, 128, 128),
+               (5, 1, 2, 1, 64, 64), (100, 40, 4, 1, 64, 64)]
+
+
+@pytest.mark.parametrize("shape", PLAN_SHAPES)
+def test_plan_levels_follow_the_workspace(L, shape):
+    full = fb.fa_back_workspace_size(*shape)
+    small = fb.fa_back_workspace_size_min(*shape)
+    assert fb.fa_back_plan_info(*shape, full)[:2] == (0, 2) and fb.fa_back_plan_info(*shape, full)[3] == full
+    assert fb.fa_back_plan_info(*shape, small) == (0, 0, 1, small)
+    assert fb.STATUS[fb.fa_back_plan_info(*shape, small - 1)[0]] == "FA_ERR_WORKSPACE"
+    # more workspace never gives a slower plan level, and a plan never uses more than it is given
+    last = -1
+    for f in [i / 16 for i in range(17)]:
+        ws = int(small + f * (full - small))
+        rc, level, splits, used = fb.fa_back_plan_info(*shape, ws)
+        assert rc == 0 and level >= last and used <= ws and splits >= 1
+        last = level
+
+
+def test_plan_of_the_long_context_shape(L):
+    shape = (2048, 75520, 24, 4, 256, 256)
+    N, M, H, Hkv, D, Dv = shape
+    copies = 2 * Hkv * M * (D + Dv)  # binary16 K'/V'
+    ds = 2 * N * H * ((M + 63) // 64 * 64)  # binary16 dS
+    _, level, _, used = fb.fa_back_plan_info(*shape, 2 << 30)  # room for the copies, not for dS
+    assert level == 1 and copies <= used < ds
+    _, level, _, used = fb.fa_back_plan_info(*shape, 1 << 40)
+    assert level == 2 and used >= copies + ds
+
+
+def test_plan_info_argument_errors(L):
+    assert fb.STATUS[fb.fa_back_plan_info(8, 32, 6, 4, 64, 64, 1 << 30)[0]] == "FA_ERR_SHAPE"
+    assert fb.STATUS[fb.fa_back_plan_info(8, 32, 4, 2, 96, 96, 1 << 30)[0]] == "FA_ERR_UNSUPPORTED"
