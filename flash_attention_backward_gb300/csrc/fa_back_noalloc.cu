@@ -8,8 +8,6 @@
 // routine.  The launch sequence is fa_back()'s, given that array as its workspace.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "fa_internal.h"
 
 namespace {
@@ -17,22 +15,14 @@ namespace {
 constexpr size_t kScratchBytes = FA_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch[kMaxDevices] = {};  // device address of g_noalloc_scratch, per device
-
-// Device address of the scratch array on the current device.  In host code the array's name
-// is only a host-side stand-in, so the address is looked up once per device with that device
-// current (this happens during the first call on the device).
-void* scratch_on(int dev, cudaError_t* err) {
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch[dev]) {
-    void* p = nullptr;
-    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (*err != cudaSuccess) return nullptr;
-    g_scratch[dev] = p;
-  }
-  return g_scratch[dev];
+// Device address of the scratch array in the current context.  In host code the array's name
+// is only a host-side stand-in, so the address is looked up on every call, with the caller's
+// device current: a context that was reset or replaced since an earlier call may have loaded
+// the module, and the array with it, at another address.
+void* scratch_here(cudaError_t* err) {
+  void* p = nullptr;
+  *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  return *err == cudaSuccess ? p : nullptr;
 }
 
 }  // namespace
@@ -41,14 +31,11 @@ extern "C" fa_status fa_back_noalloc(const float* q, const void* k, int k_type, 
                                      const uint16_t* mask, int mask_heads, const float* dO, float scale, int N,
                                      int M, int H, int Hkv, int D, int Dv, int causal, float* dQ, float* dK,
                                      float* dV, float* lse, float* delta, void* stream) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_DEVICE;
   // the plan takes fewer key splits where that keeps the workspace within the scratch
   const size_t need = fab_workspace_size_capped(N, M, H, Hkv, D, Dv, kScratchBytes);
   if (need > kScratchBytes) return FA_ERR_WORKSPACE;  // larger than the static scratch
   cudaError_t err = cudaSuccess;
-  void* scratch = scratch_on(dev, &err);
+  void* scratch = scratch_here(&err);
   if (!scratch) return FA_ERR_CUDA;
   return fab_back_capped(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal, dQ, dK,
                          dV, lse, delta, scratch, kScratchBytes, stream, kScratchBytes, nullptr, nullptr, nullptr);

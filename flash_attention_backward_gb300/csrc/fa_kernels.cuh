@@ -539,17 +539,33 @@ __global__ void __launch_bounds__(1024) k_finalize(Params p) {
   }
   ram[tid] = my_am;
   __syncthreads();
-  __shared__ float s_sV;
+  __shared__ float s_sV, s_utop;
   if (tid == 0) {
     float ramax = 0.f;
     for (int t = 0; t < (int)blockDim.x; ++t) ramax = fmaxf(ramax, ram[t]);
     ram[0] = ramax;
     s_sV = pow2_scale_for(am[3] + ramax, 14);  // |v^ - r| <= |v^| + |r|
+    // spacing of binary16 values in the top binade that the shifted operand V' can reach
+    int eb = 0;
+    frexpf((am[3] + ramax) * s_sV, &eb);  // bound < 2^eb
+    s_utop = ldexpf(1.f, eb - 11);
   }
   __syncthreads();
-  // the shift actually applied is r' = binary16(r * sV) / sV, so that -r' * sV is exact in binary16
+  // The shift actually applied, r', is r rounded (in scaled units) to a multiple of the top
+  // binade's spacing, or of binary16's spacing at r where that is coarser.  -r' sV is then an
+  // exact binary16 value, and for every cache value whose scaled v^ sV is itself a binary16 value
+  // v^ sV - r' sV lands on the binary16 grid: those rows are shifted without rounding.  With r'
+  // carrying finer bits, all such values would round by the same amount, an error that does not
+  // average out over the keys of a row and that delta (a weighted mean over the keys) keeps whole.
   for (int idx = tid; idx < p.Hkv * p.Dv; idx += blockDim.x) {
-    const float rs = __half2float(__float2half_rn(p.rmean[idx] * s_sV));
+    const float x = p.rmean[idx] * s_sV;
+    float rs = 0.f;
+    if (x != 0.f) {
+      int ex = 0;
+      frexpf(x, &ex);  // |x| < 2^ex
+      const float u = fmaxf(s_utop, ldexpf(1.f, ex - 11));
+      rs = rintf(x / u) * u;
+    }
     p.rmean[idx] = rs / s_sV;
     p.rsh[idx] = -rs;
   }

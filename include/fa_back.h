@@ -244,8 +244,8 @@ int fa_back_profile_read(float* ms_sum, int* launches, const char** names, int m
  *   - The plan is fa_back()'s for a workspace of FA_NOALLOC_SCRATCH_BYTES: the fastest that
  *     fits.  Problems whose fa_back_workspace_size_min() exceeds it are rejected with
  *     FA_ERR_WORKSPACE before anything is enqueued.
- *   - The first call on a device looks up the array's device address with that device
- *     current; make that first call before any stream capture.
+ *   - Every call looks up the array's device address in the current device's context (the
+ *     module, and the array with it, is loaded in each context that first uses the library).
  *   - Every call on a device shares the one array, which keeps the last call's contents.
  *     Nothing in it needs to start at zero: each call writes every scratch word before reading
  *     it.  Calls whose work overlaps on the GPU (other streams, other threads) race on the

@@ -259,18 +259,26 @@ def make_problem(name: str = "custom", *, N: int, M: int, H: int, Hkv: int, D: i
                  k_type="f32", v_type="f32", causal: bool = False, seed: int = 1,
                  scale: Optional[float] = None, mask: Optional[str] = None, mask_p: float = 0.1,
                  full_rows: int = 0, mask_heads: int = 0, v_offset: float = 0.0, v_sigma: float = 1.0,
-                 do_sigma: float = 1.0, q_sigma: float = 1.0, k_sigma: float = 1.0) -> Problem:
+                 do_sigma: float = 1.0, q_sigma: float = 1.0, k_sigma: float = 1.0,
+                 row_decades: float = 0.0) -> Problem:
     """Build a seeded problem.
 
     mask: None, "random" (entries -inf with probability mask_p, else 0, plus
     full_rows query rows set to -inf for every key and head) or "finite"
     (entries uniform in [-2, 0), plus the same -inf pattern).
+    row_decades: when > 0, every (i, h) row of Q and of dO is multiplied by its own
+    10**u, u uniform in [-row_decades, row_decades] (per-row dynamic range).
     """
     kt, vt = _type(k_type), _type(v_type)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     q = normal_f32(seed, S_Q, (N, H, D), q_sigma)
     dO = normal_f32(seed, S_DO, (N, H, Dv), do_sigma)
+    if row_decades > 0:
+        fq = 10.0 ** (row_decades * (2.0 * uniform(seed, S_ROWS + 10, N * H) - 1.0))
+        fo = 10.0 ** (row_decades * (2.0 * uniform(seed, S_ROWS + 11, N * H) - 1.0))
+        q = (q * fq.reshape(N, H, 1)).astype(np.float32)
+        dO = (dO * fo.reshape(N, H, 1)).astype(np.float32)
     kf = normal_f32(seed, S_K, (M, Hkv, D), k_sigma)
     vf = normal_f32(seed, S_V, (M, Hkv, Dv), v_sigma, v_offset)
     k = quantize_rows(kf, kt)
