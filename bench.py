@@ -33,7 +33,7 @@ import synth  # noqa: E402
 METRIC = "FA-back ms + TFLOP/s at N2048/M75520/H24/Hkv4/D256 q8_0; % of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_PRODUCTS = {  # contractions (of the five) each pass forms on every visible (i, j) pair
-    "k_rows_lse": 2, "k_rows_dq": 3, "k_cols": 4, "k_dq_gemm": 1}
+    "k_rows_lse": 2, "k_rows_dq": 3, "k_cols": 4, "k_cols_rowscale": 4, "k_dq_gemm": 1}
 
 
 def peaks():

@@ -26,6 +26,7 @@
 #include "../../include/fa_back.h"
 #include "fa_internal.h"
 #include "fa_kernels.cuh"
+#include "fa_lse_pair.cuh"
 
 namespace fab {
 
@@ -38,7 +39,7 @@ struct Plan {
   int dsq;  // 1 (with pre): the dK/dV pass stores dS and dQ is one product over it (k_dq_gemm)
   int ldds; // 64-key tiles per stored dS row tile (whole gradient-pass key tiles)
   int nsm;
-  size_t off_stats, off_rmean, off_rsh, off_dOr, off_lse2, off_dlt, off_part, off_dqpart, off_q16, off_do16,
+  size_t off_stats, off_rmean, off_rsh, off_dOr, off_lamr, off_lse2, off_dlt, off_part, off_dqpart, off_q16, off_do16,
       off_bstat, off_vsum, off_kd, off_vd, off_ds, total;
 };
 
@@ -57,6 +58,7 @@ static void layout(Plan& P, int M, int Hkv, int D, int Dv) {
   P.off_rmean = o; o = align256(o + sizeof(float) * (size_t)Hkv * Dv);
   P.off_rsh = o; o = align256(o + sizeof(float) * (size_t)Hkv * Dv);
   P.off_dOr = o; o = align256(o + sizeof(float) * (size_t)Hkv * P.R);
+  P.off_lamr = o; o = align256(o + sizeof(float) * (size_t)Hkv * P.R);
   P.off_lse2 = o; o = align256(o + sizeof(float) * (size_t)Hkv * P.R);
   P.off_dlt = o; o = align256(o + sizeof(float) * (size_t)Hkv * P.R);
   P.off_part = o; o = align256(o + sizeof(float) * 3 * (size_t)P.nsplit * Hkv * P.R);
@@ -174,10 +176,10 @@ constexpr int kProfCalls = 256, kProfSlots = 16;
 // (the read-out measures each kernel from the marker recorded before it)
 static const char* const kKernelNames[kProfSlots] = {
     "k_row_stats", "k_vsum", "k_finalize", "k_convert", "k_predecode", "k_rows_lse", "k_lse_merge", "k_rows_dq",
-    "k_dq_reduce", "k_cols", "k_dq_gemm", "k_stats_in", "k_fwd_lse", "k_fwd_o", "k_o_reduce", ""};
+    "k_dq_reduce", "k_cols", "k_dq_gemm", "k_stats_in", "k_fwd_lse", "k_fwd_o", "k_o_reduce", "k_cols_rowscale"};
 enum {
   KS_STATS = 0, KS_VSUM, KS_FINAL, KS_CONVERT, KS_PREDECODE, KS_ROWS_LSE, KS_MERGE, KS_ROWS_DQ, KS_DQ_REDUCE,
-  KS_COLS, KS_DQ_GEMM, KS_STATS_IN, KS_FWD_LSE, KS_FWD_O, KS_O_REDUCE, KS_N
+  KS_COLS, KS_DQ_GEMM, KS_STATS_IN, KS_FWD_LSE, KS_FWD_O, KS_O_REDUCE, KS_COLS_ROWSCALE, KS_N
 };
 
 struct Profiler {
@@ -265,6 +267,28 @@ static void pick_raw(Params& q, int budget, int BK) {
 
 static int raw_bytes(const Params& q) { return q.ke * (q.raw_depth * q.rbk_pad + q.raw_depth_v * q.rbv_pad); }
 
+// The LSE/D pass on CTA pairs from the raw cache (k_lse_pair), then the merge.  Needs raw rows
+// that TMA can box (16-byte multiples); returns cudaErrorNotSupported otherwise, before launching.
+template <int D, int Dv>
+static cudaError_t lse_pair(Params pl, const Plan& P, cudaStream_t s, CallRec& rec) {
+  using L = LsePairCfg<D, Dv>;
+  if (!pl.raw_bulk) return cudaErrorNotSupported;
+  pick_raw(pl, L::RAW_BUDGET, L::HK);
+  if (L::HK % pl.ke || (pl.ke * pl.rbk_pad) % 128 || (pl.ke * pl.rbv_pad) % 128) return cudaErrorNotSupported;
+  const int sm = L::OFF_RAW + raw_bytes(pl) + 1024 + 64;  // + base alignment, decoders' realigning reads
+  if (sm > 232448) return cudaErrorNotSupported;
+  CUtensorMap tk, tv;
+  if (!make_raw_map(&tk, pl.k, pl.rbk, pl.Hkv, pl.M, pl.ke) || !make_raw_map(&tv, pl.v, pl.rbv, pl.Hkv, pl.M, pl.ke))
+    return cudaErrorInvalidValue;
+  cudaError_t e;
+  if ((e = set_smem(k_lse_pair<D, Dv>, sm)) != cudaSuccess) return e;
+  k_lse_pair<D, Dv><<<dim3(2 * ((P.nQT + 1) / 2), pl.Hkv, P.nsplit), L::NT, sm, s>>>(tk, tv, pl);
+  rec.mark(KS_ROWS_LSE);
+  k_lse_merge<<<(unsigned)(((long)pl.Hkv * P.R + 255) / 256), 256, 0, s>>>(pl);
+  rec.mark(KS_MERGE);
+  return cudaGetLastError();
+}
+
 // Row passes over the binary16 K'/V' copies (written here by k_predecode), fed by TMA.
 template <int D, int Dv, int BK, int BKL>
 static cudaError_t rows_pre(const Params& pl, const Params& pq, const Plan& P, const CUtensorMap& tmQ, dim3 grid,
@@ -325,10 +349,15 @@ static cudaError_t rows_raw(Params pl, Params pq, const Plan& P, const CUtensorM
       return cudaErrorInvalidValue;
   }
   if (!pl.lse_in) {
-    k_rows2<D, Dv, BKL, 0><<<grid, RL::NT, sm_l, s>>>(tmQ, tkl, tvl, pl);
-    rec.mark(KS_ROWS_LSE);
-    k_lse_merge<<<(unsigned)(((long)pl.Hkv * P.R + 255) / 256), 256, 0, s>>>(pl);
-    rec.mark(KS_MERGE);
+    cudaError_t ep = lse_pair<D, Dv>(pl, P, s, rec);
+    if (ep == cudaErrorNotSupported) {
+      k_rows2<D, Dv, BKL, 0><<<grid, RL::NT, sm_l, s>>>(tmQ, tkl, tvl, pl);
+      rec.mark(KS_ROWS_LSE);
+      k_lse_merge<<<(unsigned)(((long)pl.Hkv * P.R + 255) / 256), 256, 0, s>>>(pl);
+      rec.mark(KS_MERGE);
+    } else if (ep != cudaSuccess) {
+      return ep;
+    }
   }
   k_rows2<D, Dv, BK, 1><<<grid, RQ::NT, sm_q, s>>>(tmQ, tkq, tvq, pq);
   rec.mark(KS_ROWS_DQ);
@@ -364,9 +393,14 @@ static cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& 
                 !make_map(&tvc, p.vd, 64, p.M, p.Hkv * (Dv / 64), BK)))
     return cudaErrorInvalidValue;
   if (P.nKT > 0) {
-    if ((e = set_smem(k_cols2<D, Dv, BK>, CC::SMEM)) != cudaSuccess) return e;
-    k_cols2<D, Dv, BK><<<dim3(P.nKT, p.Hkv), 384, CC::SMEM, s>>>(tmQ, tmO, tmS, tkc, tvc, p);
+    if ((e = set_smem(k_cols2<D, Dv, BK, false>, CC::SMEM)) != cudaSuccess) return e;
+    k_cols2<D, Dv, BK, false><<<dim3(P.nKT, p.Hkv), 384, CC::SMEM, s>>>(tmQ, tmO, tmS, tkc, tvc, p);
     rec.mark(KS_COLS);
+    if (P.dsq) {  // the variant with per-row multipliers on the stored dS (returns at once if not needed)
+      if ((e = set_smem(k_cols2<D, Dv, BK, true>, CC::SMEM)) != cudaSuccess) return e;
+      k_cols2<D, Dv, BK, true><<<dim3(P.nKT, p.Hkv), 384, CC::SMEM, s>>>(tmQ, tmO, tmS, tkc, tvc, p);
+      rec.mark(KS_COLS_ROWSCALE);
+    }
   }
   if (P.dsq) {
     using GC = GemmCfg<D, BK>;
@@ -634,6 +668,7 @@ extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, 
   p.st = reinterpret_cast<Stats*>(ws + P.off_stats);
   p.rmean = reinterpret_cast<float*>(ws + P.off_rmean);
   p.dOr = reinterpret_cast<float*>(ws + P.off_dOr);
+  p.lamr = reinterpret_cast<float*>(ws + P.off_lamr);
   p.lse2 = reinterpret_cast<float*>(ws + P.off_lse2);
   p.dlt = reinterpret_cast<float*>(ws + P.off_dlt);
   p.part = reinterpret_cast<float*>(ws + P.off_part);

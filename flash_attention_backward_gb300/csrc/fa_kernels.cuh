@@ -23,6 +23,7 @@
 #pragma once
 #include <cuda_fp16.h>
 #include <math_constants.h>
+#include <climits>
 #include <stdint.h>
 
 #include "sm100.cuh"
@@ -44,7 +45,18 @@ struct Stats {
   float dq_fac, dk_fac, dv_fac, delta_fac;
   float amax[4], norm2[4];
   float rnorm, ramax;
+  int lamr_exp;  // largest exponent of the per-row dS multipliers (raised by k_convert)
 };
+
+// The dS stored for the dQ product takes each row's own multiplier only when some row's exceeds
+// the common one by more than 2^12.  A row within that gap has its largest |dS| value no more
+// than 2^12 below the common scale's 2^15, so its values stay far inside binary16's normal range
+// and keep its relative precision; the per-row copy costs the dK/dV pass extra shared-memory
+// traffic, so typical inputs (rows of similar size) skip it.
+__host__ __device__ constexpr int kRowScaleGap = 12;
+__device__ __forceinline__ bool rows_need_own_scale(const Stats& st) {
+  return st.lamr_exp - ilogbf(st.lam) > kRowScaleGap;
+}
 
 struct Params {
   const float* q;
@@ -80,7 +92,9 @@ struct Params {
   __half* kd;     // [Hkv][D/64][M][64]   binary16 K' = k^ sK, panel-major (TMA-fed passes; else null)
   __half* vd;     // [Hkv][Dv/64][M][64]  binary16 V' = v^ sV - r' sV
   float* o_out;   // [N][H][Dv] forward output O (fa_forward), or null
-  __half* ds;     // binary16 lam * dS from the dK/dV pass, read by k_dq_gemm (or null): contiguous
+  float* lamr;    // [Hkv][R]  per-row multiplier of dS for the dQ product (power of two), from
+                  //           the row's own |dO_i| bound, so small rows keep binary16 precision
+  __half* ds;     // binary16 lamr * dS from the dK/dV pass, read by k_dq_gemm (or null): contiguous
                   // [128 rows][64 keys] tiles, tile (hk, row tile qt, key tile kt64) at
                   // (hk * nQT + qt) * ldds + kt64
   int ldds;       // 64-key tiles per row tile (whole gradient-pass key tiles)
@@ -598,13 +612,18 @@ __global__ void __launch_bounds__(1024) k_finalize(Params p) {
     s.dk_fac = p.scale / (s.lam * s.sdO * s.sV * s.sQ);
     s.dv_fac = 1.f / (s.sP * s.sdO);
     s.delta_fac = 1.f / (s.sdO * s.sV);
+    s.lamr_exp = ilogbf(s.lam);
     *p.st = s;
   }
 }
 
-// One warp per (i, h): binary16 rows of Q and dO (row r = i*G + g of head hk) and dO_i . r.
+// One warp per (i, h): binary16 rows of Q and dO (row r = i*G + g of head hk), dO_i . r and the
+// row's dS multiplier for the dQ product.
 __global__ void __launch_bounds__(256) k_convert(Params p) {
+  __shared__ int s_lexp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) s_lexp = INT_MIN;
+  __syncthreads();
   const long nrow = (long)p.N * p.H;
   const float sQ = p.st->sQ, sdO = p.st->sdO;
   for (long rw = (long)blockIdx.x * 8 + warp; rw < nrow; rw += (long)gridDim.x * 8) {
@@ -621,16 +640,29 @@ __global__ void __launch_bounds__(256) k_convert(Params p) {
     const float* os = p.dO + rw * p.Dv;
     __half* od = p.do16 + ((size_t)hk * p.R + r) * p.Dv;
     const float* rm = p.rmean + (size_t)hk * p.Dv;
-    float dot = 0.f;
+    float dot = 0.f, n2 = 0.f;
     for (int c = 2 * lane; c < p.Dv; c += 64) {
       const float2 x = __ldg(reinterpret_cast<const float2*>(os + c));
       *reinterpret_cast<__half2*>(od + c) = __floats2half2_rn(x.x * sdO, x.y * sdO);
       dot = fmaf(x.x, rm[c], dot);
       dot = fmaf(x.y, rm[c + 1], dot);
+      n2 = fmaf(x.x, x.x, fmaf(x.y, x.y, n2));
     }
     dot = warp_sum(dot);
-    if (lane == 0) p.dOr[(size_t)hk * p.R + r] = dot;
+    n2 = warp_sum(n2);
+    if (lane == 0) {
+      p.dOr[(size_t)hk * p.R + r] = dot;
+      // this row's |dS_ij| <= p_ij |dP'_ij - delta'_i| <= 2 |dO_i| max_j |v^_j - r| (scaled units)
+      const Stats* st = p.st;
+      const float bound = 2.f * (sqrtf(n2) * sdO) * ((sqrtf(st->norm2[3]) + st->rnorm) * st->sV) * 1.01f;
+      const float lr = pow2_scale_for(bound, 15);
+      p.lamr[(size_t)hk * p.R + r] = lr;
+      atomicMax(&s_lexp, ilogbf(lr));
+    }
   }
+  __syncthreads();
+  // the exponents' maximum over rows: the same result in any order
+  if (threadIdx.x == 0 && s_lexp != INT_MIN) atomicMax(&p.st->lamr_exp, s_lexp);
 }
 
 // Binary16 operand copies of the cache for the producer-fed row passes: K'[hk][j] = k^_j sK and
@@ -1059,7 +1091,9 @@ __global__ void __launch_bounds__(Rows2Cfg<D, Dv, BK, MODE>::NT, 1)
       dl = p.dlt[(size_t)hk * R + r];
     }
     const bool live = MODE == 1 ? (lse2 > -CUDART_INF_F) : rvalid;
-    const float c2 = st.c2, lam = st.lam, dq_fac = st.dq_fac;
+    // the dQ pass scales this row's dS by its own power of two lamr (the product sums over keys only)
+    const float lam = (MODE == 1 && rvalid) ? p.lamr[(size_t)hk * R + r] : st.lam;
+    const float c2 = st.c2, dq_fac = st.dq_fac * (st.lam / lam);
     // 2^(t2 + nlse2) = p (0 on a dead row); in the dQ pass the exponent also carries log2(lam),
     // so the exponential yields lam * p directly (lam is a power of two)
     const float nlse2 = live ? -lse2 + (MODE == 1 ? (float)ilogbf(lam) : 0.f) : -CUDART_INF_F;
@@ -1526,7 +1560,9 @@ __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
       if (MODE == 1) dl = p.dlt[(size_t)hk * R + r];
     }
     const bool live = C::ROWQ ? (lse2 > -CUDART_INF_F) : rvalid;
-    const float c2 = st.c2, lam = st.lam, dq_fac = st.dq_fac;
+    // the dQ pass scales this row's dS by its own power of two lamr (the product sums over keys only)
+    const float lam = (MODE == 1 && rvalid) ? p.lamr[(size_t)hk * R + r] : st.lam;
+    const float c2 = st.c2, dq_fac = st.dq_fac * (st.lam / lam);
     // 2^(t2 + nlse2) = p (0 on a dead row); the exponent also carries log2 of the power-of-two
     // multiplier of the product's binary16 panel, so the exponential yields it directly: lam * p
     // in the dQ pass (dS = lam p (dP - delta)), sP * p in the forward O pass
@@ -1849,9 +1885,12 @@ __global__ void __launch_bounds__(256) k_dq_reduce(Params p) {
 // released when the last product reading it completes, so the next tile's loads overlap this
 // tile's final products without a second buffer.
 // Warp roles (12 warps): 0 producer, 1 MMA issuer / tensor-memory owner, 4-11 softmax and
-// epilogue; without the binary16 copies every warp decodes K' and V' at the start.  Where the plan keeps dS for a separate
-// dQ product (p.ds), warp 2 stores each tile's dS panels to it with TMA, and the dS buffer is
-// released only once both the gradient products and that store have read it.
+// epilogue; without the binary16 copies every warp decodes K' and V' at the start.  Where the
+// plan keeps dS for a separate dQ product (p.ds), the copy it stores is scaled by each row's own
+// power of two (p.lamr) rather than the common multiplier of the dK^T operand: dQ is formed per
+// row, so rows whose dO is much smaller than the largest keep binary16's relative precision.  The
+// softmax writes that copy into the P panel once the dV^T product has read P, and warp 2 stores
+// it with TMA; the next tile's P waits for the store to have read the panel.
 
 template <int D, int Dv, int BK>
 struct Cols2Cfg {
@@ -1877,12 +1916,19 @@ enum {
   C_DS_FULL,
   C_DS_EMPTY,
   C_DONE,
-  C_KV_FULL,  // K'/V' tiles loaded from the binary16 copies (levels 2 and 1)
+  C_KV_FULL,   // K'/V' tiles loaded from the binary16 copies (levels 2 and 1)
+  C_DSR_FULL,  // the softmax left this tile's per-row-scaled dS in the P panel (stored dS only)
+  C_PS_EMPTY,  // the TMA store read that copy: the P panel may take the next tile's P
   C_COUNT
 };
 static_assert(8 * C_COUNT + 8 <= 256, "dK/dV pass barrier area");
 
-template <int D, int Dv, int BK>
+// ROWCOPY selects the variant whose stored dS takes per-row multipliers.  Both variants are
+// launched where dS is stored; each reads the decision (rows_need_own_scale, from the statistics
+// on the device) first and returns at once unless it is the one that applies.  Separate variants
+// keep the copy's code out of the common one: built into one kernel behind a run-time branch, it
+// slowed the pass by about 5 % even where the branch was never taken.
+template <int D, int Dv, int BK, bool ROWCOPY>
 __global__ void __launch_bounds__(384, 1)
     k_cols2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
             const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmKd,
@@ -1911,6 +1957,10 @@ __global__ void __launch_bounds__(384, 1)
   }
   const int nq = R > 0 ? max(0, p.nQT - qt_begin) : 0;
 
+  // the dS kept for the dQ product: the dK^T operand's panel as it is, or a copy with each row's
+  // own multiplier (left by the softmax in the P panel) when rows differ widely in size
+  constexpr bool rowcopy = ROWCOPY;
+  if (ROWCOPY != (p.ds != nullptr && rows_need_own_scale(*p.st))) return;  // the other variant applies
   if (warp == 1) tmem_alloc(tslot, C::TCOLS);
   if (tid == 0) {
     for (int c = 0; c < 4; ++c) {
@@ -1923,9 +1973,11 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&bar[C_P_FULL], 8);
     mbar_init(&bar[C_P_EMPTY], 1);
     mbar_init(&bar[C_DS_FULL], 8);
-    mbar_init(&bar[C_DS_EMPTY], p.ds ? 2 : 1);
+    mbar_init(&bar[C_DS_EMPTY], (p.ds && !rowcopy) ? 2 : 1);  // the dK^T product (and the store)
     mbar_init(&bar[C_DONE], 1);
     mbar_init(&bar[C_KV_FULL], 1);
+    mbar_init(&bar[C_DSR_FULL], 8);
+    mbar_init(&bar[C_PS_EMPTY], 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -2041,17 +2093,18 @@ __global__ void __launch_bounds__(384, 1)
       mma_commit(&bar[C_DONE]);
     }
   } else if (warp == 2) {
-    // ------------------------------------------------------------------ dS store (dQ by GEMM)
+    // ------------------------------------------------------------------ stored dS (dQ product)
     if (lane == 0 && p.ds) {
       prefetch_tmap(&tmS);
       for (int t = 0; t < nq; ++t) {
-        if (!wait(&bar[C_DS_FULL], t & 1)) break;
+        if (!wait(&bar[rowcopy ? C_DSR_FULL : C_DS_FULL], t & 1)) break;
+        uint8_t* src = rowcopy ? sP : sS;
 #pragma unroll
         for (int c = 0; c < BK / 64; ++c)
-          tma_store_3d(&tmS, sS + c * (128 * 128), 0, 0, (hk * p.nQT + qt_begin + t) * p.ldds + j0 / 64 + c);
+          tma_store_3d(&tmS, src + c * (128 * 128), 0, 0, (hk * p.nQT + qt_begin + t) * p.ldds + j0 / 64 + c);
         bulk_commit_group();
-        bulk_wait_read_all();  // the panels may be overwritten once read
-        mbar_arrive(&bar[C_DS_EMPTY]);
+        bulk_wait_read_all();  // the panel may be overwritten once read
+        mbar_arrive(&bar[rowcopy ? C_PS_EMPTY : C_DS_EMPTY]);
       }
       bulk_wait_all();
     }
@@ -2060,33 +2113,55 @@ __global__ void __launch_bounds__(384, 1)
     const int q4 = warp & 3, ch = (warp - 4) >> 2;
     const int row = q4 * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    auto row_stats = [&](int t, float& lse2, float& dl, long& jlast, const uint16_t*& mrow) {
+    auto row_stats = [&](int t, float& lse2, float& dl, float& lr, long& jlast, const uint16_t*& mrow) {
       const int r = (qt_begin + t) * 128 + row;
       const bool rvalid = r < R;
       const int i = rvalid ? r / G : 0;
       const int h = hk * G + (rvalid ? r % G : 0);
       lse2 = rvalid ? p.lse2[(size_t)hk * R + r] : -CUDART_INF_F;
       dl = rvalid ? p.dlt[(size_t)hk * R + r] : 0.f;
+      lr = (rvalid && rowcopy) ? p.lamr[(size_t)hk * R + r] * (1.f / 32768.f) : 0.f;  // row multiplier / sP
       jlast = rvalid ? (p.causal ? min((long)p.M - 1, (long)p.M - p.N + i) : (long)p.M - 1) : -1;
       mrow = p.mask ? p.mask + ((size_t)(h % p.Hm) * p.N + i) * p.M : nullptr;
     };
-    float lse2 = 0.f, dl = 0.f;
+    float lse2 = 0.f, dl = 0.f, lr = 0.f;
     long jlast = -1;
     const uint16_t* mrow = nullptr;
+    constexpr bool keep = ROWCOPY;
+    // this thread's 32 values of the stored dS copy (row multiplier lr; 0 for a row past R)
+    auto ds_row = [&](const float* pv, const float* dpv, uint32_t* w) {
+#pragma unroll
+      for (int x = 0; x < 32; x += 2)
+        w[x / 2] = h2_as_u32(__floats2half2_rn(pv[x] * (dpv[x] - dl) * lr, pv[x + 1] * (dpv[x + 1] - dl) * lr));
+    };
+    // once the dV^T product of tile t has read P, the stored dS copy goes into the P panel
+    auto put_ds_copy = [&](int t, int col0, const uint32_t* w, int nchunk) -> bool {
+      if (!wait(&bar[C_P_EMPTY], t & 1)) return false;
+      for (int c = 0; c < nchunk; ++c)
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          sts_v4(smem_u32(sP) + panel_off_u(128, row, col0 + 32 * c + 8 * g), w[16 * c + 4 * g], w[16 * c + 4 * g + 1],
+                 w[16 * c + 4 * g + 2], w[16 * c + 4 * g + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[C_DSR_FULL]);
+      return true;
+    };
     const uint32_t sP_u = smem_u32(sP), sS_u = smem_u32(sS);
     // the exponent carries log2 of the P multiplier (a power of two), so the exponential is
     // the scaled P directly and dS takes lam / sP
     const float c2 = st.c2, lp = (float)ilogbf(st.sP), lam = st.lam / st.sP;
-    if (nq > 0) row_stats(0, lse2, dl, jlast, mrow);
+    if (nq > 0) row_stats(0, lse2, dl, lr, jlast, mrow);
     for (int t = 0; t < nq; ++t) {
-      float nlse2 = 0.f, ndl = 0.f;  // next tile's row values, fetched ahead
+      float nlse2 = 0.f, ndl = 0.f, nlr = 0.f;  // next tile's row values, fetched ahead
       long njlast = -1;
       const uint16_t* nmrow = nullptr;
-      if (t + 1 < nq) row_stats(t + 1, nlse2, ndl, njlast, nmrow);
+      if (t + 1 < nq) row_stats(t + 1, nlse2, ndl, nlr, njlast, nmrow);
       const float nl = lse2 > -CUDART_INF_F ? lp - lse2 : -CUDART_INF_F;  // sP * p = 2^(t2 + nl); 0 on a dead row
       if (!wait(&bar[C_S_FULL], t & 1)) break;
-      // the previous tile's P panel is free once its dV product read it
+      // the previous tile's P panel is free once its dV product (and the store of its dS copy) read it
       if (!wait(&bar[C_P_EMPTY], (t & 1) ^ 1)) break;
+      if (keep && !wait(&bar[C_PS_EMPTY], (t & 1) ^ 1)) break;
       tc_fence_after();
       // log2-domain exponents of one 32-key chunk; a fully visible chunk without a mask takes
       // no per-key tests
@@ -2126,18 +2201,27 @@ __global__ void __launch_bounds__(384, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[C_P_FULL]);
-        uint32_t pd[16];
+        uint32_t pd[16], pr[16];
 #pragma unroll
         for (int x = 0; x < 32; x += 2)
           pd[x / 2] = h2_as_u32(__floats2half2_rn(s[x] * (dp[x] - dl) * lam, s[x + 1] * (dp[x + 1] - dl) * lam));
-        // the previous tile's dS panel is free once its dK product and its store read it
+        if (keep) ds_row(s, dp, pr);
+        // the previous tile's dS panel is free once its dK product (and its store) read it
         if (!wait(&bar[C_DS_EMPTY], (t & 1) ^ 1)) break;
 #pragma unroll
         for (int g = 0; g < 4; ++g)
           sts_v4(sS_u + panel_off_u(128, row, col0 + 8 * g), pd[4 * g], pd[4 * g + 1], pd[4 * g + 2], pd[4 * g + 3]);
+        if (keep) {
+          tc_fence_before();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar[C_DS_FULL]);
+          if (!put_ds_copy(t, col0, pr, 1)) break;
+        }
       } else {
         if (!wait(&bar[C_DS_EMPTY], (t & 1) ^ 1)) break;
-#pragma unroll 1
+        uint32_t pr[C::HALF / 2];
+#pragma unroll
         for (int c = 0; c < C::HALF; c += 32) {
           const int col0 = ch * C::HALF + c;
           float s[32], dp[32];
@@ -2146,12 +2230,15 @@ __global__ void __launch_bounds__(384, 1)
           tmem_ld_wait();
           exponents(col0, s);
 #pragma unroll
+          for (int x = 0; x < 32; ++x) s[x] = ex2(s[x]);  // sP * p; 0 for masked keys and dead rows
+          if (keep) ds_row(s, dp, pr + c / 2);
+#pragma unroll
           for (int g = 0; g < 32; g += 8) {
             uint32_t pp[4], pd[4];
 #pragma unroll
             for (int n = 0; n < 8; n += 2) {
               const int x = g + n;
-              const float p0 = ex2(s[x]), p1 = ex2(s[x + 1]);  // sP * p; 0 for masked keys and dead rows
+              const float p0 = s[x], p1 = s[x + 1];
               pp[n / 2] = h2_as_u32(__floats2half2_rn(p0, p1));
               pd[n / 2] = h2_as_u32(__floats2half2_rn(p0 * (dp[x] - dl) * lam, p1 * (dp[x + 1] - dl) * lam));
             }
@@ -2163,13 +2250,22 @@ __global__ void __launch_bounds__(384, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[C_P_FULL]);
+        if (keep) {
+          tc_fence_before();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar[C_DS_FULL]);
+          if (!put_ds_copy(t, ch * C::HALF, pr, C::HALF / 32)) break;
+        }
       }
       if (*s_abort) break;
-      tc_fence_before();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[C_DS_FULL]);
-      lse2 = nlse2, dl = ndl, jlast = njlast, mrow = nmrow;
+      if (!keep) {
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[C_DS_FULL]);
+      }
+      lse2 = nlse2, dl = ndl, lr = nlr, jlast = njlast, mrow = nmrow;
     }
     // epilogue: lane = feature row of a half, columns = keys; this warp takes half the keys
     const bool have = nq > 0 && wait(&bar[C_DONE], 0);
@@ -2351,7 +2447,10 @@ __global__ void __launch_bounds__(256, 1)
     float* out = !rvalid ? nullptr
                  : p.nsplit == 1 ? p.dQ + ((size_t)i * p.H + h) * D
                                  : p.dqpart + (((size_t)split * p.Hkv + hk) * R + r) * D;
-    const float dq_fac = p.st->dq_fac;
+    const Stats st = *p.st;
+    const float dq_fac = !rvalid ? 0.f
+                         : rows_need_own_scale(st) ? st.dq_fac * (st.lam / p.lamr[(size_t)hk * R + r])
+                                                   : st.dq_fac;
     const bool have = ntiles > 0 && wait(&bar[G_ACC], 0);
     if (have) tc_fence_after();
 #pragma unroll 1

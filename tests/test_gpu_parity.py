@@ -90,12 +90,19 @@ def test_edge_cases(fb, name):
 
 # Shapes that stress the precision of delta: it is a softmax-weighted mean of dP_ij, so when the
 # softmax of a row is spread over many keys it is small next to its terms.  Near-uniform rows come
-# from Q scaled close to zero.
+# from Q scaled close to zero.  The row-range case multiplies every (i, h) row of Q and of dO by
+# its own factor in [1e-3, 1e3] (the scale is reduced so that the largest rows' logits stay near
+# one); rows with a small dO then depend on the per-row multiplier of dS in the dQ product.  The
+# logit case doubles Q (logits about 2 in size), inside the envelope of single-pass binary16 S.
 PRECISION = {
     "d64_q4v_17k": dict(N=256, M=17000, H=8, Hkv=2, D=64, Dv=64, k_type="q8_0", v_type="q4_0", causal=True),
     "uniform_d64_65k": dict(N=64, M=65536, H=8, Hkv=2, D=64, Dv=64, k_type="q8_0", v_type="q8_0", q_sigma=1e-3),
     "uniform_d256_65k": dict(N=32, M=65536, H=4, Hkv=1, D=256, Dv=256, k_type="q8_0", v_type="q8_0",
                              q_sigma=1e-3, causal=True),
+    "row_range_d128": dict(N=128, M=4096, H=8, Hkv=2, D=128, Dv=128, k_type="q8_0", v_type="q4_0", causal=True,
+                           row_decades=3.0, scale=1e-3 / 128 ** 0.5),
+    "logits_x2_d128": dict(N=128, M=4096, H=8, Hkv=2, D=128, Dv=128, k_type="q8_0", v_type="q8_0", causal=True,
+                           q_sigma=2.0),
 }
 
 
