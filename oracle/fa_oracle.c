@@ -29,6 +29,20 @@
  *
  *   O[i,h]  = sum_j p_ij * V^[j,hk]
  *
+ * Extensions (oracle_fa_back_ext).  The pages exclude these and define none,
+ * so the definitions are the common ones, each optional:
+ *   soft-capping, c > 0:  s_ij = c * tanh(scale * q_i . k^_j / c) + mask
+ *                          (the cap applies to the scaled product only), and
+ *                          dS_ij = p_ij (dP_ij - delta_ih) (1 - tanh^2(.))
+ *                          since ds/d(scale q.k) = 1 - tanh^2
+ *   ALiBi slope m_h:       s_ij += m_h * (j - (M - N + i))   (query i sits
+ *                          at position M - N + i, as in the causal tail)
+ *   sink logit sigma_h:    e^sigma_h joins the softmax denominator:
+ *                          lse_ih = log(e^sigma_h + sum_allowed e^s_ij)
+ *                          (finite even without an allowed key); the sink
+ *                          has no value, so delta and dS keep their form;
+ *                          dsigma_h = -sum_i e^(sigma_h - lse_ih) delta_ih
+ *
  * K^ and V^ are the cache rows decoded exactly as the block formats define
  * them (a q8_0 block: binary16 scale d, then 32 int8 codes, value code*d;
  * a q4_0 block: binary16 scale d, then 16 bytes whose low nibble is element
@@ -123,6 +137,10 @@ typedef struct {
   const int64_t* dq_index; /* [N]: position in the dQ output or -1 */
   const int64_t* keys;
   int nkeys;
+  /* extensions (all optional) */
+  const double* alibi; /* [H] slopes, or NULL */
+  double softcap;      /* c > 0, or 0 */
+  const double* sinks; /* [H] sink logits, or NULL */
   /* outputs */
   double *lse, *delta, *dQ, *dK, *dV;
   double* O; /* [N][H][Dv] forward output, or NULL */
@@ -148,7 +166,22 @@ static int is_allowed(const Job* J, int i, int j, double mval) {
 
 /* Phase 1: for a group of RB rows r = i*G + g of KV head hk, form s and dP for
  * every key, then lse, delta and (for selected i) dQ row by row. */
-static void phase1_item(Job* J, int item, double* S, double* DP, double* qt, double* dot) {
+/* The logit from the scaled product: soft-capping, then the mask and the ALiBi bias.  *fac is
+ * d(logit)/d(scaled product): 1 - tanh^2 under the cap, else 1. */
+static double logit_of(const Job* J, double raw, double mv, int i, int j, int h, double* fac) {
+  double s = raw;
+  *fac = 1.0;
+  if (J->softcap > 0.0) {
+    const double t = tanh(raw / J->softcap);
+    s = J->softcap * t;
+    *fac = 1.0 - t * t;
+  }
+  s += mv;
+  if (J->alibi) s += J->alibi[h] * ((double)j - ((double)J->M - J->N + i));
+  return s;
+}
+
+static void phase1_item(Job* J, int item, double* S, double* DP, double* qt, double* dot, double* F) {
   const int G = J->G, D = J->D, Dv = J->Dv, M = J->M, N = J->N, H = J->H, Hkv = J->Hkv;
   const int rows_per_hk = N * G;
   const int nblk = (rows_per_hk + RB - 1) / RB;
@@ -199,7 +232,8 @@ static void phase1_item(Job* J, int item, double* S, double* DP, double* qt, dou
     const int rr = r0 + r, i = rr / G, h = hk * G + rr % G;
     double* s = S + (int64_t)r * M;
     const double* dp = DP + (int64_t)r * M;
-    /* add the mask; keys that are not allowed are marked with -inf */
+    double* fac = F + (int64_t)r * M;
+    /* the logits (cap, mask, bias); keys that are not allowed are marked with -inf */
     double mx = -INFINITY;
     int any = 0;
     for (int j = 0; j < M; ++j) {
@@ -208,22 +242,25 @@ static void phase1_item(Job* J, int item, double* S, double* DP, double* qt, dou
         s[j] = -INFINITY;
         continue;
       }
-      s[j] += mv;
+      s[j] = logit_of(J, s[j], mv, i, j, h, &fac[j]);
       if (!any || s[j] > mx) mx = s[j];
       any = 1;
     }
     const int64_t o = (int64_t)i * H + h;
     int64_t qi = J->dq_index ? J->dq_index[i] : -1;
-    if (!any) {
+    const double sink = J->sinks ? J->sinks[h] : -INFINITY;
+    if (!any && !J->sinks) {
       J->lse[o] = -INFINITY;
       J->delta[o] = 0.0;
       if (qi >= 0) memset(J->dQ + (qi * H + h) * (int64_t)D, 0, sizeof(double) * D);
       if (J->O) memset(J->O + o * Dv, 0, sizeof(double) * Dv);
       continue;
     }
+    if (J->sinks && (!any || sink > mx)) mx = sink;
     double sum = 0.0;
     for (int j = 0; j < M; ++j)
       if (s[j] != -INFINITY) sum += exp(s[j] - mx);
+    if (J->sinks) sum += exp(sink - mx);
     const double lse = mx + log(sum);
     double delta = 0.0;
     for (int j = 0; j < M; ++j)
@@ -246,7 +283,7 @@ static void phase1_item(Job* J, int item, double* S, double* DP, double* qt, dou
       for (int j = 0; j < M; ++j) {
         if (s[j] == -INFINITY) continue;
         const double p = exp(s[j] - lse);
-        const double ds = p * (dp[j] - delta);
+        const double ds = p * (dp[j] - delta) * fac[j];
         const double* k = J->Kh + ((int64_t)j * Hkv + (h / G)) * D;
         for (int c = 0; c < D; ++c) out[c] += ds * k[c];
       }
@@ -298,9 +335,10 @@ static void phase2_item(Job* J, int item, double* kt, double* vt) {
         const int j = (int)J->keys[k0 + t];
         const double mv = mask_at(J, i, j, h);
         if (!is_allowed(J, i, j, mv)) continue;
-        const double s = J->scale * acc[t] + mv;
+        double fac;
+        const double s = logit_of(J, J->scale * acc[t], mv, i, j, h, &fac);
         const double p = exp(s - lse);
-        const double ds = p * (acc2[t] - J->delta[o]);
+        const double ds = p * (acc2[t] - J->delta[o]) * fac;
         const int64_t ko = ((int64_t)(k0 + t) * Hkv + hk);
         double* dk = J->dK + ko * D;
         double* dv = J->dV + ko * Dv;
@@ -313,15 +351,16 @@ static void phase2_item(Job* J, int item, double* kt, double* vt) {
 static void* worker(void* arg) {
   Job* J = (Job*)arg;
   const int RBmax = RB;
-  double *S = NULL, *DP = NULL, *bufA = NULL, *bufB = NULL;
+  double *S = NULL, *DP = NULL, *F = NULL, *bufA = NULL, *bufB = NULL;
   int64_t dmax = J->D > J->Dv ? J->D : J->Dv;
   bufA = (double*)malloc(sizeof(double) * dmax * RBmax);
   bufB = (double*)malloc(sizeof(double) * dmax * RBmax);
   if (J->phase == 1) {
     S = (double*)malloc(sizeof(double) * ((int64_t)RBmax * J->M + 1));
     DP = (double*)malloc(sizeof(double) * ((int64_t)RBmax * J->M + 1));
+    F = (double*)malloc(sizeof(double) * ((int64_t)RBmax * J->M + 1));
   }
-  if (!bufA || !bufB || (J->phase == 1 && (!S || !DP))) {
+  if (!bufA || !bufB || (J->phase == 1 && (!S || !DP || !F))) {
     pthread_mutex_lock(&J->mu);
     J->err = 2;
     pthread_mutex_unlock(&J->mu);
@@ -332,13 +371,14 @@ static void* worker(void* arg) {
       pthread_mutex_unlock(&J->mu);
       if (it >= J->nitems) break;
       if (J->phase == 1)
-        phase1_item(J, it, S, DP, bufA, bufB);
+        phase1_item(J, it, S, DP, bufA, bufB, F);
       else
         phase2_item(J, it, bufA, bufB);
     }
   }
   free(S);
   free(DP);
+  free(F);
   free(bufA);
   free(bufB);
   return NULL;
@@ -378,8 +418,10 @@ static int run_oracle(const float* q, const uint8_t* k, int k_type, const uint8_
                       const uint16_t* mask, int mask_heads, const float* dO, double scale, int N, int M, int H,
                       int Hkv, int D, int Dv, int causal, const int64_t* dq_rows, int n_dq_rows,
                       const int64_t* dkv_keys, int n_dkv_keys, double* lse, double* delta, double* dQ, double* dK,
-                      double* dV, double* O, int nthreads) {
+                      double* dV, double* O, const double* alibi, double softcap, const double* sinks,
+                      double* dsinks, int nthreads) {
   if (!q || !k || !v || !dO || !lse || !delta) return 1;
+  if (!(softcap >= 0.0) || isinf(softcap)) return 1;
   if (N < 0 || M < 0 || H <= 0 || Hkv <= 0 || D <= 0 || Dv <= 0 || H % Hkv) return 1;
   if (mask && mask_heads != 1 && mask_heads != H) return 1;
   if (oracle_row_bytes(k_type, D) <= 0 || oracle_row_bytes(v_type, Dv) <= 0) return 1;
@@ -390,6 +432,7 @@ static int run_oracle(const float* q, const uint8_t* k, int k_type, const uint8_
   J.N = N, J.M = M, J.H = H, J.Hkv = Hkv, J.D = D, J.Dv = Dv, J.G = H / Hkv, J.causal = causal;
   J.scale = scale, J.mask = mask, J.Hm = mask ? mask_heads : 1;
   J.lse = lse, J.delta = delta, J.dQ = dQ, J.dK = dK, J.dV = dV, J.O = O;
+  J.alibi = alibi, J.softcap = softcap, J.sinks = sinks;
   int rc = 0;
   double* Qd = (double*)malloc(sizeof(double) * ((int64_t)N * H * D + 1));
   double* dOd = (double*)malloc(sizeof(double) * ((int64_t)N * H * Dv + 1));
@@ -433,6 +476,17 @@ static int run_oracle(const float* q, const uint8_t* k, int k_type, const uint8_
     rc = run_phase(&J, nthreads);
     if (rc) goto done;
   }
+  /* the sink logits' gradient, rows in order: dsigma_h = -sum_i e^(sigma_h - lse_ih) delta_ih */
+  if (sinks && dsinks) {
+    for (int h = 0; h < H; ++h) {
+      double acc = 0.0;
+      for (int i = 0; i < N; ++i) {
+        const int64_t o = (int64_t)i * H + h;
+        acc -= exp(sinks[h] - lse[o]) * delta[o];
+      }
+      dsinks[h] = acc;
+    }
+  }
   if (dK && dV && J.nkeys > 0) {
     J.phase = 2;
     J.nitems = Hkv * ((J.nkeys + RB - 1) / RB);
@@ -455,7 +509,22 @@ int oracle_fa_back(const float* q, const uint8_t* k, int k_type, const uint8_t* 
                    const int64_t* dkv_keys, int n_dkv_keys, double* lse, double* delta, double* dQ, double* dK,
                    double* dV, int nthreads) {
   return run_oracle(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal, dq_rows,
-                    n_dq_rows, dkv_keys, n_dkv_keys, lse, delta, dQ, dK, dV, NULL, nthreads);
+                    n_dq_rows, dkv_keys, n_dkv_keys, lse, delta, dQ, dK, dV, NULL, NULL, 0.0, NULL, NULL, nthreads);
+}
+
+/*
+ * oracle_fa_back with the extensions of the header comment: alibi [H] slopes or NULL, softcap
+ * c > 0 or 0, sinks [H] logits or NULL, and dsinks [H] (written when sinks and dsinks are given).
+ */
+int oracle_fa_back_ext(const float* q, const uint8_t* k, int k_type, const uint8_t* v, int v_type,
+                       const uint16_t* mask, int mask_heads, const float* dO, double scale, int N, int M, int H,
+                       int Hkv, int D, int Dv, int causal, const int64_t* dq_rows, int n_dq_rows,
+                       const int64_t* dkv_keys, int n_dkv_keys, double* lse, double* delta, double* dQ, double* dK,
+                       double* dV, const double* alibi, double softcap, const double* sinks, double* dsinks,
+                       int nthreads) {
+  return run_oracle(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal, dq_rows,
+                    n_dq_rows, dkv_keys, n_dkv_keys, lse, delta, dQ, dK, dV, NULL, alibi, softcap, sinks, dsinks,
+                    nthreads);
 }
 
 /*
@@ -470,7 +539,8 @@ int oracle_fa_forward(const float* q, const uint8_t* k, int k_type, const uint8_
   double* delta = (double*)malloc(sizeof(double) * ((size_t)N * H + 1));
   int rc = (!dO || !delta) ? 2
                            : run_oracle(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv,
-                                        causal, NULL, 0, NULL, 0, lse, delta, NULL, NULL, NULL, O, nthreads);
+                                        causal, NULL, 0, NULL, 0, lse, delta, NULL, NULL, NULL, O, NULL, 0.0, NULL,
+                                        NULL, nthreads);
   free(dO);
   free(delta);
   return rc;

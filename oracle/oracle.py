@@ -65,6 +65,13 @@ def _declare(L):
         + [ctypes.c_int] * 7
         + [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
         + [ctypes.c_void_p] * 5 + [ctypes.c_int])
+    L.oracle_fa_back_ext.restype = ctypes.c_int
+    L.oracle_fa_back_ext.argtypes = (
+        [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+         ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_double]
+        + [ctypes.c_int] * 7
+        + [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
+        + [ctypes.c_void_p] * 5 + [ctypes.c_void_p, ctypes.c_double, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int])
     L.oracle_fa_forward.restype = ctypes.c_int
     L.oracle_fa_forward.argtypes = (
         [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
@@ -103,7 +110,9 @@ def fa_back(p, dq_rows: Optional[Sequence[int]] = None, dkv_keys: Optional[Seque
     """Run the oracle on a synth.Problem.
 
     Returns float64 arrays: lse, delta [N][H]; dQ [n_dq][H][D];
-    dK [n_keys][Hkv][D]; dV [n_keys][Hkv][Dv].
+    dK [n_keys][Hkv][D]; dV [n_keys][Hkv][Dv]; with the problem's optional
+    extensions (ALiBi slopes, soft-cap, sink logits) also dsinks [H] when it
+    has sink logits.
     """
     L = lib if lib is not None else _load()
     N, M, H, Hkv, D, Dv = p.N, p.M, p.H, p.Hkv, p.D, p.Dv
@@ -121,13 +130,26 @@ def fa_back(p, dq_rows: Optional[Sequence[int]] = None, dkv_keys: Optional[Seque
     dQ = np.empty((nq, H, D), dtype=np.float64) if want_dq else None
     dK = np.empty((nk, Hkv, D), dtype=np.float64) if want_dkv else None
     dV = np.empty((nk, Hkv, Dv), dtype=np.float64) if want_dkv else None
-    rc = L.oracle_fa_back(_ptr(q), _ptr(k), p.k_type, _ptr(v), p.v_type, _ptr(mask), p.mask_heads if mask is not None else 0,
-                          _ptr(dO), float(p.scale), N, M, H, Hkv, D, Dv, int(p.causal),
-                          _ptr(rows), 0 if rows is None else rows.size, _ptr(keys), 0 if keys is None else keys.size,
-                          _ptr(lse), _ptr(delta), _ptr(dQ), _ptr(dK), _ptr(dV), int(nthreads))
+    alibi = getattr(p, "alibi", None)
+    softcap = float(getattr(p, "softcap", 0.0) or 0.0)
+    sinks = getattr(p, "sinks", None)
+    common = [_ptr(q), _ptr(k), p.k_type, _ptr(v), p.v_type, _ptr(mask), p.mask_heads if mask is not None else 0,
+              _ptr(dO), float(p.scale), N, M, H, Hkv, D, Dv, int(p.causal),
+              _ptr(rows), 0 if rows is None else rows.size, _ptr(keys), 0 if keys is None else keys.size,
+              _ptr(lse), _ptr(delta), _ptr(dQ), _ptr(dK), _ptr(dV)]
+    out = {"lse": lse, "delta": delta, "dQ": dQ, "dK": dK, "dV": dV}
+    if alibi is None and softcap == 0.0 and sinks is None:
+        rc = L.oracle_fa_back(*common, int(nthreads))
+    else:
+        al = None if alibi is None else np.ascontiguousarray(alibi, dtype=np.float64)
+        sk = None if sinks is None else np.ascontiguousarray(sinks, dtype=np.float64)
+        ds = None if sinks is None else np.empty(H, dtype=np.float64)
+        rc = L.oracle_fa_back_ext(*common, _ptr(al), softcap, _ptr(sk), _ptr(ds), int(nthreads))
+        if ds is not None:
+            out["dsinks"] = ds
     if rc:
         raise RuntimeError("oracle_fa_back failed with code %d" % rc)
-    return {"lse": lse, "delta": delta, "dQ": dQ, "dK": dK, "dV": dV}
+    return out
 
 
 def fa_forward(p, nthreads: int = 0, lib=None) -> dict:

@@ -196,6 +196,14 @@ class Problem:
     mask: Optional[np.ndarray] = None
     mask_heads: int = 0
     meta: dict = field(default_factory=dict)
+    # optional extensions (none by default): ALiBi slopes [H], soft-cap c (0 = none), sink logits [H]
+    alibi: Optional[np.ndarray] = None
+    softcap: float = 0.0
+    sinks: Optional[np.ndarray] = None
+
+    @property
+    def has_ext(self) -> bool:
+        return self.alibi is not None or self.softcap > 0 or self.sinks is not None
 
     @property
     def G(self) -> int:
@@ -260,7 +268,8 @@ def make_problem(name: str = "custom", *, N: int, M: int, H: int, Hkv: int, D: i
                  scale: Optional[float] = None, mask: Optional[str] = None, mask_p: float = 0.1,
                  full_rows: int = 0, mask_heads: int = 0, v_offset: float = 0.0, v_sigma: float = 1.0,
                  do_sigma: float = 1.0, q_sigma: float = 1.0, k_sigma: float = 1.0,
-                 row_decades: float = 0.0) -> Problem:
+                 row_decades: float = 0.0, alibi: bool = False, softcap: float = 0.0,
+                 sinks: Optional[float] = None) -> Problem:
     """Build a seeded problem.
 
     mask: None, "random" (entries -inf with probability mask_p, else 0, plus
@@ -268,6 +277,8 @@ def make_problem(name: str = "custom", *, N: int, M: int, H: int, Hkv: int, D: i
     (entries uniform in [-2, 0), plus the same -inf pattern).
     row_decades: when > 0, every (i, h) row of Q and of dO is multiplied by its own
     10**u, u uniform in [-row_decades, row_decades] (per-row dynamic range).
+    alibi: ALiBi slopes 2^(-8 (h+1) / H) per query head; softcap: the soft-cap c (0 = none);
+    sinks: when given, sink logits sinks * N(0,1) + 1 per query head.
     """
     kt, vt = _type(k_type), _type(v_type)
     if scale is None:
@@ -301,8 +312,11 @@ def make_problem(name: str = "custom", *, N: int, M: int, H: int, Hkv: int, D: i
             rows = sample_indices(seed, S_ROWS, N, full_rows)
             m[:, rows, :] = F16_NEG_INF
             meta["full_rows"] = rows
+    slopes = (2.0 ** (-8.0 * (np.arange(H) + 1) / H)).astype(np.float32) if alibi else None
+    sink = (1.0 + sinks * normal(seed, S_ROWS + 12, H)).astype(np.float32) if sinks is not None else None
     return Problem(name=name, N=N, M=M, H=H, Hkv=Hkv, D=D, Dv=Dv, k_type=kt, v_type=vt, causal=bool(causal),
-                   scale=float(scale), q=q, k=k, v=v, dO=dO, mask=m, mask_heads=hm, meta=meta)
+                   scale=float(scale), q=q, k=k, v=v, dO=dO, mask=m, mask_heads=hm, meta=meta, alibi=slopes,
+                   softcap=float(softcap), sinks=sink)
 
 
 def from_config(name: str, **over) -> Problem:

@@ -19,8 +19,8 @@ SRC = os.path.join(os.path.dirname(orc.__file__), "fa_oracle.c")
 MUTATIONS = {
     "gqa_index_in_dq": ("const double* k = J->Kh + ((int64_t)j * Hkv + (h / G)) * D;",
                         "const double* k = J->Kh + ((int64_t)j * Hkv + (h % Hkv)) * D;"),
-    "mask_term_dropped": ("s[j] += mv;", "s[j] += 0.0 * mv;"),
-    "ds_sign": ("const double ds = p * (dp[j] - delta);", "const double ds = p * (dp[j] + delta);"),
+    "mask_term_dropped": ("  s += mv;", "  s += 0.0 * mv;"),
+    "ds_sign": ("const double ds = p * (dp[j] - delta) * fac[j];", "const double ds = p * (dp[j] + delta) * fac[j];"),
     "causal_off_by_one": ("if (J->causal && (int64_t)j > (int64_t)J->M - J->N + i) return 0;",
                           "if (J->causal && (int64_t)j >= (int64_t)J->M - J->N + i) return 0;"),
     "dk_scale_dropped": ("dk[c] += J->scale * ds * q[c];", "dk[c] += ds * q[c];"),
@@ -32,6 +32,18 @@ MUTATIONS = {
                             "for (int t = 0; t < RB; ++t) acc2[t] += oc * (kt + (vc - vt))[t];"),
     "q8_scale_ignored": ("out[32 * b + t] = (double)(int8_t)blk[2 + t] * d;",
                          "out[32 * b + t] = (double)(int8_t)blk[2 + t] * 0.01;"),
+}
+
+# mistakes in the extensions, caught by the extension pin (ALiBi, soft-cap and sinks together)
+EXT_MUTATIONS = {
+    "softcap_derivative_dropped": ("*fac = 1.0 - t * t;", "*fac = 1.0;"),
+    "alibi_sign": ("s += J->alibi[h] * ((double)j - ((double)J->M - J->N + i));",
+                   "s -= J->alibi[h] * ((double)j - ((double)J->M - J->N + i));"),
+    "alibi_position_from_row_start": ("s += J->alibi[h] * ((double)j - ((double)J->M - J->N + i));",
+                                      "s += J->alibi[h] * ((double)j - (double)i);"),
+    "sink_not_in_denominator": ("if (J->sinks) sum += exp(sink - mx);", "if (J->sinks) sum += 0.0;"),
+    "sink_gradient_sign": ("acc -= exp(sinks[h] - lse[o]) * delta[o];", "acc += exp(sinks[h] - lse[o]) * delta[o];"),
+    "softcap_inside_scale": ("const double t = tanh(raw / J->softcap);", "const double t = tanh(raw);"),
 }
 
 
@@ -87,3 +99,24 @@ def test_planted_mistake_fails_the_golden_fixtures(tmp_path, name):
         assert lib.oracle_dequant(raw.ctypes.data, t, 1, 32, out.ctypes.data) == 0
         worst = max(worst, float(np.max(np.abs(out[0] - np.array(golden_io.vector(blocks[block]["values"]))))))
     assert worst > 0.1, (name, worst)
+
+
+@pytest.fixture(scope="module")
+def ext_problem():
+    return synth.make_problem("mutx", N=9, M=33, H=4, Hkv=2, D=64, Dv=32, k_type="q4_0", v_type="q8_0",
+                              mask="finite", mask_p=0.2, mask_heads=4, causal=True, alibi=True, softcap=2.0,
+                              sinks=0.5, seed=78)
+
+
+@pytest.mark.parametrize("name", sorted(EXT_MUTATIONS))
+def test_planted_extension_mistake_is_caught(ext_problem, tmp_path, name):
+    old, new = EXT_MUTATIONS[name]
+    text = open(SRC).read()
+    assert text.count(old) == 1, name
+    src = tmp_path / f"mutx_{name}.c"
+    src.write_text(text.replace(old, new))
+    lib = orc.load(orc.compile_source(str(src), str(tmp_path / f"libx_{name}.so")))
+    got = orc.fa_back(ext_problem, lib=lib)
+    ref = torch_reference(ext_problem)
+    worst = max(rel_err(got[k], ref[k]) for k in ("lse", "delta", "dQ", "dK", "dV", "dsinks"))
+    assert worst > 1e-6, (name, worst)

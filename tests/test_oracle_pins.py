@@ -37,7 +37,9 @@ def np_decode(raw: np.ndarray, t: int, D: int) -> np.ndarray:
 
 
 def torch_reference(p, khat=None, vhat=None):
-    """float64 autograd of L = sum(dO * softmax(scale*QK^T + mask) V)."""
+    """float64 autograd of L = sum(dO * softmax(scale*QK^T + mask) V), with the problem's optional
+    soft-cap (c tanh(x / c) of the scaled product), ALiBi bias m_h (j - (M - N + i)) and sink
+    logits (one more softmax column per row whose value is zero)."""
     N, M, H, Hkv = p.N, p.M, p.H, p.Hkv
     if khat is None:
         khat = np_decode(p.k, p.k_type, p.D)
@@ -51,19 +53,30 @@ def torch_reference(p, khat=None, vhat=None):
     kk = k.repeat_interleave(G, dim=1)
     vv = v.repeat_interleave(G, dim=1)
     s = torch.einsum("nhd,mhd->hnm", q, kk) * p.scale
+    if getattr(p, "softcap", 0.0):
+        s = p.softcap * torch.tanh(s / p.softcap)
     if p.mask is not None:
         s = s + torch.tensor(p.mask.view(np.float16).astype(np.float64))
+    i = torch.arange(N, dtype=torch.float64)[:, None]
+    j = torch.arange(M, dtype=torch.float64)[None, :]
+    if getattr(p, "alibi", None) is not None:
+        s = s + torch.tensor(p.alibi, dtype=torch.float64)[:, None, None] * (j - (M - N + i))
     if p.causal:
-        i = torch.arange(N)[:, None]
-        j = torch.arange(M)[None, :]
         s = s.masked_fill(j > M - N + i, float("-inf"))
+    sk = None
+    if getattr(p, "sinks", None) is not None:
+        sk = torch.tensor(p.sinks, dtype=torch.float64, requires_grad=True)
+        s = torch.cat([s, sk[:, None, None].expand(H, N, 1)], dim=-1)
     lse = torch.logsumexp(s, dim=-1).T.contiguous()
-    pr = torch.softmax(s, dim=-1)
+    pr = torch.softmax(s, dim=-1)[..., :M]
     o = torch.einsum("hnm,mhd->nhd", pr, vv)
     (o * dO).sum().backward()
     delta = (o * dO).sum(-1)
-    return {"lse": lse.detach().numpy(), "delta": delta.detach().numpy(), "dQ": q.grad.numpy(),
-            "dK": k.grad.numpy(), "dV": v.grad.numpy(), "O": o.detach().numpy()}
+    out = {"lse": lse.detach().numpy(), "delta": delta.detach().numpy(), "dQ": q.grad.numpy(),
+           "dK": k.grad.numpy(), "dV": v.grad.numpy(), "O": o.detach().numpy()}
+    if sk is not None:
+        out["dsinks"] = sk.grad.numpy()
+    return out
 
 
 def rel_err(a, b):
@@ -147,6 +160,60 @@ def test_oracle_matches_torch_autograd(oracle_lib, case):
     got = oracle_lib.fa_back(p)
     for name in ("lse", "delta", "dQ", "dK", "dV"):
         assert rel_err(got[name], ref[name]) < 1e-12, name
+
+
+# the extensions (ALiBi, soft-capping, sink logits), alone and together, against the same
+# autograd route
+EXT_CASES = [
+    dict(N=5, M=9, H=2, Hkv=2, D=8, Dv=8, k_type="f32", v_type="f32", alibi=True),
+    dict(N=6, M=11, H=4, Hkv=2, D=16, Dv=8, k_type="f16", v_type="f16", causal=True, softcap=1.5),
+    dict(N=4, M=13, H=2, Hkv=1, D=32, Dv=32, k_type="q8_0", v_type="q8_0", sinks=1.0),
+    dict(N=9, M=33, H=4, Hkv=2, D=64, Dv=32, k_type="q4_0", v_type="q8_0", mask="finite", mask_p=0.2,
+         mask_heads=4, causal=True, alibi=True, softcap=2.0, sinks=0.5),
+]
+
+
+@pytest.mark.parametrize("case", range(len(EXT_CASES)))
+def test_extensions_match_torch_autograd(oracle_lib, case):
+    p = synth.make_problem(f"ext{case}", seed=320 + case, **EXT_CASES[case])
+    ref = torch_reference(p)
+    got = oracle_lib.fa_back(p)
+    names = ["lse", "delta", "dQ", "dK", "dV"] + (["dsinks"] if p.sinks is not None else [])
+    for name in names:
+        assert rel_err(got[name], ref[name]) < 1e-11, name
+
+
+def test_extensions_switched_off_equal_the_plain_oracle(oracle_lib):
+    """Zero ALiBi slopes and a sink logit of -1e300 change nothing; a soft-cap of 1e7 changes the
+    logits by less than x^3 / (3 c^2)."""
+    base = dict(N=7, M=20, H=4, Hkv=2, D=32, Dv=32, k_type="q8_0", v_type="q8_0", causal=True, seed=330)
+    p = synth.make_problem("plain", **base)
+    ref = oracle_lib.fa_back(p)
+    q = synth.make_problem("off", alibi=True, sinks=1.0, **base)
+    q.alibi = np.zeros(p.H, dtype=np.float32)
+    q.sinks = np.full(p.H, -1e300)
+    got = oracle_lib.fa_back(q)
+    for name in ("lse", "delta", "dQ", "dK", "dV"):
+        assert np.array_equal(got[name], ref[name]), name
+    assert np.all(got["dsinks"] == 0.0)
+    r = synth.make_problem("cap", softcap=1e7, **base)
+    got = oracle_lib.fa_back(r)
+    for name in ("lse", "delta", "dQ", "dK", "dV"):
+        assert rel_err(got[name], ref[name]) < 1e-12, name
+
+
+def test_sink_with_a_fully_masked_row(oracle_lib):
+    """A row without an allowed key: with a sink its lse is the sink logit, its delta, dQ row and
+    share of the sink's gradient are zero."""
+    p = synth.make_problem("sinkmask", N=6, M=15, H=2, Hkv=1, D=16, Dv=16, k_type="f32", v_type="f32",
+                           mask="random", mask_p=0.1, full_rows=2, mask_heads=2, sinks=1.0, seed=331)
+    got = oracle_lib.fa_back(p)
+    rows = p.meta["full_rows"]
+    for h in range(p.H):
+        assert np.array_equal(got["lse"][rows, h], np.full(len(rows), float(p.sinks[h])))
+    assert np.all(got["delta"][rows] == 0.0) and np.all(got["dQ"][rows] == 0.0)
+    ref = torch_reference(p)
+    assert rel_err(got["dsinks"], ref["dsinks"]) < 1e-11
 
 
 def test_delta_is_rowsum_dO_times_O(oracle_lib):
