@@ -50,6 +50,9 @@ def lib():
     L.fa_back_plan_info.argtypes = [i] * 6 + [sz, vp, vp, vp]
     L.fa_back.restype = i
     L.fa_back.argtypes = [vp, vp, i, vp, i, vp, i, vp, f, i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.fa_back_ext.restype = i
+    L.fa_back_ext.argtypes = [vp, vp, i, vp, i, vp, i, vp, f, i, i, i, i, i, i, i, vp, f, vp, vp, vp, vp, vp, vp, vp,
+                              vp, sz, vp]
     L.fa_back_with_stats.restype = i
     L.fa_back_with_stats.argtypes = [vp, vp, i, vp, i, vp, i, vp, vp, vp, f, i, i, i, i, i, i, i, vp, vp, vp, vp, sz,
                                      vp]
@@ -108,6 +111,15 @@ def fa_back(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, 
                              int(causal), dQ, dK, dV, lse, delta, workspace, workspace_bytes, stream))
 
 
+def fa_back_ext(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal,
+                alibi_slopes, softcap, sinks, dsinks, dQ, dK, dV, lse, delta, workspace, workspace_bytes,
+                stream) -> int:
+    """fa_back with the score extensions (ALiBi slopes, soft cap, sink logits); see the header."""
+    return int(lib().fa_back_ext(q, k, k_type, v, v_type, mask, mask_heads, dO, float(scale), N, M, H, Hkv, D, Dv,
+                                 int(causal), alibi_slopes, float(softcap), sinks, dsinks, dQ, dK, dV, lse, delta,
+                                 workspace, workspace_bytes, stream))
+
+
 def fa_back_with_stats(q, k, k_type, v, v_type, mask, mask_heads, dO, lse, delta, scale, N, M, H, Hkv, D, Dv,
                        causal, dQ, dK, dV, workspace, workspace_bytes, stream) -> int:
     return int(lib().fa_back_with_stats(q, k, k_type, v, v_type, mask, mask_heads, dO, lse, delta, float(scale), N,
@@ -158,7 +170,7 @@ def fa_back_profile(enable: bool) -> int:
     return int(lib().fa_back_profile(1 if enable else 0))
 
 
-def fa_back_profile_read(max_kernels: int = 16) -> dict:
+def fa_back_profile_read(max_kernels: int = 32) -> dict:
     """{kernel name: (summed ms, launches)} of the recorded fa_back calls; clears the record."""
     ms = (ctypes.c_float * max_kernels)()
     cnt = (ctypes.c_int * max_kernels)()

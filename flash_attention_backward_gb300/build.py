@@ -4,6 +4,7 @@ from __future__ import annotations
 import os
 import subprocess
 import sys
+import tempfile
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
@@ -37,20 +38,35 @@ def nvcc() -> str:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Build libfa_back.so next to this file; returns its path."""
+    """Build libfa_back.so next to this file; returns its path.  The translation units compile in
+    parallel (one nvcc per file, objects in a temporary folder), then one link."""
     if not force and up_to_date():
         return LIB
     tmp = LIB + ".tmp%d" % os.getpid()
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-           "-I", INCLUDE, *sources(), "-o", tmp]
+    flags = [*ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
     if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
-    if r.returncode != 0:
-        sys.stderr.write(r.stdout)
-        raise RuntimeError("nvcc failed building libfa_back.so")
-    if verbose:
-        sys.stderr.write(r.stdout)
+        flags.insert(0, "-Xptxas=-v")
+    with tempfile.TemporaryDirectory(prefix="fa_back_build_") as obj_dir:
+        jobs = []
+        for src in sources():
+            obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
+            cmd = [nvcc(), *flags, "-c", src, "-o", obj]
+            jobs.append((obj, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
+        failed = False
+        for obj, proc in jobs:
+            out, _ = proc.communicate()
+            if proc.returncode != 0:
+                failed = True
+                sys.stderr.write(out)
+            elif verbose:
+                sys.stderr.write(out)
+        if failed:
+            raise RuntimeError("nvcc failed building libfa_back.so")
+        r = subprocess.run([nvcc(), *ARCH, "-shared", *[o for o, _ in jobs], "-o", tmp], stdout=subprocess.PIPE,
+                           stderr=subprocess.STDOUT, text=True)
+        if r.returncode != 0:
+            sys.stderr.write(r.stdout)
+            raise RuntimeError("nvcc failed linking libfa_back.so")
     os.replace(tmp, LIB)
     return LIB
 

@@ -38,5 +38,6 @@ extern "C" fa_status fa_back_noalloc(const float* q, const void* k, int k_type, 
   void* scratch = scratch_here(&err);
   if (!scratch) return FA_ERR_CUDA;
   return fab_back_capped(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal, dQ, dK,
-                         dV, lse, delta, scratch, kScratchBytes, stream, kScratchBytes, nullptr, nullptr, nullptr);
+                         dV, lse, delta, scratch, kScratchBytes, stream, kScratchBytes, nullptr, nullptr, nullptr,
+                         nullptr);
 }

@@ -46,6 +46,9 @@ struct Stats {
   float amax[4], norm2[4];
   float rnorm, ramax;
   int lamr_exp;  // largest exponent of the per-row dS multipliers (raised by k_convert)
+  // score extensions (ext_scores): the soft cap's argument u = cu * (Q.K accumulator) =
+  // scale q.k / c and its height c log2(e); both 0 without a cap
+  float cu, cap2;
 };
 
 // The dS stored for the dQ product takes each row's own multiplier only when some row's exceeds
@@ -53,7 +56,7 @@ struct Stats {
 // than 2^12 below the common scale's 2^15, so its values stay far inside binary16's normal range
 // and keep its relative precision; the per-row copy costs the dK/dV pass extra shared-memory
 // traffic, so typical inputs (rows of similar size) skip it.
-__host__ __device__ constexpr int kRowScaleGap = 12;
+constexpr int kRowScaleGap = 12;
 __device__ __forceinline__ bool rows_need_own_scale(const Stats& st) {
   return st.lamr_exp - ilogbf(st.lam) > kRowScaleGap;
 }
@@ -107,6 +110,12 @@ struct Params {
   int raw_depth;       // entries of the K ring (2..8)
   int raw_depth_v;     // entries of the V ring (1..8)
   int* err;
+  // score extensions (fa_back_ext); all null / 0 for the plain operation
+  float softcap;       // c > 0: the score x = scale q.k becomes c tanh(x / c); 0: none
+  const float* alibi;  // [H] slopes: bias slope_h (j - (M - N + i)) added after the mask, or null
+  const float* sinks;  // [H] sink logits joining every row's softmax denominator, or null
+  float* dsinks;       // [H] gradient of the sink logits (with sinks), or null
+  float* sg;           // [Hkv][R] per-row sink-gradient terms, summed per head by k_sink_grad
 };
 
 __host__ __device__ constexpr int pow2_at_least(int x) {
@@ -392,6 +401,52 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// ---- score extensions: soft cap, ALiBi bias (and, in k_lse_merge, sink logits)
+//
+// Log2-domain exponents of one 32-key chunk (keys j0 .. j0+31, row r of KV head hk) with the
+// extensions applied in this order: x = scale q.k (the Q.K accumulator s[n] times c2), the soft
+// cap c tanh(x / c) (when st.cap2 > 0), the mask, the ALiBi bias slope_h (j - (M - N + i)), and
+// the row offset t2off.  Masked keys get -inf.  tanh(u) = sign(u) (1 - 2w) with w = 1 / (1 +
+// e^{2|u|}) (the exponential form of tanh), whose derivative is 1 - tanh^2 = 4 w (1 - w); computed
+// this way the derivative keeps its relative precision where tanh is close to one.
+//   FAC 0: exponents only (LSE/D passes);
+//   FAC 1: log2 of the derivative added to the exponent (dQ passes: the exponential is then
+//          lam p (1 - tanh^2), the multiplier of (dP - delta) in dS);
+//   FAC 2: dp[n] replaced by (dp[n] - dl)(1 - tanh^2) (the dK/dV pass, which needs p itself for
+//          dV; it then subtracts 0 instead of dl).
+// Only the passes' EXT variants contain it; the plain operation's kernels are built without.
+template <int FAC>
+__device__ __forceinline__ void ext_scores(float* s, float* dp, int j0, int r, int hk, float t2off, float dl,
+                                           long jlast, const uint16_t* mrow, const Stats& st, const float* slopes,
+                                           int G, int diag0) {
+  const int i = r / G, h = hk * G + r % G;
+  const float sl2 = slopes ? __ldg(slopes + h) * kLog2e : 0.f;
+  const long jd = (long)diag0 + i;  // the query's position on the key axis
+#pragma unroll
+  for (int n = 0; n < 32; ++n) {
+    const int j = j0 + n;
+    bool ok = (long)j <= jlast;
+    float mv = 0.f;
+    if (ok && mrow) {
+      mv = h2f(__ldg(reinterpret_cast<const unsigned short*>(mrow) + j));
+      ok = !(mv == -CUDART_INF_F);
+    }
+    float y, f = 1.f;
+    if (st.cap2 > 0.f) {
+      const float u = s[n] * st.cu;
+      const float w = __frcp_rn(1.f + ex2(fabsf(u) * (2.f * kLog2e)));
+      y = st.cap2 * copysignf(1.f - 2.f * w, u);
+      f = 4.f * w * (1.f - w);
+    } else {
+      y = s[n] * st.c2;
+    }
+    float t = ok ? y + fmaf(mv, kLog2e, fmaf(sl2, (float)((long)j - jd), t2off)) : -CUDART_INF_F;
+    if (FAC == 1) t += __log2f(f);  // f = 0 (a saturated cap) gives -inf: no contribution
+    s[n] = t;
+    if (FAC == 2) dp[n] = ok ? (dp[n] - dl) * f : 0.f;
+  }
+}
+
 // ------------------------------------------------------------------------------------------------
 // statistics and packing
 
@@ -432,7 +487,7 @@ __device__ __forceinline__ void decode8_f(const uint8_t* row, int type, int c0, 
 
 // One warp per row of Q, dO, K^ or V^ (lane = 8 consecutive values): max |x| and max squared
 // row norm, reduced per block.
-__global__ void __launch_bounds__(256) k_row_stats(Params p) {
+static __global__ void __launch_bounds__(256) k_row_stats(Params p) {
   __shared__ float red[8][4][2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long nQ = (long)p.N * p.H, nK = (long)p.M * p.Hkv;
@@ -486,7 +541,7 @@ __global__ void __launch_bounds__(256) k_row_stats(Params p) {
     p.bstat[((size_t)blockIdx.x * 4 + t) * 2 + w] = m;
   }
 }
-__global__ void __launch_bounds__(256) k_vsum(Params p) {
+static __global__ void __launch_bounds__(256) k_vsum(Params p) {
   // block = (chunk, hk); its eight warps take every eighth key of the chunk and their sums are
   // added in warp order, so the result does not depend on timing
   __shared__ float part[8][256];
@@ -526,7 +581,7 @@ __device__ __forceinline__ float pow2_scale_for(float amax, int target_exp) {
   return ldexpf(1.f, s);
 }
 
-__global__ void __launch_bounds__(1024) k_finalize(Params p) {
+static __global__ void __launch_bounds__(1024) k_finalize(Params p) {
   __shared__ float am[4], nm[4];
   __shared__ float rn2[1024], ram[1024];
   const int tid = threadIdx.x;
@@ -613,13 +668,15 @@ __global__ void __launch_bounds__(1024) k_finalize(Params p) {
     s.dv_fac = 1.f / (s.sP * s.sdO);
     s.delta_fac = 1.f / (s.sdO * s.sV);
     s.lamr_exp = ilogbf(s.lam);
+    s.cu = p.softcap > 0.f ? p.scale / (p.softcap * s.sQ * s.sK) : 0.f;
+    s.cap2 = p.softcap > 0.f ? p.softcap * kLog2e : 0.f;
     *p.st = s;
   }
 }
 
 // One warp per (i, h): binary16 rows of Q and dO (row r = i*G + g of head hk), dO_i . r and the
 // row's dS multiplier for the dQ product.
-__global__ void __launch_bounds__(256) k_convert(Params p) {
+static __global__ void __launch_bounds__(256) k_convert(Params p) {
   __shared__ int s_lexp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) s_lexp = INT_MIN;
@@ -670,7 +727,7 @@ __global__ void __launch_bounds__(256) k_convert(Params p) {
 // row-pass variants see the same operands.  Thread = 8 values; cache rows are read in order.
 // The copies are panel-major, [hk][64-column panel][key][64]: the TMA box of one operand panel
 // (BK keys x 64 columns) is then one contiguous block.
-__global__ void __launch_bounds__(256) k_predecode(Params p) {
+static __global__ void __launch_bounds__(256) k_predecode(Params p) {
   const float sK = p.st->sK, sV = p.st->sV;
   const long uk = (long)p.M * p.Hkv * (p.D / 8), uv = (long)p.M * p.Hkv * (p.Dv / 8);
   for (long u = (long)blockIdx.x * 256 + threadIdx.x; u < uk + uv; u += (long)gridDim.x * 256) {
@@ -797,8 +854,8 @@ __device__ __forceinline__ void drain_loads(uint64_t* full, int nst, int issued,
     mbar_wait_until(&full[n % nst], (uint32_t)(n / nst) & 1u, deadline);
 }
 
-template <int D, int Dv, int BK, int MODE>
-__global__ void __launch_bounds__(Rows2Cfg<D, Dv, BK, MODE>::NT, 1)
+template <int D, int Dv, int BK, int MODE, bool EXT = false>
+static __global__ void __launch_bounds__(Rows2Cfg<D, Dv, BK, MODE>::NT, 1)
     k_rows2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
             const __grid_constant__ CUtensorMap tmV, Params p) {
   using C = Rows2Cfg<D, Dv, BK, MODE>;
@@ -1151,7 +1208,12 @@ __global__ void __launch_bounds__(Rows2Cfg<D, Dv, BK, MODE>::NT, 1)
         const bool full = mrow == nullptr && (long)(j0 + col0 + 31) <= jlast;
         float t2[32];  // log2-domain scores (dQ pass: already minus lse, plus log2(lam))
         const float t2off = MODE == 1 ? nlse2 : 0.f;
-        if (full) {
+        if constexpr (EXT) {
+#pragma unroll
+          for (int n = 0; n < 32; ++n) t2[n] = s[n];
+          ext_scores<MODE == 1 ? 1 : 0>(t2, nullptr, j0 + col0, r, hk, t2off, 0.f, jlast, mrow, st, p.alibi, G,
+                                        p.M - p.N);
+        } else if (full) {
 #pragma unroll
           for (int n = 0; n < 32; ++n) t2[n] = fmaf(s[n], c2, t2off);
         } else {
@@ -1368,8 +1430,8 @@ enum {
 };
 static_assert(8 * R3_COUNT + 8 <= 512, "barrier area");
 
-template <int D, int Dv, int BK, int MODE>
-__global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
+template <int D, int Dv, int BK, int MODE, bool EXT = false>
+static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
     k_rows3(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
             const __grid_constant__ CUtensorMap tmV, Params p) {
   using C = Rows3Cfg<D, Dv, BK, MODE>;
@@ -1608,7 +1670,10 @@ __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[R3_S_FREE]);
       // log2-domain scores (dQ pass: already minus lse, plus log2(lam)); masked keys -> -inf
-      if (mrow == nullptr && (long)(j0 + col0 + 31) <= jlast) {
+      if constexpr (EXT) {
+        ext_scores<MODE == 1 ? 1 : 0>(s, nullptr, j0 + col0, r, hk, t2off, 0.f, jlast, mrow, st, p.alibi, G,
+                                      p.M - p.N);
+      } else if (mrow == nullptr && (long)(j0 + col0 + 31) <= jlast) {
 #pragma unroll
         for (int n = 0; n < 32; ++n) s[n] = fmaf(s[n], c2, t2off);
       } else {
@@ -1779,7 +1844,13 @@ __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
 }
 
 // Merge the split partials: lse and delta outputs plus the gradient passes' per-row values.
-__global__ void __launch_bounds__(256) k_lse_merge(Params p) {
+// With sink logits sigma_h, the sink joins the denominator as one more term e^sigma that has no
+// value row: lse = log(e^sigma + sum_j e^s_j), and the keys' weights then sum to 1 - p_sink with
+// p_sink = e^(sigma - lse).  delta = sum_j p_j dP_j is still the keys' sum, but the shift by r' no
+// longer cancels in it: the shifted delta the gradient passes subtract is
+//   delta - dO_i . r' = SD / L - p_sink dO_i . r'      (accumulator units: times sdO sV),
+// and the row's term of the sink gradient is -p_sink delta (summed per head by k_sink_grad).
+static __global__ void __launch_bounds__(256) k_lse_merge(Params p) {
   const long idx = (long)blockIdx.x * 256 + threadIdx.x;
   if (idx >= (long)p.Hkv * p.R) return;
   const int hk = (int)(idx / p.R), r = (int)(idx % p.R);
@@ -1797,26 +1868,67 @@ __global__ void __launch_bounds__(256) k_lse_merge(Params p) {
   }
   const int i = r / p.G, h = hk * p.G + r % p.G;
   const Stats* st = p.st;
+  float sink2 = -CUDART_INF_F;  // the sink logit in log2 units
+  if (p.sinks) {
+    sink2 = p.sinks[h] * kLog2e;
+    const float mm = fmaxf(m2, sink2);
+    const float f = m2 > -CUDART_INF_F ? exp2f(m2 - mm) : 0.f;
+    l = fmaf(l, f, exp2f(sink2 - mm));
+    sd *= f;
+    m2 = mm;
+  }
   if (l > 0.f) {
     const float lse2 = m2 + log2f(l);
-    const float dl = sd / l;
+    const float ps = p.sinks ? exp2f(sink2 - lse2) : 0.f;
+    const float dl = sd / l - ps * p.dOr[idx] * (st->sdO * st->sV);
+    const float delta = dl * st->delta_fac + p.dOr[idx];
     p.lse2[idx] = lse2;
     p.dlt[idx] = dl;
     p.lse[(size_t)i * p.H + h] = lse2 * kLn2;
-    if (p.delta) p.delta[(size_t)i * p.H + h] = dl * st->delta_fac + p.dOr[idx];
+    if (p.delta) p.delta[(size_t)i * p.H + h] = delta;
+    if (p.sg) p.sg[idx] = -ps * delta;
   } else {
     p.lse2[idx] = -CUDART_INF_F;
     p.dlt[idx] = 0.f;
     p.lse[(size_t)i * p.H + h] = -CUDART_INF_F;
     if (p.delta) p.delta[(size_t)i * p.H + h] = 0.f;
+    if (p.sg) p.sg[idx] = 0.f;
   }
+}
+
+// Gradient of the sink logits: dsinks_h = sum_i -p_sink(i, h) delta_ih, the per-row terms of
+// k_lse_merge summed in a fixed order (one block per head; thread t takes rows t, t + 256, ...
+// in order, in double, then a fixed tree over the threads), so the result is deterministic.
+static __global__ void __launch_bounds__(256) k_sink_grad(Params p) {
+  __shared__ double part[256];
+  const int h = blockIdx.x, hk = h / p.G, g = h % p.G;
+  double acc = 0.0;
+  for (int i = threadIdx.x; i < p.N; i += 256) acc += (double)p.sg[(size_t)hk * p.R + (size_t)i * p.G + g];
+  part[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if ((int)threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) p.dsinks[h] = (float)part[0];
+}
+
+// Fills the outputs of a problem without keys that has sink logits: every row's softmax holds the
+// sink alone, so lse = sigma_h, delta = 0 and dQ = 0 (filled by the caller), and dsinks = 0.
+static __global__ void k_sink_only(const float* sinks, float* lse, float* delta, float* dsinks, int N, int H) {
+  const long idx = (long)blockIdx.x * 256 + threadIdx.x;
+  if (idx < (long)N * H) {
+    lse[idx] = sinks[idx % H];
+    if (delta) delta[idx] = 0.f;
+  }
+  if (dsinks && idx < H) dsinks[idx] = 0.f;
 }
 
 // The per-row values of the gradient passes from a given lse and delta (instead of the LSE
 // pass): lse2 = lse / ln 2 and the shifted delta in accumulator units, (delta - dO_i . r) sdO sV
 // (the gradient passes take dP' - delta' with dP' = dO' . V', V' shifted by r).  A row whose lse
 // is -inf (or not finite) has no allowed key.
-__global__ void __launch_bounds__(256) k_stats_in(Params p) {
+static __global__ void __launch_bounds__(256) k_stats_in(Params p) {
   const long idx = (long)blockIdx.x * 256 + threadIdx.x;
   if (idx >= (long)p.Hkv * p.R) return;
   const int hk = (int)(idx / p.R), r = (int)(idx % p.R);
@@ -1834,7 +1946,7 @@ __global__ void __launch_bounds__(256) k_stats_in(Params p) {
 
 // O = sum of the forward O pass's split partials in split order, plus the V shift r for a row
 // with keys (its weights sum to one); 0 for a row without keys.
-__global__ void __launch_bounds__(256) k_o_reduce(Params p) {
+static __global__ void __launch_bounds__(256) k_o_reduce(Params p) {
   const long nv = (long)p.Hkv * p.R * (p.Dv / 4);
   const long idx = (long)blockIdx.x * 256 + threadIdx.x;
   if (idx >= nv) return;
@@ -1855,7 +1967,7 @@ __global__ void __launch_bounds__(256) k_o_reduce(Params p) {
 }
 
 // dQ = sum of the split partials, in split order.
-__global__ void __launch_bounds__(256) k_dq_reduce(Params p) {
+static __global__ void __launch_bounds__(256) k_dq_reduce(Params p) {
   const long nv = (long)p.Hkv * p.R * (p.D / 4);
   const long idx = (long)blockIdx.x * 256 + threadIdx.x;
   if (idx >= nv) return;
@@ -1928,8 +2040,8 @@ static_assert(8 * C_COUNT + 8 <= 256, "dK/dV pass barrier area");
 // on the device) first and returns at once unless it is the one that applies.  Separate variants
 // keep the copy's code out of the common one: built into one kernel behind a run-time branch, it
 // slowed the pass by about 5 % even where the branch was never taken.
-template <int D, int Dv, int BK, bool ROWCOPY>
-__global__ void __launch_bounds__(384, 1)
+template <int D, int Dv, int BK, bool ROWCOPY, bool EXT = false>
+static __global__ void __launch_bounds__(384, 1)
     k_cols2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
             const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmKd,
             const __grid_constant__ CUtensorMap tmVd, Params p) {
@@ -2125,6 +2237,7 @@ __global__ void __launch_bounds__(384, 1)
       mrow = p.mask ? p.mask + ((size_t)(h % p.Hm) * p.N + i) * p.M : nullptr;
     };
     float lse2 = 0.f, dl = 0.f, lr = 0.f;
+    float dls = 0.f;  // delta subtracted from dP in dS: the row's, or 0 where ext_scores has done it
     long jlast = -1;
     const uint16_t* mrow = nullptr;
     constexpr bool keep = ROWCOPY;
@@ -2132,7 +2245,7 @@ __global__ void __launch_bounds__(384, 1)
     auto ds_row = [&](const float* pv, const float* dpv, uint32_t* w) {
 #pragma unroll
       for (int x = 0; x < 32; x += 2)
-        w[x / 2] = h2_as_u32(__floats2half2_rn(pv[x] * (dpv[x] - dl) * lr, pv[x + 1] * (dpv[x + 1] - dl) * lr));
+        w[x / 2] = h2_as_u32(__floats2half2_rn(pv[x] * (dpv[x] - dls) * lr, pv[x + 1] * (dpv[x + 1] - dls) * lr));
     };
     // once the dV^T product of tile t has read P, the stored dS copy goes into the P panel
     auto put_ds_copy = [&](int t, int col0, const uint32_t* w, int nchunk) -> bool {
@@ -2158,6 +2271,8 @@ __global__ void __launch_bounds__(384, 1)
       const uint16_t* nmrow = nullptr;
       if (t + 1 < nq) row_stats(t + 1, nlse2, ndl, nlr, njlast, nmrow);
       const float nl = lse2 > -CUDART_INF_F ? lp - lse2 : -CUDART_INF_F;  // sP * p = 2^(t2 + nl); 0 on a dead row
+      const int rcur = (qt_begin + t) * 128 + row;
+      dls = EXT ? 0.f : dl;
       if (!wait(&bar[C_S_FULL], t & 1)) break;
       // the previous tile's P panel is free once its dV product (and the store of its dS copy) read it
       if (!wait(&bar[C_P_EMPTY], (t & 1) ^ 1)) break;
@@ -2165,8 +2280,11 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       // log2-domain exponents of one 32-key chunk; a fully visible chunk without a mask takes
       // no per-key tests
-      auto exponents = [&](int col0, float* v) {
-        if (mrow == nullptr && (long)(j0 + col0 + 31) <= jlast) {
+      // (with the score extensions, dP also becomes (dP - delta) times the soft cap's derivative)
+      auto exponents = [&](int col0, float* v, float* dpv) {
+        if constexpr (EXT) {
+          ext_scores<2>(v, dpv, j0 + col0, rcur, hk, nl, dl, jlast, mrow, st, p.alibi, G, p.M - p.N);
+        } else if (mrow == nullptr && (long)(j0 + col0 + 31) <= jlast) {
 #pragma unroll
           for (int x = 0; x < 32; ++x) v[x] = fmaf(v[x], c2, nl);
         } else {
@@ -2190,7 +2308,7 @@ __global__ void __launch_bounds__(384, 1)
         tmem_ld32(tbase + C::T_S + lane_off + col0, s);
         tmem_ld32(tbase + C::T_P + lane_off + col0, dp);
         tmem_ld_wait();
-        exponents(col0, s);
+        exponents(col0, s, dp);
 #pragma unroll
         for (int x = 0; x < 32; ++x) s[x] = ex2(s[x]);  // sP * p; 0 for masked keys and dead rows
 #pragma unroll
@@ -2204,7 +2322,7 @@ __global__ void __launch_bounds__(384, 1)
         uint32_t pd[16], pr[16];
 #pragma unroll
         for (int x = 0; x < 32; x += 2)
-          pd[x / 2] = h2_as_u32(__floats2half2_rn(s[x] * (dp[x] - dl) * lam, s[x + 1] * (dp[x + 1] - dl) * lam));
+          pd[x / 2] = h2_as_u32(__floats2half2_rn(s[x] * (dp[x] - dls) * lam, s[x + 1] * (dp[x + 1] - dls) * lam));
         if (keep) ds_row(s, dp, pr);
         // the previous tile's dS panel is free once its dK product (and its store) read it
         if (!wait(&bar[C_DS_EMPTY], (t & 1) ^ 1)) break;
@@ -2228,7 +2346,7 @@ __global__ void __launch_bounds__(384, 1)
           tmem_ld32(tbase + C::T_S + lane_off + col0, s);
           tmem_ld32(tbase + C::T_P + lane_off + col0, dp);
           tmem_ld_wait();
-          exponents(col0, s);
+          exponents(col0, s, dp);
 #pragma unroll
           for (int x = 0; x < 32; ++x) s[x] = ex2(s[x]);  // sP * p; 0 for masked keys and dead rows
           if (keep) ds_row(s, dp, pr + c / 2);
@@ -2240,7 +2358,7 @@ __global__ void __launch_bounds__(384, 1)
               const int x = g + n;
               const float p0 = s[x], p1 = s[x + 1];
               pp[n / 2] = h2_as_u32(__floats2half2_rn(p0, p1));
-              pd[n / 2] = h2_as_u32(__floats2half2_rn(p0 * (dp[x] - dl) * lam, p1 * (dp[x + 1] - dl) * lam));
+              pd[n / 2] = h2_as_u32(__floats2half2_rn(p0 * (dp[x] - dls) * lam, p1 * (dp[x + 1] - dls) * lam));
             }
             const uint32_t off = panel_off_u(128, row, col0 + g);
             sts_v4(sP_u + off, pp[0], pp[1], pp[2], pp[3]);
@@ -2322,7 +2440,7 @@ __global__ void __launch_bounds__(384, 1)
 
 // Failure-detection self-test: one thread waits on an mbarrier nothing arrives on, gives up
 // after limit_ns (the path every bounded wait of the backward takes) and records the timeout.
-__global__ void k_wait_selftest(int* err, unsigned long long limit_ns) {
+static __global__ void k_wait_selftest(int* err, unsigned long long limit_ns) {
   __shared__ uint64_t bar;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
@@ -2332,7 +2450,7 @@ __global__ void k_wait_selftest(int* err, unsigned long long limit_ns) {
 }
 
 // Fill kernel for degenerate shapes (a value into n floats).
-__global__ void k_fill(float* x, long n, float v) {
+static __global__ void k_fill(float* x, long n, float v) {
   const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx < n) x[idx] = v;
 }
@@ -2358,7 +2476,7 @@ struct GemmCfg {
 enum { G_FULL = 0, G_EMPTY = 6, G_ACC = 12, G_COUNT };
 
 template <int D, int BK>
-__global__ void __launch_bounds__(256, 1)
+static __global__ void __launch_bounds__(256, 1)
     k_dq_gemm(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmK, Params p) {
   using C = GemmCfg<D, BK>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];

@@ -95,7 +95,7 @@ enum {
 };
 static_assert(8 * L_COUNT + 8 <= 512, "barrier area");
 
-template <int D, int Dv>
+template <int D, int Dv, bool EXT = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LsePairCfg<D, Dv>::NT, 1)
     k_lse_pair(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, Params p) {
   using C = LsePairCfg<D, Dv>;
@@ -346,7 +346,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LsePairCfg<D, Dv>::N
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int k0 = j0 + col0 + 32 * c;
-        if (mrow == nullptr && (long)(k0 + 31) <= jlast) {
+        if constexpr (EXT) {
+          ext_scores<0>(e[c], nullptr, k0, r, hk, 0.f, 0.f, jlast, mrow, st, p.alibi, G, p.M - p.N);
+        } else if (mrow == nullptr && (long)(k0 + 31) <= jlast) {
 #pragma unroll
           for (int n = 0; n < 32; ++n) e[c][n] = e[c][n] * c2;
         } else {

@@ -130,6 +130,35 @@ fa_status fa_back_with_stats(const float* q, const void* k, int k_type, const vo
                              size_t workspace_bytes, void* stream);
 
 /*
+ * fa_back() with three score extensions that the operation above does not have.  The pull request
+ * this library follows lists ALiBi, soft-capping and sink gradients among the features it does
+ * not support and defines none of them; the definitions taken here are the usual ones:
+ *   x_ij   = scale * q_i . k^_j
+ *   s_ij   = c tanh(x_ij / c)    (softcap = c > 0: the logit soft-capping of the Gemma 2 models)
+ *            or x_ij             (softcap = 0)
+ *            + mask[h % Hm][i][j]
+ *            + alibi_slopes[h] * (j - (M - N + i))   (ALiBi, Press, Smith and Lewis, "Train Short,
+ *              Test Long": 0 on the causal diagonal, falling linearly with the distance to
+ *              earlier keys; M - N + i is query i's position on the key axis, as for causal)
+ *   lse_ih = log(exp(sinks[h]) + sum_{allowed j} exp(s_ij))   (a sink: one logit per head that
+ *            joins every row's softmax denominator and has no value row)
+ *   p_ij, delta_ih as in fa_back() with this lse (the keys' weights sum to 1 - exp(sinks[h] - lse))
+ *   dS_ij  = p_ij (dO_i . v^_j - delta_ih) (1 - tanh^2(x_ij / c))   (the last factor 1 without a cap)
+ *   dQ, dK, dV as in fa_back() with this dS;  dsinks[h] = -sum_i exp(sinks[h] - lse_ih) delta_ih.
+ * alibi_slopes [H] and sinks [H] are f32 device arrays, or NULL for none; softcap must be >= 0
+ * and finite (else FA_ERR_SHAPE).  dsinks [H] (f32, device) is written when sinks is given and
+ * may then be NULL (no sink gradient); it is ignored without sinks.  These pointers need 4-byte
+ * alignment.  With sinks, a row without an allowed key has lse = sinks[h], delta = 0 and a zero
+ * dQ row.  All four NULL / 0 is fa_back() itself: the same plan and bit-identical results.
+ * Workspace, plan, asynchrony and the other errors are those of fa_back().
+ */
+fa_status fa_back_ext(const float* q, const void* k, int k_type, const void* v, int v_type,
+                      const uint16_t* mask, int mask_heads, const float* dO, float scale, int N, int M, int H,
+                      int Hkv, int D, int Dv, int causal, const float* alibi_slopes, float softcap,
+                      const float* sinks, float* dsinks, float* dQ, float* dK, float* dV, float* lse,
+                      float* delta, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * The forward of the same attention over the raw cache: O [N][H][Dv] = softmax(scale * q k^T +
  * mask, causal tail) v and lse [N][H] (natural log), f32.  A row without an allowed key gets
  * O = 0 and lse = -inf.  Arguments as for fa_back(); O and lse are written, 16-byte aligned.

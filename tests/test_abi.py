@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
-        ["fa_back", "fa_back_batched", "fa_back_get_error", "fa_back_noalloc", "fa_back_plan_info", "fa_back_profile",
+        ["fa_back", "fa_back_batched", "fa_back_ext", "fa_back_get_error", "fa_back_noalloc", "fa_back_plan_info", "fa_back_profile",
          "fa_back_profile_read",
          "fa_back_selftest_timeout", "fa_back_status_string", "fa_back_strided", "fa_back_strided_workspace_size",
          "fa_back_workspace_size",
@@ -77,6 +77,29 @@ def _call(**kw):
 ])
 def test_argument_errors_are_reported_before_any_launch(L, kw, code):
     assert fb.STATUS[_call(**kw)] == code
+
+
+def _ext_call(**kw):
+    a = dict(q=0x1000, k=0x2000, k_type=2, v=0x3000, v_type=2, mask=None, mask_heads=0, dO=0x4000, scale=0.1,
+             N=8, M=32, H=4, Hkv=2, D=128, Dv=128, causal=0, alibi_slopes=None, softcap=0.0, sinks=None,
+             dsinks=None, dQ=0x5000, dK=0x6000, dV=0x7000, lse=0x8000, delta=0x9000, workspace=0x10000,
+             workspace_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return fb.fa_back_ext(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(softcap=-1.0), "FA_ERR_SHAPE"),
+    (dict(softcap=float("nan")), "FA_ERR_SHAPE"),
+    (dict(softcap=float("inf")), "FA_ERR_SHAPE"),
+    (dict(alibi_slopes=0xB001), "FA_ERR_ALIGN"),
+    (dict(sinks=0xB002), "FA_ERR_ALIGN"),
+    (dict(sinks=0xB000, dsinks=0xC003), "FA_ERR_ALIGN"),
+    (dict(k_type=9, softcap=1.0), "FA_ERR_TYPE"),
+    (dict(q=None, sinks=0xB000), "FA_ERR_NULL"),
+])
+def test_ext_argument_errors_are_reported_before_any_launch(L, kw, code):
+    assert fb.STATUS[_ext_call(**kw)] == code
 
 
 def test_workspace_size_grows_with_the_problem(L):
