@@ -74,6 +74,8 @@ def lib():
     L.fa_back_status_string.argtypes = [i]
     L.fa_back_noalloc.restype = i
     L.fa_back_noalloc.argtypes = [vp, vp, i, vp, i, vp, i, vp, f, i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp]
+    L.fa_back_test_wait_limit.restype = i
+    L.fa_back_test_wait_limit.argtypes = [ctypes.c_ulonglong]
     L.fa_back_selftest_timeout.restype = i
     L.fa_back_selftest_timeout.argtypes = [ctypes.c_ulonglong, vp]
     L.fa_back_profile.restype = i
@@ -191,3 +193,8 @@ def fa_back_noalloc(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, 
 
 def fa_back_selftest_timeout(limit_ns: int, stream=None) -> int:
     return int(lib().fa_back_selftest_timeout(limit_ns, stream))
+
+
+def fa_back_test_wait_limit(limit_ns: int) -> int:
+    """Failure-detection hook: the next call's kernels give up on waits longer than limit_ns."""
+    return int(lib().fa_back_test_wait_limit(limit_ns))

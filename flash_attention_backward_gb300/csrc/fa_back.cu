@@ -19,6 +19,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <limits>
@@ -131,6 +132,9 @@ static const char* const kKernelNames[kProfSlots] = {
     "k_dq_reduce", "k_cols", "k_dq_gemm", "k_stats_in", "k_fwd_lse", "k_fwd_o", "k_o_reduce", "k_cols_rowscale",
     "k_sink_grad"};
 Profiler g_prof;
+
+// Failure-detection hook: the wait limit of the next call's kernels plus one (0: none pending).
+static std::atomic<unsigned long long> g_next_wait_ns{0};
 
 static RunFn pick_seq(int D, int Dv, bool ext, bool forward) {
   switch (D) {
@@ -307,6 +311,7 @@ extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, 
   if (!workspace || workspace_bytes < P.total) return FA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return FA_ERR_ALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const unsigned long long wait_hook = g_next_wait_ns.exchange(0);  // this call takes a pending limit
 
   // ---- degenerate shapes: every output element is still written
   if (N == 0 || M == 0) {
@@ -366,6 +371,7 @@ extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, 
   p.rbk_pad = (int)((rbk + 15) / 16 * 16);
   p.rbv_pad = (int)((rbv + 15) / 16 * 16);
   p.err = errp;
+  p.wait_ns = wait_hook ? wait_hook - 1 : kWaitLimitNs;
   p.softcap = X.softcap;
   p.alibi = X.alibi;
   p.sinks = X.sinks;
@@ -400,6 +406,12 @@ extern "C" fa_status fa_back_selftest_timeout(unsigned long long limit_ns, void*
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&errp), g_err) != cudaSuccess) return FA_ERR_CUDA;
   k_wait_selftest<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(errp, limit_ns);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+extern "C" fa_status fa_back_test_wait_limit(unsigned long long limit_ns) {
+  if (limit_ns > kWaitLimitNs) return FA_ERR_SHAPE;
+  g_next_wait_ns.store(limit_ns + 1);
+  return FA_OK;
 }
 
 extern "C" fa_status fa_back_get_error(void) {

@@ -32,7 +32,7 @@ namespace fab {
 
 constexpr int kTypeF32 = 0, kTypeF16 = 1, kTypeQ8 = 2, kTypeQ4 = 3;
 constexpr int kErrTimeout = 8;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait (and per drain after an abort)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -110,6 +110,8 @@ struct Params {
   int raw_depth;       // entries of the K ring (2..8)
   int raw_depth_v;     // entries of the V ring (1..8)
   int* err;
+  uint64_t wait_ns;    // a wait gives up after this long: kWaitLimitNs, shorter only under the
+                       // failure-detection hook (fa_back_test_wait_limit); drains keep kWaitLimitNs
   // score extensions (fa_back_ext); all null / 0 for the plain operation
   float softcap;       // c > 0: the score x = scale q.k becomes c tanh(x / c); 0: none
   const float* alibi;  // [H] slopes: bias slope_h (j - (M - N + i)) added after the mask, or null
@@ -824,10 +826,11 @@ static_assert(8 * B_COUNT + 8 <= 512, "barrier area");
 struct Waiter {
   volatile int* abort;
   int* err;
+  uint64_t limit_ns;
   __device__ __forceinline__ bool operator()(uint64_t* bar, uint32_t parity) const {
     if (mbar_try_wait(bar, parity)) return true;  // fast path: the phase is already complete
     if (*abort) return false;
-    if (mbar_wait_bounded(bar, parity, kWaitLimitNs)) return true;
+    if (mbar_wait_bounded(bar, parity, limit_ns)) return true;
     *abort = 1;
     record_error(err, kErrTimeout);
     return false;
@@ -918,7 +921,7 @@ static __global__ void __launch_bounds__(Rows2Cfg<D, Dv, BK, MODE>::NT, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-  const Waiter wait{s_abort, p.err};
+  const Waiter wait{s_abort, p.err, p.wait_ns};
   const Stats st = *p.st;
   int n_kraw = 0, n_vraw = 0, n_dq = 0;  // producer: raw entries loaded, dQ products issued
   bool s_issued = false;                 // issuer: any S product issued
@@ -1020,7 +1023,7 @@ static __global__ void __launch_bounds__(Rows2Cfg<D, Dv, BK, MODE>::NT, 1)
         t0 = globaltimer_ns();
       } else {
         if (*s_abort) break;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > p.wait_ns) {
           if (lane == 0) {
             *s_abort = 1;
             record_error(p.err, kErrTimeout);
@@ -1486,7 +1489,7 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-  const Waiter wait{s_abort, p.err};
+  const Waiter wait{s_abort, p.err, p.wait_ns};
   const Stats st = *p.st;
   int n_kload = 0, n_vload = 0, n_prod = 0;  // producer: K' and V' tiles loaded, products issued
   bool s_issued = false;                     // issuer: any S product issued
@@ -1560,7 +1563,7 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
           t0 = globaltimer_ns();
         } else {
           if (*s_abort) break;
-          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          if (globaltimer_ns() - t0 > p.wait_ns) {
             *s_abort = 1;
             record_error(p.err, kErrTimeout);
             break;
@@ -2104,7 +2107,7 @@ static __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-  const Waiter wait{s_abort, p.err};
+  const Waiter wait{s_abort, p.err, p.wait_ns};
   int n_oload = 0, n_qload = 0;  // producer: dO and Q panels loaded
 
   if (warp == 0) {
@@ -2512,7 +2515,7 @@ static __global__ void __launch_bounds__(256, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-  const Waiter wait{s_abort, p.err};
+  const Waiter wait{s_abort, p.err, p.wait_ns};
   int n_load = 0;  // producer: stages loaded
 
   if (warp == 0) {

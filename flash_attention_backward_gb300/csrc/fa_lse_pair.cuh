@@ -37,6 +37,7 @@ template <bool Poll>
 struct WaiterC {
   volatile int* abort;
   int* err;
+  uint64_t limit_ns;
   __device__ __forceinline__ bool test(uint64_t* bar, uint32_t parity) const {
     return Poll ? mbar_test_wait_cluster(bar, parity) : mbar_try_wait_cluster(bar, parity);
   }
@@ -46,7 +47,7 @@ struct WaiterC {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
       if (test(bar, parity)) return true;
-      if ((it & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) break;
+      if (((it & 255u) == 0 || limit_ns < kShortWaitNs) && globaltimer_ns() - t0 > limit_ns) break;
     }
     *abort = 1;
     record_error(err, kErrTimeout);
@@ -157,9 +158,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LsePairCfg<D, Dv>::N
   cluster_sync_all();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-  const Waiter wait{s_abort, p.err};
-  const WaiterC<false> wait_c{s_abort, p.err};
-  const WaiterC<true> poll_c{s_abort, p.err};
+  const Waiter wait{s_abort, p.err, p.wait_ns};
+  const WaiterC<false> wait_c{s_abort, p.err, p.wait_ns};
+  const WaiterC<true> poll_c{s_abort, p.err, p.wait_ns};
   const Stats st = *p.st;
   // the even CTA's barrier at the offset of local barrier `b`
   auto lead_bar = [&](int b) { return mapa_shared(smem_u32(&bar[b]), 0); };
@@ -209,7 +210,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LsePairCfg<D, Dv>::N
           t0 = globaltimer_ns();
         } else {
           if (*s_abort) break;
-          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          if (globaltimer_ns() - t0 > p.wait_ns) {
             *s_abort = 1;
             record_error(p.err, kErrTimeout);
             break;

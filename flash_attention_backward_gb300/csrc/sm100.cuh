@@ -86,12 +86,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Waits for the phase with the given parity to complete; gives up after `limit_ns`.  (A
 // suspend-time hint on try_wait measured slower here: the woken thread resumes late.)
+// Limits below this are checked on every try rather than every 256th (the failure-detection
+// hook's short limits must take effect on the first wait that outlasts them).
+constexpr uint64_t kShortWaitNs = 1000000ull;
+
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    if (((it & 255u) == 0 || limit_ns < kShortWaitNs) && globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -296,6 +296,19 @@ fa_status fa_back_noalloc(const float* q, const void* k, int k_type, const void*
  */
 fa_status fa_back_selftest_timeout(unsigned long long limit_ns, void* stream);
 
+/*
+ * Failure-detection hook for the real passes (not part of the operation).  The kernels of the
+ * next call that validates its arguments and runs the passes (fa_back(), fa_back_ext(),
+ * fa_back_with_stats(), fa_forward(), or an entry point built on them) give up on every wait
+ * that lasts longer than limit_ns nanoseconds (0: on every wait not complete at once) instead of
+ * after 2 s.  They then take the path of a real stall: FA_ERR_TIMEOUT is recorded in the device
+ * error word, each CTA stops issuing work, waits (up to 2 s) for its own loads and tensor-core
+ * products still in flight, frees its tensor memory and exits.  That call's outputs are
+ * undefined; later calls use the normal limit.  Returns FA_OK, or FA_ERR_SHAPE for a limit
+ * above 2 s.
+ */
+fa_status fa_back_test_wait_limit(unsigned long long limit_ns);
+
 #ifdef __cplusplus
 }
 #endif

@@ -29,6 +29,7 @@ def test_header_declares_the_entry_points():
         ["fa_back", "fa_back_batched", "fa_back_ext", "fa_back_get_error", "fa_back_noalloc", "fa_back_plan_info", "fa_back_profile",
          "fa_back_profile_read",
          "fa_back_selftest_timeout", "fa_back_status_string", "fa_back_strided", "fa_back_strided_workspace_size",
+         "fa_back_test_wait_limit",
          "fa_back_workspace_size",
          "fa_back_with_stats", "fa_back_workspace_size_min", "fa_forward", "fa_forward_workspace_size",
          "fa_row_bytes"])

@@ -4,6 +4,11 @@ Every mbarrier wait in the kernels gives up after a time limit, records FA_ERR_T
 device word and lets its CTA finish.  fa_back_selftest_timeout() runs that path on a barrier
 that nothing completes (with a 1 ms limit); the error must reach the host once, be cleared by
 reading it, and leave the context usable for a correct backward afterwards.
+
+fa_back_test_wait_limit() makes the real passes give up: their waits run out after a short limit
+instead of 2 s, so each CTA takes its abort path (stop issuing, wait for its own loads and
+tensor-core products still in flight, free tensor memory) at whatever point its pipeline has
+reached.  The call after must again match the oracle.
 """
 import numpy as np
 import pytest
@@ -45,3 +50,56 @@ def test_expired_wait_is_reported_and_the_context_stays_usable(fb):
 def test_limit_out_of_range_is_rejected_before_launch(fb):
     assert fb.STATUS[fb.fa_back_selftest_timeout(0)] == "FA_ERR_SHAPE"
     assert fb.STATUS[fb.fa_back_selftest_timeout(3_000_000_000)] == "FA_ERR_SHAPE"
+
+
+def _run(fb, p, workspace_bytes=None):
+    t = synth.device.to_torch(p, "cuda")
+    out = fb.backward(t["q"], t["k"], p.k_type, t["v"], p.v_type, t["dO"], H=p.H, Hkv=p.Hkv, D=p.D, Dv=p.Dv,
+                      M=p.M, scale=p.scale, causal=p.causal, mask=t["mask"], mask_heads=p.mask_heads,
+                      workspace_bytes=workspace_bytes)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def _level(fb, p):
+    return fb.fa_back_plan_info(p.N, p.M, p.H, p.Hkv, p.D, p.Dv,
+                                fb.fa_back_workspace_size(p.N, p.M, p.H, p.Hkv, p.D, p.Dv))[1]
+
+
+def test_passes_give_up_at_once_then_the_next_call_is_correct(fb):
+    """Limit 0: every wait that is not complete at once gives up, in the LSE pass, the dK/dV pass
+    and the dQ product (plan level 2); the timeout reaches the host once."""
+    import oracle
+    p = synth.from_config("0")
+    assert _level(fb, p) == 2
+    assert fb.fa_back_get_error() == 0
+    assert fb.STATUS[fb.fa_back_test_wait_limit(0)] == "FA_OK"
+    _run(fb, p)
+    assert fb.STATUS[fb.fa_back_get_error()] == "FA_ERR_TIMEOUT"
+    assert fb.fa_back_get_error() == 0
+    got = _run(fb, p)  # the hook held for one call only
+    assert fb.fa_back_get_error() == 0
+    check_components(got, oracle.fa_back(p), NMSE_TOL)
+
+
+@pytest.mark.parametrize("limit_ns", [2_000, 20_000])
+def test_passes_give_up_mid_pipeline_then_the_next_call_is_correct(fb, limit_ns):
+    """A limit of a few microseconds: some CTAs give up with loads and products in flight, others
+    finish; whichever happened, the context stays usable and the next call is correct."""
+    import oracle
+    p = synth.from_config("1")
+    assert _level(fb, p) == 2
+    assert fb.fa_back_get_error() == 0
+    assert fb.STATUS[fb.fa_back_test_wait_limit(limit_ns)] == "FA_OK"
+    _run(fb, p)
+    status = fb.STATUS[fb.fa_back_get_error()]
+    print(limit_ns, status)
+    assert status in ("FA_OK", "FA_ERR_TIMEOUT")
+    got = _run(fb, p)
+    assert fb.fa_back_get_error() == 0
+    check_components(got, oracle.fa_back(p), NMSE_TOL)
+
+
+def test_wait_limit_above_the_normal_one_is_rejected(fb):
+    assert fb.STATUS[fb.fa_back_test_wait_limit(3_000_000_000)] == "FA_ERR_SHAPE"
+
