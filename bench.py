@@ -33,7 +33,7 @@ import synth  # noqa: E402
 METRIC = "FA-back ms + TFLOP/s at N2048/M75520/H24/Hkv4/D256 q8_0; % of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_PRODUCTS = {  # contractions (of the five) each pass forms on every visible (i, j) pair
-    "k_rows_lse": 2, "k_rows_dq": 3, "k_cols": 4, "k_cols_rowscale": 4, "k_dq_gemm": 1}
+    "k_rows_lse": 2, "k_rows_dq": 3, "k_cols": 4, "k_cols_rowscale": 4, "k_dq_gemm": 1, "k_dq_raw": 1}
 
 
 def peaks():
@@ -329,22 +329,52 @@ def run_ours(args):
     fw_ms = timed(lambda: fb.forward(t["q"], t["k"], p.k_type, t["v"], p.v_type, H=p.H, Hkv=p.Hkv, D=p.D, Dv=p.Dv,
                                      M=p.M, scale=p.scale, causal=p.causal, mask=t["mask"],
                                      mask_heads=p.mask_heads, workspace=ws, stream=stream), n_var)
+    def timed_kernels(fn, n):
+        # the same, plus each kernel's mean time from the library's profile record
+        ms_ = timed(fn, n)
+        fb.fa_back_profile(True)
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        fb.fa_back_profile(False)
+        return ms_, {k: v[0] / v[1] for k, v in fb.fa_back_profile_read().items() if v[1]}
+
+    # the plans that keep no decoded copy of the cache: the stored dS with every pass decoding the
+    # raw cache (fa_back_nocopy's default workspace), and the smallest workspace (level 0)
+    wnc = fb.fa_back_workspace_size_nocopy(p.N, p.M, p.H, p.Hkv, p.D, p.Dv)
+    wsnc = fb.Workspace(dev)
+    nc_ms, nc_kern = timed_kernels(lambda: fb.backward(
+        t["q"], t["k"], p.k_type, t["v"], p.v_type, t["dO"], H=p.H, Hkv=p.Hkv, D=p.D, Dv=p.Dv, M=p.M, scale=p.scale,
+        causal=p.causal, mask=t["mask"], mask_heads=p.mask_heads, out=out, workspace=wsnc, stream=stream,
+        workspace_bytes=wnc, nocopy=True), n_var)
+    del wsnc
     wmin = fb.fa_back_workspace_size_min(p.N, p.M, p.H, p.Hkv, p.D, p.Dv)
     lvl_min = fb.fa_back_plan_info(p.N, p.M, p.H, p.Hkv, p.D, p.Dv, wmin)
     wsmin = fb.Workspace(dev)
-    mn_ms = timed(lambda: fb.backward(t["q"], t["k"], p.k_type, t["v"], p.v_type, t["dO"], H=p.H, Hkv=p.Hkv, D=p.D,
-                                      Dv=p.Dv, M=p.M, scale=p.scale, causal=p.causal, mask=t["mask"],
-                                      mask_heads=p.mask_heads, out=out, workspace=wsmin, stream=stream,
-                                      workspace_bytes=wmin), n_var)
+    mn_ms, mn_kern = timed_kernels(lambda: fb.backward(
+        t["q"], t["k"], p.k_type, t["v"], p.v_type, t["dO"], H=p.H, Hkv=p.Hkv, D=p.D, Dv=p.Dv, M=p.M, scale=p.scale,
+        causal=p.causal, mask=t["mask"], mask_heads=p.mask_heads, out=out, workspace=wsmin, stream=stream,
+        workspace_bytes=wmin), n_var)
     del wsmin
     assert fb.fa_back_get_error() == 0
-    ws_ms, fw_ms, mn_ms = max_over_ranks(dist, [ws_ms, fw_ms, mn_ms], dev)
+    ws_ms, fw_ms, mn_ms, nc_ms = max_over_ranks(dist, [ws_ms, fw_ms, mn_ms, nc_ms], dev)
+    pk_v, _ = peaks()
+    peak_v = float(pk_v.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     variants = {
         "fa_back_with_stats": {"ms": ws_ms, "TFLOP/s": job_tflops(world, p.flops(), ws_ms),
                                "note": "lse and delta given; the LSE/D pass is skipped; same F_alg"},
+        "fa_back_nocopy": {"ms": nc_ms, "TFLOP/s": job_tflops(world, p.flops(), nc_ms),
+                           "path_roofline_frac": p.flops() / (peak_v * 1e12) / (nc_ms * 1e-3),
+                           "workspace_bytes": wnc,
+                           "plan": fb.fa_back_plan_info(p.N, p.M, p.H, p.Hkv, p.D, p.Dv, wnc), "kernels_ms": nc_kern,
+                           "note": "no decoded copy of the cache: raw K/V tiles decoded in shared memory by every "
+                                   "pass, dS stored (plan level 3); fa_back_nocopy() with "
+                                   "fa_back_workspace_size_nocopy() bytes"},
         "fa_back_min_workspace": {"ms": mn_ms, "TFLOP/s": job_tflops(world, p.flops(), mn_ms),
-                                  "workspace_bytes": wmin, "plan": lvl_min,
-                                  "note": "fa_back given fa_back_workspace_size_min() bytes"},
+                                  "path_roofline_frac": p.flops() / (peak_v * 1e12) / (mn_ms * 1e-3),
+                                  "workspace_bytes": wmin, "plan": lvl_min, "kernels_ms": mn_kern,
+                                  "note": "fa_back given fa_back_workspace_size_min() bytes (level 0: no copy, "
+                                          "dS recomputed in a dQ pass)"},
         "fa_forward": {"ms": fw_ms, "TFLOP/s": job_tflops(world, 4.0 * p.D * p.H * p.visible_pairs(), fw_ms),
                        "note": "O and lse; TFLOP/s of its two contractions (S, P V)"},
     }
@@ -395,12 +425,33 @@ def run_ours(args):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / e_steps
 
+    def copy_ms(h2d_dir: bool) -> float:
+        # one step's input copies (or result copies) alone on the compute stream: the copy rate
+        # the pipelined form has to hide behind the backward
+        best = float("inf")
+        for _ in range(3):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            c0.record(stream)
+            with torch.cuda.stream(stream):
+                if h2d_dir:
+                    for k in keys_in:
+                        din[0][k].copy_(hq[k], non_blocking=True)
+                else:
+                    for k, v in dout[0].items():
+                        hout[0][k].copy_(v, non_blocking=True)
+            c1.record(stream)
+            torch.cuda.synchronize()
+            best = min(best, c0.elapsed_time(c1))
+        return best
+
     run_e2e(True)  # warm: first use of the second buffer set and of the copy streams
     e2e_serial_ms = run_e2e(False)
     e2e_ms = min(run_e2e(True), run_e2e(True))
+    h2d_ms, d2h_ms = copy_ms(True), copy_ms(False)
     rc = fb.fa_back_get_error()
     assert rc == 0, fb.fa_back_status_string(rc)
-    e2e_ms, e2e_serial_ms = max_over_ranks(dist, [e2e_ms, e2e_serial_ms], dev)
+    e2e_ms, e2e_serial_ms, h2d_ms, d2h_ms = max_over_ranks(dist, [e2e_ms, e2e_serial_ms, h2d_ms, d2h_ms], dev)
 
     flops = p.flops()
     tflops = job_tflops(world, flops, ms)
@@ -445,7 +496,13 @@ def run_ours(args):
             "e2e": {"value": e2e_tflops, "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
                     "pipelining": "input copy, backward and result copy on three streams, double-buffered",
-                    "serial": {"value": job_tflops(world, flops, e2e_serial_ms), "ms_per_step": e2e_serial_ms}}}
+                    "serial": {"value": job_tflops(world, flops, e2e_serial_ms), "ms_per_step": e2e_serial_ms},
+                    # what the overlap has to hide: each direction's copies alone, and the host
+                    # setting that would serialise the three streams if set to 1
+                    "copies": {"h2d_ms": h2d_ms, "d2h_ms": d2h_ms, "h2d_GBps": h2d / (h2d_ms * 1e6),
+                               "d2h_GBps": d2h / (d2h_ms * 1e6),
+                               "pipelined_bound_ms": max(ms, h2d_ms, d2h_ms),
+                               "CUDA_DEVICE_MAX_CONNECTIONS": os.environ.get("CUDA_DEVICE_MAX_CONNECTIONS")}}}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(p)
     if rank == 0:

@@ -7,7 +7,8 @@ on the current stream.
 """
 from ._native import (  # noqa: F401
     FA_F16, FA_F32, FA_MASK_BITS, FA_MASK_F16, FA_Q4_0, FA_Q8_0, STATUS, NativeLibraryMissing, LIB_PATH,
-    fa_back, fa_back_batched, fa_back_ext, fa_back_get_error, fa_back_noalloc, fa_back_plan_info, fa_back_profile,
+    fa_back, fa_back_batched, fa_back_ext, fa_back_get_error, fa_back_noalloc, fa_back_nocopy, fa_back_plan_info,
+    fa_back_profile, fa_back_workspace_size_nocopy,
     fa_back_profile_read, fa_back_selftest_timeout, fa_back_status_string, fa_back_strided,
     fa_back_strided_workspace_size, fa_back_test_wait_limit, fa_strides,
     fa_back_with_stats, fa_back_workspace_size, fa_back_workspace_size_min, fa_forward, fa_forward_workspace_size,

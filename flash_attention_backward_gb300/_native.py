@@ -50,6 +50,10 @@ def lib():
     L.fa_back_plan_info.argtypes = [i] * 6 + [sz, vp, vp, vp]
     L.fa_back.restype = i
     L.fa_back.argtypes = [vp, vp, i, vp, i, vp, i, vp, f, i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.fa_back_nocopy.restype = i
+    L.fa_back_nocopy.argtypes = [vp, vp, i, vp, i, vp, i, vp, f, i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.fa_back_workspace_size_nocopy.restype = sz
+    L.fa_back_workspace_size_nocopy.argtypes = [i] * 6
     L.fa_back_ext.restype = i
     L.fa_back_ext.argtypes = [vp, vp, i, vp, i, vp, i, vp, f, i, i, i, i, i, i, i, vp, f, vp, vp, vp, vp, vp, vp, vp,
                               vp, sz, vp]
@@ -111,6 +115,17 @@ def fa_back(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, 
     """Direct call of the C entry point; pointers are integers (device addresses) or None."""
     return int(lib().fa_back(q, k, k_type, v, v_type, mask, mask_heads, dO, float(scale), N, M, H, Hkv, D, Dv,
                              int(causal), dQ, dK, dV, lse, delta, workspace, workspace_bytes, stream))
+
+
+def fa_back_nocopy(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal,
+                   dQ, dK, dV, lse, delta, workspace, workspace_bytes, stream) -> int:
+    """fa_back restricted to the plans without a decoded copy of the cache (levels 3 and 0)."""
+    return int(lib().fa_back_nocopy(q, k, k_type, v, v_type, mask, mask_heads, dO, float(scale), N, M, H, Hkv, D,
+                                    Dv, int(causal), dQ, dK, dV, lse, delta, workspace, workspace_bytes, stream))
+
+
+def fa_back_workspace_size_nocopy(N: int, M: int, H: int, Hkv: int, D: int, Dv: int) -> int:
+    return int(lib().fa_back_workspace_size_nocopy(N, M, H, Hkv, D, Dv))
 
 
 def fa_back_ext(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal,

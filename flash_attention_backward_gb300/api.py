@@ -40,7 +40,7 @@ def backward(q: torch.Tensor, k: torch.Tensor, k_type: int, v: torch.Tensor, v_t
              workspace: Optional[Workspace] = None, stream: Optional[torch.cuda.Stream] = None,
              workspace_bytes: Optional[int] = None, lse: Optional[torch.Tensor] = None,
              delta: Optional[torch.Tensor] = None, alibi_slopes: Optional[torch.Tensor] = None,
-             softcap: float = 0.0, sinks: Optional[torch.Tensor] = None) -> dict:
+             softcap: float = 0.0, sinks: Optional[torch.Tensor] = None, nocopy: bool = False) -> dict:
     """Run the backward on device tensors.
 
     q [N][H][D] f32, dO [N][H][Dv] f32, k/v uint8 raw cache rows [M][Hkv][row], mask int16/uint16
@@ -49,7 +49,9 @@ def backward(q: torch.Tensor, k: torch.Tensor, k_type: int, v: torch.Tensor, v_t
     runs the fastest plan that fits it (at least fa_back_workspace_size_min).  Given the forward's
     row statistics lse and delta ([N][H] f32), fa_back_with_stats runs instead and the result
     holds dQ, dK and dV only.  With ALiBi slopes ([H] f32), a soft cap c > 0 or sink logits ([H]
-    f32), fa_back_ext runs; with sinks the result also holds "dsinks" ([H] f32).
+    f32), fa_back_ext runs; with sinks the result also holds "dsinks" ([H] f32).  nocopy runs
+    fa_back_nocopy (plans without a decoded copy of the cache; default workspace
+    fa_back_workspace_size_nocopy).
     """
     N = q.shape[0]
     dev = q.device
@@ -67,6 +69,8 @@ def backward(q: torch.Tensor, k: torch.Tensor, k_type: int, v: torch.Tensor, v_t
     ext = alibi_slopes is not None or softcap != 0.0 or sinks is not None
     if ext and given:
         raise FaBackError("the score extensions need the backward's own lse/delta pass")
+    if nocopy and (ext or given):
+        raise FaBackError("nocopy runs the plain backward")
     if sinks is not None and "dsinks" not in out:
         out["dsinks"] = torch.empty((H,), dtype=torch.float32, device=dev)
     if given:
@@ -75,7 +79,8 @@ def backward(q: torch.Tensor, k: torch.Tensor, k_type: int, v: torch.Tensor, v_t
     for t in (q, k, v, dO, mask, lse, delta, alibi_slopes, sinks, *out.values()):
         if t is not None and not t.is_contiguous():
             raise FaBackError("tensors must be contiguous")
-    ws_bytes = nat.fa_back_workspace_size(N, M, H, Hkv, D, Dv) if workspace_bytes is None else int(workspace_bytes)
+    size_fn = nat.fa_back_workspace_size_nocopy if nocopy else nat.fa_back_workspace_size
+    ws_bytes = size_fn(N, M, H, Hkv, D, Dv) if workspace_bytes is None else int(workspace_bytes)
     ws = (workspace or Workspace(dev)).get(ws_bytes)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     nbytes = ws.numel() if workspace_bytes is None else ws_bytes
@@ -83,6 +88,10 @@ def backward(q: torch.Tensor, k: torch.Tensor, k_type: int, v: torch.Tensor, v_t
         rc = nat.fa_back_with_stats(_ptr(q), _ptr(k), k_type, _ptr(v), v_type, _ptr(mask), mask_heads, _ptr(dO),
                                     _ptr(lse), _ptr(delta), scale, N, M, H, Hkv, D, Dv, causal, _ptr(out["dQ"]),
                                     _ptr(out["dK"]), _ptr(out["dV"]), ws.data_ptr(), nbytes, s.cuda_stream)
+    elif nocopy:
+        rc = nat.fa_back_nocopy(_ptr(q), _ptr(k), k_type, _ptr(v), v_type, _ptr(mask), mask_heads, _ptr(dO), scale,
+                                N, M, H, Hkv, D, Dv, causal, _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]),
+                                _ptr(out["lse"]), _ptr(out["delta"]), ws.data_ptr(), nbytes, s.cuda_stream)
     elif ext:
         rc = nat.fa_back_ext(_ptr(q), _ptr(k), k_type, _ptr(v), v_type, _ptr(mask), mask_heads, _ptr(dO), scale,
                              N, M, H, Hkv, D, Dv, causal, _ptr(alibi_slopes), softcap, _ptr(sinks),

@@ -60,15 +60,16 @@ static void layout(Plan& P, int M, int Hkv, int D, int Dv) {
   P.total = o;
 }
 
-// Launch plan and workspace layout for one variant (level 2: stored dS and a dQ product over it;
-// 1: binary16 K'/V' copies feeding the row passes; 0: row passes decoding the raw cache).  The
+// Launch plan and workspace layout for one variant (level 2: binary16 K'/V' copies and the stored
+// dS with a dQ product over it; 3: the stored dS without the copies, every pass decoding the raw
+// cache; 1: the copies only, feeding the row passes; 0: passes decoding the raw cache).  The
 // keys of each row tile are split so that the last wave of CTAs (one per SM) wastes least,
 // counting a small cost per split for the partial merges; among split counts whose workspace
 // fits `ws_cap`, the cheapest is taken (1 if none fits).
 static Plan plan_variant(int N, int M, int H, int Hkv, int D, int Dv, int nsm, size_t ws_cap, int level) {
   Plan P;
   std::memset(&P, 0, sizeof(P));
-  P.pre = level >= 1;
+  P.pre = level == 1 || level == 2;
   P.dsq = level >= 2;
   P.ldds = (M + block_keys(D, Dv) - 1) / block_keys(D, Dv) * (block_keys(D, Dv) / 64);  // whole key tiles
   P.nsm = nsm;
@@ -103,15 +104,21 @@ static Plan plan_variant(int N, int M, int H, int Hkv, int D, int Dv, int nsm, s
   return P;
 }
 
-// The fastest plan whose workspace fits ws_cap, trying the levels from 2 down; level 0 with one
-// split is the smallest workspace fa_back() accepts.
-static Plan make_plan(int N, int M, int H, int Hkv, int D, int Dv, int nsm, size_t ws_cap = SIZE_MAX) {
-  for (int level = 2; level > 0; --level) {
+// The fastest plan whose workspace fits ws_cap, trying the levels in the order of their speed
+// (2, 3, 1; their workspaces grow as 1 < 3 < 2); level 0 with one split is the smallest workspace
+// fa_back() accepts.  nocopy keeps to the plans without the binary16 copy of the cache (3, 0).
+static Plan make_plan(int N, int M, int H, int Hkv, int D, int Dv, int nsm, size_t ws_cap = SIZE_MAX,
+                      bool nocopy = false) {
+  static const int kOrder[] = {2, 3, 1};
+  for (int level : kOrder) {
+    if (nocopy && level != 3) continue;
     const Plan P = plan_variant(N, M, H, Hkv, D, Dv, nsm, ws_cap, level);
     if (P.total <= ws_cap) return P;
   }
   return plan_variant(N, M, H, Hkv, D, Dv, nsm, ws_cap, 0);
 }
+
+static int plan_level(const Plan& P) { return P.dsq ? (P.pre ? 2 : 3) : P.pre ? 1 : 0; }
 
 static int device_sms(int* major, int* minor) {
   int dev = 0, nsm = 0;
@@ -130,7 +137,7 @@ static int device_sms(int* major, int* minor) {
 static const char* const kKernelNames[kProfSlots] = {
     "k_row_stats", "k_vsum", "k_finalize", "k_convert", "k_predecode", "k_rows_lse", "k_lse_merge", "k_rows_dq",
     "k_dq_reduce", "k_cols", "k_dq_gemm", "k_stats_in", "k_fwd_lse", "k_fwd_o", "k_o_reduce", "k_cols_rowscale",
-    "k_sink_grad"};
+    "k_sink_grad", "k_dq_raw"};
 Profiler g_prof;
 
 // Failure-detection hook: the wait limit of the next call's kernels plus one (0: none pending).
@@ -178,6 +185,13 @@ extern "C" size_t fa_back_workspace_size_min(int N, int M, int H, int Hkv, int D
   return fab_workspace_size_capped(N, M, H, Hkv, D, Dv, 0);
 }
 
+extern "C" size_t fa_back_workspace_size_nocopy(int N, int M, int H, int Hkv, int D, int Dv) {
+  if (N < 0 || M < 0 || H <= 0 || Hkv <= 0 || H % Hkv) return 0;
+  int nsm = device_sms(nullptr, nullptr);
+  if (nsm <= 0) nsm = 152;
+  return make_plan(N, M, H, Hkv, D, Dv, nsm, SIZE_MAX, true).total;
+}
+
 extern "C" fa_status fa_back_plan_info(int N, int M, int H, int Hkv, int D, int Dv, size_t workspace_bytes,
                                        int* level, int* key_splits, size_t* plan_bytes) {
   if (N < 0 || M < 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || Hkv > 256) return FA_ERR_SHAPE;
@@ -186,7 +200,7 @@ extern "C" fa_status fa_back_plan_info(int N, int M, int H, int Hkv, int D, int 
   if (nsm <= 0) nsm = 152;  // no device: the GB300's SM count
   const Plan P = make_plan(N, M, H, Hkv, D, Dv, nsm, workspace_bytes);
   if (workspace_bytes < P.total) return FA_ERR_WORKSPACE;
-  if (level) *level = P.dsq ? 2 : P.pre ? 1 : 0;
+  if (level) *level = plan_level(P);
   if (key_splits) *key_splits = P.nsplit;
   if (plan_bytes) *plan_bytes = P.total;
   return FA_OK;
@@ -207,7 +221,17 @@ extern "C" fa_status fa_back_ext(const float* q, const void* k, int k_type, cons
                                  int H, int Hkv, int D, int Dv, int causal, const float* alibi_slopes, float softcap,
                                  const float* sinks, float* dsinks, float* dQ, float* dK, float* dV, float* lse,
                                  float* delta, void* workspace, size_t workspace_bytes, void* stream) {
-  const fab_ext x = {alibi_slopes, softcap, sinks, dsinks};
+  const fab_opts x = {alibi_slopes, softcap, sinks, dsinks, 0};
+  return fab_back_capped(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal, dQ,
+                         dK, dV, lse, delta, workspace, workspace_bytes, stream, workspace_bytes, nullptr, nullptr,
+                         nullptr, &x);
+}
+
+extern "C" fa_status fa_back_nocopy(const float* q, const void* k, int k_type, const void* v, int v_type,
+                                    const uint16_t* mask, int mask_heads, const float* dO, float scale, int N, int M,
+                                    int H, int Hkv, int D, int Dv, int causal, float* dQ, float* dK, float* dV,
+                                    float* lse, float* delta, void* workspace, size_t workspace_bytes, void* stream) {
+  const fab_opts x = {nullptr, 0.f, nullptr, nullptr, 1};
   return fab_back_capped(q, k, k_type, v, v_type, mask, mask_heads, dO, scale, N, M, H, Hkv, D, Dv, causal, dQ,
                          dK, dV, lse, delta, workspace, workspace_bytes, stream, workspace_bytes, nullptr, nullptr,
                          nullptr, &x);
@@ -275,11 +299,11 @@ extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, 
                                      int M, int H, int Hkv, int D, int Dv, int causal, float* dQ, float* dK,
                                      float* dV, float* lse, float* delta, void* workspace, size_t workspace_bytes,
                                      void* stream, size_t ws_cap, const float* lse_in, const float* delta_in,
-                                     float* O, const fab_ext* ext) {
+                                     float* O, const fab_opts* ext) {
   const bool given = lse_in != nullptr;  // fa_back_with_stats: no lse/delta outputs
   const bool forward = O != nullptr;     // fa_forward: lse and O only
-  const fab_ext none = {nullptr, 0.f, nullptr, nullptr};
-  const fab_ext& X = ext ? *ext : none;
+  const fab_opts none = {nullptr, 0.f, nullptr, nullptr, 0};
+  const fab_opts& X = ext ? *ext : none;
   if (!(X.softcap >= 0.f) || !std::isfinite(X.softcap)) return FA_ERR_SHAPE;
   if ((given || forward) && (X.alibi || X.softcap > 0.f || X.sinks)) return FA_ERR_UNSUPPORTED;
   // ---- argument checks (nothing is enqueued on failure)
@@ -307,7 +331,8 @@ extern "C" fa_status fab_back_capped(const float* q, const void* k, int k_type, 
   if (nsm <= 0) return FA_ERR_CUDA;
   if (major != 10 || minor != 3) return FA_ERR_DEVICE;
   // the forward runs plan level 1 (K'/V' copies, no stored dS)
-  const Plan P = forward ? plan_variant(N, M, H, Hkv, D, Dv, nsm, SIZE_MAX, 1) : make_plan(N, M, H, Hkv, D, Dv, nsm, ws_cap);
+  const Plan P = forward ? plan_variant(N, M, H, Hkv, D, Dv, nsm, SIZE_MAX, 1)
+                         : make_plan(N, M, H, Hkv, D, Dv, nsm, ws_cap, X.nocopy != 0);
   if (!workspace || workspace_bytes < P.total) return FA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return FA_ERR_ALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -11,6 +11,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "fa_dq_raw.cuh"
 #include "fa_kernels.cuh"
 #include "fa_lse_pair.cuh"
 
@@ -71,10 +72,11 @@ inline bool make_map(CUtensorMap* m, void* base, int d0, int d1, int d2, int row
 // ------------------------------------------------------------------------------------------------
 // measurement hook: one CUDA event before the sequence and one after each launch
 
-constexpr int kProfCalls = 256, kProfSlots = 17;
+constexpr int kProfCalls = 256, kProfSlots = 18;
 enum {
   KS_STATS = 0, KS_VSUM, KS_FINAL, KS_CONVERT, KS_PREDECODE, KS_ROWS_LSE, KS_MERGE, KS_ROWS_DQ, KS_DQ_REDUCE,
-  KS_COLS, KS_DQ_GEMM, KS_STATS_IN, KS_FWD_LSE, KS_FWD_O, KS_O_REDUCE, KS_COLS_ROWSCALE, KS_SINK_GRAD, KS_N
+  KS_COLS, KS_DQ_GEMM, KS_STATS_IN, KS_FWD_LSE, KS_FWD_O, KS_O_REDUCE, KS_COLS_ROWSCALE, KS_SINK_GRAD, KS_DQ_RAW,
+  KS_N
 };
 
 struct Profiler {
@@ -255,8 +257,40 @@ cudaError_t rows_raw(Params pl, Params pq, const Plan& P, const CUtensorMap& tmQ
       return ep;
     }
   }
-  k_rows2<D, Dv, BK, 1, EXT><<<grid, RQ::NT, sm_q, s>>>(tmQ, tkq, tvq, pq);
-  rec.mark(KS_ROWS_DQ);
+  if (!P.dsq) {  // else dQ comes from the stored dS after the dK/dV pass
+    k_rows2<D, Dv, BK, 1, EXT><<<grid, RQ::NT, sm_q, s>>>(tmQ, tkq, tvq, pq);
+    rec.mark(KS_ROWS_DQ);
+  }
+  return cudaSuccess;
+}
+
+// Raw K staging of k_dq_raw: the largest entry (a whole key tile, else halves down to 32 keys)
+// of which at least two fit the budget, and as many entries as fit (at most kMaxRawDepth).
+inline void pick_raw_k(Params& q, int budget, int BK) {
+  int ke = BK;
+  while (ke > 32 && 2 * ke * q.rbk_pad > budget) ke >>= 1;
+  while (ke > 1 && 2 * ke * q.rbk_pad > budget) ke >>= 1;
+  q.ke = ke;
+  q.raw_depth = std::max(1, std::min(kMaxRawDepth, budget / std::max(1, ke * q.rbk_pad)));
+}
+
+// dQ over the stored dS with K decoded from the raw cache (k_dq_raw): two row tiles per CTA.
+template <int D, int BK>
+cudaError_t dq_raw(Params pr, const Plan& P, const CUtensorMap& tmS, cudaStream_t s, CallRec& rec) {
+  using QC = DqRawCfg<D, BK>;
+  pick_raw_k(pr, QC::RAW_BUDGET, BK);
+  if ((pr.ke * pr.rbk_pad) % 128) pr.raw_bulk = 0;  // TMA destinations start on 128-byte boundaries
+  if (pr.raw_depth < 2 || BK % pr.ke) return cudaErrorInvalidValue;
+  CUtensorMap tk;
+  std::memset(&tk, 0, sizeof(tk));
+  if (pr.raw_bulk && !make_raw_map(&tk, pr.k, pr.rbk, pr.Hkv, pr.M, pr.ke)) return cudaErrorInvalidValue;
+  // + 1024 for aligning the base, + 64 for the decoders' realigning reads past the last raw row
+  const int sm = QC::OFF_RAW + pr.ke * pr.raw_depth * pr.rbk_pad + 1024 + 64;
+  if (sm > QC::SMEM_MAX) return cudaErrorInvalidValue;
+  cudaError_t e;
+  if ((e = set_smem(k_dq_raw<D, BK>, sm)) != cudaSuccess) return e;
+  k_dq_raw<D, BK><<<dim3((P.nQT + 1) / 2, pr.Hkv, P.nsplit), QC::NT, sm, s>>>(tmS, tk, pr);
+  rec.mark(KS_DQ_RAW);
   return cudaSuccess;
 }
 
@@ -302,13 +336,15 @@ cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& tmQ, co
       rec.mark(KS_COLS_ROWSCALE);
     }
   }
-  if (P.dsq) {
+  if (P.dsq && P.pre) {
     using GC = GemmCfg<D, BK>;
     CUtensorMap tkg;
     if (!make_map(&tkg, p.kd, 64, p.M, p.Hkv * (D / 64), BK)) return cudaErrorInvalidValue;
     if ((e = set_smem(k_dq_gemm<D, BK>, GC::SMEM)) != cudaSuccess) return e;
     k_dq_gemm<D, BK><<<grid, 256, GC::SMEM, s>>>(tmS, tkg, p);
     rec.mark(KS_DQ_GEMM);
+  } else if (P.dsq) {  // no K' copy: the dQ product decodes raw K tiles itself
+    if ((e = dq_raw<D, BK>(p, P, tmS, s, rec)) != cudaSuccess) return e;
   }
   if (P.nsplit_dq > 1) {
     k_dq_reduce<<<(unsigned)(((long)p.Hkv * P.R * (D / 4) + 255) / 256), 256, 0, s>>>(p);

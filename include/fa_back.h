@@ -83,8 +83,9 @@ long fa_row_bytes(int type, int D);
 /* Workspace bytes of fa_back()'s fastest plan on the current device for this shape.  Beside the
  * per-row statistics and split partials, that plan holds binary16 copies of the decoded K and V
  * cache (2 * Hkv * M * (D + Dv) bytes) and the binary16 dS of every row and key (2 * N * H * M'
- * bytes, M' = M rounded up to 64), from which dQ is one product.  A workspace too small for dS
- * but large enough for the K/V copies gets the plan that recomputes dS in a dQ pass. */
+ * bytes, M' = M rounded up to 64), from which dQ is one product.  A workspace too small for both
+ * gets the next fastest plan that fits: the stored dS without the copies (every pass then decodes
+ * the raw cache tiles in shared memory), else the copies alone (dS recomputed in a dQ pass). */
 size_t fa_back_workspace_size(int N, int M, int H, int Hkv, int D, int Dv);
 
 /* The smallest workspace fa_back() accepts for this shape: its plan decodes the raw cache inside
@@ -94,8 +95,9 @@ size_t fa_back_workspace_size(int N, int M, int H, int Hkv, int D, int Dv);
 size_t fa_back_workspace_size_min(int N, int M, int H, int Hkv, int D, int Dv);
 
 /* The plan fa_back() runs for this shape and workspace_bytes on the current device (an SM count
- * of 152 when no device is visible): *level 2 (binary16 K'/V' copies and the stored dS), 1 (the
- * copies only) or 0 (raw rows decoded in the passes), the number of key splits of its row
+ * of 152 when no device is visible): *level 2 (binary16 K'/V' copies and the stored dS), 3 (the
+ * stored dS, raw rows decoded in the passes), 1 (the copies only) or 0 (raw rows decoded in the
+ * passes, dS recomputed in a dQ pass), the number of key splits of its row
  * passes, and the workspace bytes it uses.  Host only: nothing is enqueued.  FA_ERR_WORKSPACE
  * when workspace_bytes is below fa_back_workspace_size_min(); FA_ERR_SHAPE / FA_ERR_UNSUPPORTED
  * as for fa_back().  Any output pointer may be NULL. */
@@ -128,6 +130,20 @@ fa_status fa_back_with_stats(const float* q, const void* k, int k_type, const vo
                              const float* delta, float scale, int N, int M, int H, int Hkv, int D, int Dv,
                              int causal, float* dQ, float* dK, float* dV, void* workspace,
                              size_t workspace_bytes, void* stream);
+
+/*
+ * fa_back() restricted to the plans that keep no decoded copy of the cache: every K and V tile is
+ * read as raw cache rows and decoded in shared memory by the pass that uses it.  With a workspace
+ * of at least fa_back_workspace_size_nocopy() bytes the plan stores dS (level 3: dQ is one product
+ * over it, decoding raw K tiles once per two row tiles); with less, down to
+ * fa_back_workspace_size_min(), it recomputes dS in a dQ pass (level 0).  Arguments, results,
+ * errors and determinism as for fa_back().
+ */
+size_t fa_back_workspace_size_nocopy(int N, int M, int H, int Hkv, int D, int Dv);
+fa_status fa_back_nocopy(const float* q, const void* k, int k_type, const void* v, int v_type,
+                         const uint16_t* mask, int mask_heads, const float* dO, float scale, int N, int M,
+                         int H, int Hkv, int D, int Dv, int causal, float* dQ, float* dK, float* dV,
+                         float* lse, float* delta, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * fa_back() with three score extensions that the operation above does not have.  The pull request

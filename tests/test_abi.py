@@ -26,7 +26,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
-        ["fa_back", "fa_back_batched", "fa_back_ext", "fa_back_get_error", "fa_back_noalloc", "fa_back_plan_info", "fa_back_profile",
+        ["fa_back", "fa_back_batched", "fa_back_ext", "fa_back_get_error", "fa_back_noalloc", "fa_back_nocopy",
+         "fa_back_plan_info", "fa_back_profile", "fa_back_workspace_size_nocopy",
          "fa_back_profile_read",
          "fa_back_selftest_timeout", "fa_back_status_string", "fa_back_strided", "fa_back_strided_workspace_size",
          "fa_back_test_wait_limit",
@@ -228,12 +229,16 @@ def test_plan_levels_follow_the_workspace(L, shape):
     assert fb.fa_back_plan_info(*shape, small) == (0, 0, 1, small)
     assert fb.STATUS[fb.fa_back_plan_info(*shape, small - 1)[0]] == "FA_ERR_WORKSPACE"
     # more workspace never gives a slower plan level, and a plan never uses more than it is given
+    # (levels from slowest to fastest: 0, 1, 3, 2)
+    speed = {0: 0, 1: 1, 3: 2, 2: 3}
     last = -1
     for f in [i / 16 for i in range(17)]:
         ws = int(small + f * (full - small))
         rc, level, splits, used = fb.fa_back_plan_info(*shape, ws)
-        assert rc == 0 and level >= last and used <= ws and splits >= 1
-        last = level
+        assert rc == 0 and speed[level] >= last and used <= ws and splits >= 1
+        last = speed[level]
+    # the plan without the cache copy needs less than the fastest plan and more than the smallest
+    assert small < fb.fa_back_workspace_size_nocopy(*shape) < full
 
 
 def test_plan_of_the_long_context_shape(L):
@@ -245,6 +250,10 @@ def test_plan_of_the_long_context_shape(L):
     assert level == 1 and copies <= used < ds
     _, level, _, used = fb.fa_back_plan_info(*shape, 1 << 40)
     assert level == 2 and used >= copies + ds
+    # room for dS but not for the copies as well: dS stored, the raw cache decoded in every pass
+    nocopy = fb.fa_back_workspace_size_nocopy(*shape)
+    _, level, _, used = fb.fa_back_plan_info(*shape, nocopy)
+    assert level == 3 and ds <= used == nocopy < ds + copies
 
 
 def test_plan_info_argument_errors(L):

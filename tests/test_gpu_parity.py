@@ -24,20 +24,20 @@ def fb():
     return m
 
 
-def run_gpu(fb, p, ws=None, workspace_bytes=None):
+def run_gpu(fb, p, ws=None, workspace_bytes=None, nocopy=False):
     t = synth.device.to_torch(p, "cuda")
     out = fb.backward(t["q"], t["k"], p.k_type, t["v"], p.v_type, t["dO"], H=p.H, Hkv=p.Hkv, D=p.D, Dv=p.Dv,
                       M=p.M, scale=p.scale, causal=p.causal, mask=t["mask"], mask_heads=p.mask_heads,
-                      workspace=ws, workspace_bytes=workspace_bytes)
+                      workspace=ws, workspace_bytes=workspace_bytes, nocopy=nocopy)
     torch.cuda.synchronize()
     assert fb.fa_back_get_error() == 0
     return {k: v.cpu().numpy() for k, v in out.items()}
 
 
-def parity(fb, p, tol=NMSE_TOL, workspace_bytes=None):
+def parity(fb, p, tol=NMSE_TOL, workspace_bytes=None, nocopy=False):
     import oracle
     ref = oracle.fa_back(p)
-    got = run_gpu(fb, p, workspace_bytes=workspace_bytes)
+    got = run_gpu(fb, p, workspace_bytes=workspace_bytes, nocopy=nocopy)
     res = check_components(got, ref, tol)
     dead = ~np.isfinite(ref["lse"])
     assert np.all(got["dQ"][dead] == 0.0)
@@ -143,6 +143,67 @@ def test_configs_minimum_workspace(fb, cfg):
     p = synth.from_config(cfg)
     wmin = fb.fa_back_workspace_size_min(p.N, p.M, p.H, p.Hkv, p.D, p.Dv)
     print(cfg, parity(fb, p, workspace_bytes=wmin))
+
+
+# The plan that stores dS but keeps no decoded copy of the cache (level 3): every pass decodes raw
+# cache tiles in shared memory, and dQ is one product over the stored dS (k_dq_raw, two row tiles
+# per CTA).  Ragged tiles, both raw staging forms (rows of 16-byte multiples by TMA, others by
+# 4-byte copies), key splits, the causal tail, Dv != D and masks.
+NOCOPY_EDGE = ["ragged_f16_causal", "n_gt_m_causal", "d256_dv128", "d64_dv128_f32", "d128_dv256", "finite_mask_hm1",
+               "single_key", "single_query", "d64_q4_mask_causal", "d128_f16k_q4v", "small_f16k_q8v"]
+
+
+def nocopy_parity(fb, p):
+    wn = fb.fa_back_workspace_size_nocopy(p.N, p.M, p.H, p.Hkv, p.D, p.Dv)
+    assert 0 < wn < fb.fa_back_workspace_size(p.N, p.M, p.H, p.Hkv, p.D, p.Dv)
+    fb.fa_back_profile(True)
+    res = parity(fb, p, workspace_bytes=wn, nocopy=True)
+    fb.fa_back_profile(False)
+    launched = {k for k, v in fb.fa_back_profile_read().items() if v[1] > 0}
+    assert "k_dq_raw" in launched and "k_predecode" not in launched, launched
+    assert "k_rows_dq" not in launched and "k_dq_gemm" not in launched, launched
+    return res
+
+
+@pytest.mark.parametrize("cfg", ["0", "1", "1c", "1t", "2", "3"])
+def test_configs_nocopy(fb, cfg):
+    print(cfg, nocopy_parity(fb, synth.from_config(cfg)))
+
+
+@pytest.mark.parametrize("name", NOCOPY_EDGE)
+def test_edge_cases_nocopy(fb, name):
+    p = synth.make_problem(name, seed=2000 + sorted(EDGE).index(name), **EDGE[name])
+    print(name, nocopy_parity(fb, p))
+
+
+@pytest.mark.parametrize("name", ["row_range_d128", "d64_q4v_17k"])
+def test_precision_cases_nocopy(fb, name):
+    import oracle
+    p = synth.make_problem(name, seed=3000 + sorted(PRECISION).index(name), **PRECISION[name])
+    ref = oracle.fa_back(p)
+    got = run_gpu(fb, p, nocopy=True)
+    print(name, check_components(got, ref))
+    rn = row_nmse(got["dQ"], ref["dQ"])
+    live = np.isfinite(ref["lse"])
+    assert np.all(rn[live] <= NMSE_TOL), float(np.max(rn[live]))
+
+
+def test_nocopy_reruns_are_bit_identical(fb):
+    p = synth.from_config("3")
+    a = run_gpu(fb, p, nocopy=True)
+    b = run_gpu(fb, p, nocopy=True)
+    for k in a:
+        assert np.array_equal(a[k], b[k], equal_nan=True), k
+
+
+def test_nocopy_below_its_workspace_runs_level_0(fb):
+    p = synth.from_config("1")
+    wmin = fb.fa_back_workspace_size_min(p.N, p.M, p.H, p.Hkv, p.D, p.Dv)
+    fb.fa_back_profile(True)
+    print(parity(fb, p, workspace_bytes=wmin, nocopy=True))
+    fb.fa_back_profile(False)
+    launched = {k for k, v in fb.fa_back_profile_read().items() if v[1] > 0}
+    assert "k_rows_dq" in launched and "k_dq_raw" not in launched and "k_predecode" not in launched, launched
 
 
 @pytest.mark.parametrize("N,M", [(0, 64), (16, 0)])
