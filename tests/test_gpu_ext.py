@@ -52,6 +52,9 @@ def level_workspace(fb, p, level):
         return lo
     if level == 2:
         return hi
+    if level == 3:  # the stored dS without the K'/V' copies (fa_back_ext picks it when the copies do not fit)
+        w = fb.fa_back_workspace_size_nocopy(p.N, p.M, p.H, p.Hkv, p.D, p.Dv)
+        return w if fb.fa_back_plan_info(p.N, p.M, p.H, p.Hkv, p.D, p.Dv, w)[1] == 3 else None
     lv = lambda w: fb.fa_back_plan_info(p.N, p.M, p.H, p.Hkv, p.D, p.Dv, w)[1]
     a, b = lo, hi  # lv(a) = 0 < lv(b): the smallest size with a level of at least 1
     while b - a > 256:
@@ -95,11 +98,31 @@ EXT = {
 }
 
 
-@pytest.mark.parametrize("level", [2, 1, 0])
+@pytest.mark.parametrize("level", [2, 3, 1, 0])
 @pytest.mark.parametrize("name", sorted(EXT))
 def test_ext_cases(fb, name, level):
     p = synth.make_problem(name, seed=7000 + sorted(EXT).index(name), **EXT[name])
     print(name, level, ext_parity(fb, p, level))
+
+
+@pytest.mark.slow
+def test_ext_on_the_long_context_shape_sampled(fb):
+    """All three extensions at N2048/M75520/H24/Hkv4/D256 (q8_0, causal tail), plan level 3: every
+    lse/delta, 48 dQ rows and 128 dK/dV keys against the oracle, and dsinks."""
+    import oracle
+    p = synth.from_config("4")
+    p = synth.make_problem("ext_long", N=p.N, M=p.M, H=p.H, Hkv=p.Hkv, D=p.D, Dv=p.Dv, k_type="q8_0",
+                           v_type="q8_0", causal=True, seed=7100, alibi=True, softcap=20.0, sinks=1.0)
+    w = level_workspace(fb, p, 3)
+    got = run_ext(fb, p, workspace_bytes=w)
+    rows = synth.sample_indices(7101, synth.gen.S_SAMPLE, p.N, 48)
+    keys = synth.sample_indices(7101, synth.gen.S_SAMPLE + 1, p.M, 128)
+    ref = oracle.fa_back(p, dq_rows=rows, dkv_keys=keys)
+    sub = {"lse": got["lse"], "delta": got["delta"], "dQ": got["dQ"][rows], "dK": got["dK"][keys],
+           "dV": got["dV"][keys]}
+    print(check_components(sub, ref))
+    # dsinks sums over every row: the sampled oracle has all lse and delta, so its dsinks is exact
+    assert nmse(got["dsinks"], ref["dsinks"]) <= NMSE_TOL
 
 
 def test_ext_off_is_fa_back(fb):
