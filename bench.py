@@ -365,8 +365,8 @@ def run_ours(args):
                                "note": "lse and delta given; the LSE/D pass is skipped; same F_alg"},
         "fa_back_nocopy": {"ms": nc_ms, "TFLOP/s": job_tflops(world, p.flops(), nc_ms),
                            "path_roofline_frac": p.flops() / (peak_v * 1e12) / (nc_ms * 1e-3),
-                           "workspace_bytes": wnc,
-                           "plan": fb.fa_back_plan_info(p.N, p.M, p.H, p.Hkv, p.D, p.Dv, wnc), "kernels_ms": nc_kern,
+                           "workspace_bytes": wnc, "plan_level": 3 if "k_dq_raw" in nc_kern else 0,
+                           "kernels_ms": nc_kern,
                            "note": "no decoded copy of the cache: raw K/V tiles decoded in shared memory by every "
                                    "pass, dS stored (plan level 3); fa_back_nocopy() with "
                                    "fa_back_workspace_size_nocopy() bytes"},
