@@ -45,22 +45,19 @@ def run_ext(fb, p, workspace_bytes=None, profile=False):
 
 
 def level_workspace(fb, p, level):
-    """A workspace size whose plan has the given level (None if no size gives it)."""
+    """A workspace size whose plan has the given level (None if no size gives it).  Levels 1 and 3
+    sit between the smallest and the fastest plan's sizes; a scan of that range finds them."""
     lo = fb.fa_back_workspace_size_min(p.N, p.M, p.H, p.Hkv, p.D, p.Dv)
     hi = fb.fa_back_workspace_size(p.N, p.M, p.H, p.Hkv, p.D, p.Dv)
     if level == 0:
         return lo
     if level == 2:
         return hi
-    if level == 3:  # the stored dS without the K'/V' copies (fa_back_ext picks it when the copies do not fit)
-        w = fb.fa_back_workspace_size_nocopy(p.N, p.M, p.H, p.Hkv, p.D, p.Dv)
-        return w if fb.fa_back_plan_info(p.N, p.M, p.H, p.Hkv, p.D, p.Dv, w)[1] == 3 else None
-    lv = lambda w: fb.fa_back_plan_info(p.N, p.M, p.H, p.Hkv, p.D, p.Dv, w)[1]
-    a, b = lo, hi  # lv(a) = 0 < lv(b): the smallest size with a level of at least 1
-    while b - a > 256:
-        m = (a + b) // 2
-        a, b = (a, m) if lv(m) >= 1 else (m, b)
-    return b if lv(b) == 1 else None
+    for k in range(401):
+        w = lo + (hi - lo) * k // 400
+        if fb.fa_back_plan_info(p.N, p.M, p.H, p.Hkv, p.D, p.Dv, w)[1] == level:
+            return w
+    return None
 
 
 def ext_parity(fb, p, level=2):
