@@ -9,8 +9,8 @@
 // the kernel (dS is read once, like k_dq_gemm's).
 //
 // Warp roles: 0 producer (dS panels and raw K rows; the whole warp for 4-byte copies), 1 tensor
-// memory owner and MMA issuer, 2 .. 2+NDEC-1 decoders, which afterwards read the accumulators
-// out (warps 2-5 row tile 0, warps 6-9 row tile 1: every tensor-memory lane quarter twice).
+// memory owner and MMA issuer, 2 .. 2+NDEC-1 decoders; warps 2-9 then read the accumulators out
+// (warps 2-5 row tile 0, warps 6-9 row tile 1: every tensor-memory lane quarter twice).
 #pragma once
 #include "fa_kernels.cuh"
 
@@ -18,7 +18,7 @@ namespace fab {
 
 template <int D, int BK>
 struct DqRawCfg {
-  static constexpr int NDEC = 8;
+  static constexpr int NDEC = 12;  // decoding one K tile takes longer than its two products
   static constexpr int NT = 32 * (2 + NDEC);
   static constexpr int AB = 128 * BK * 2;  // one row tile's dS panels for one key tile
   static constexpr int KB = BK * D * 2;    // binary16 K' tile
@@ -249,38 +249,40 @@ static __global__ void __launch_bounds__(DqRawCfg<D, BK>::NT, 1)
     }
     // epilogue: warps 2-5 read row tile 0's accumulator, warps 6-9 row tile 1's
     const int a = (warp - 2) >> 2;
-    const int q4 = warp & 3;
-    const int row = q4 * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const int qt = qt0 + a;
-    const int r = qt * 128 + row;
-    const bool rvalid = qt < p.nQT && r < R;
-    const int i = rvalid ? r / G : 0;
-    const int h = hk * G + (rvalid ? r % G : 0);
-    float* out = !rvalid ? nullptr
-                 : p.nsplit == 1 ? p.dQ + ((size_t)i * p.H + h) * D
-                                 : p.dqpart + (((size_t)split * p.Hkv + hk) * R + r) * D;
-    const Stats st = *p.st;
-    const float dq_fac = !rvalid ? 0.f
-                         : rows_need_own_scale(st) ? st.dq_fac * (st.lam / p.lamr[(size_t)hk * R + r])
-                                                   : st.dq_fac;
-    const bool have = (a ? nt[1] : nt[0]) > 0 && wait(&bar[Q_ACC_FULL], 0);
-    if (have) tc_fence_after();
+    if (a < 2) {
+      const int q4 = warp & 3;
+      const int row = q4 * 32 + lane;
+      const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+      const int qt = qt0 + a;
+      const int r = qt * 128 + row;
+      const bool rvalid = qt < p.nQT && r < R;
+      const int i = rvalid ? r / G : 0;
+      const int h = hk * G + (rvalid ? r % G : 0);
+      float* out = !rvalid ? nullptr
+                   : p.nsplit == 1 ? p.dQ + ((size_t)i * p.H + h) * D
+                                   : p.dqpart + (((size_t)split * p.Hkv + hk) * R + r) * D;
+      const Stats st = *p.st;
+      const float dq_fac = !rvalid ? 0.f
+                           : rows_need_own_scale(st) ? st.dq_fac * (st.lam / p.lamr[(size_t)hk * R + r])
+                                                     : st.dq_fac;
+      const bool have = (a ? nt[1] : nt[0]) > 0 && wait(&bar[Q_ACC_FULL], 0);
+      if (have) tc_fence_after();
 #pragma unroll 1
-    for (int c = 0; c < D; c += 32) {
-      float v[32];
-      if (have) {
-        tmem_ld32(tbase + a * D + lane_off + c, v);
-        tmem_ld_wait();
-      } else {
+      for (int c = 0; c < D; c += 32) {
+        float v[32];
+        if (have) {
+          tmem_ld32(tbase + a * D + lane_off + c, v);
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-        for (int x = 0; x < 32; ++x) v[x] = 0.f;
-      }
-      if (out) {
+          for (int x = 0; x < 32; ++x) v[x] = 0.f;
+        }
+        if (out) {
 #pragma unroll
-        for (int x = 0; x < 32; x += 4)
-          *reinterpret_cast<float4*>(out + c + x) =
-              make_float4(v[x] * dq_fac, v[x + 1] * dq_fac, v[x + 2] * dq_fac, v[x + 3] * dq_fac);
+          for (int x = 0; x < 32; x += 4)
+            *reinterpret_cast<float4*>(out + c + x) =
+                make_float4(v[x] * dq_fac, v[x + 1] * dq_fac, v[x + 2] * dq_fac, v[x + 3] * dq_fac);
+        }
       }
     }
   }
