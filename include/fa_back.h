@@ -32,7 +32,9 @@
  * workspace.  The library allocates no device memory and keeps no reference after return.
  *
  * Asynchrony: fa_back() validates its arguments on the host, enqueues its kernels on `stream`
- * and returns without synchronising.  Outputs are valid once the stream's work completes.
+ * and returns without synchronising.  Outputs are valid once the stream's work completes.  A
+ * call may be captured into a CUDA graph (stream capture): its host work runs at the call and
+ * only kernel launches are enqueued, so a replay reruns the backward on the same buffers.
  *
  * Errors: argument errors are reported before anything is enqueued and leave the outputs
  * untouched.  A launch failure returns FA_ERR_CUDA.  A kernel that gives up on a bounded wait

@@ -374,3 +374,37 @@ def test_golden_worked_example(fb, name):
     got = run_gpu(fb, p)
     print(check_components(got, want))
     assert np.all(got["dQ"][~np.isfinite(want["lse"])] == 0.0)
+
+
+def test_captured_in_a_cuda_graph_and_replayed(fb):
+    """fa_back enqueues only kernels on the caller's stream (its host work, argument checks and
+    tensor maps, runs at the call), so a CUDA graph captured around one call replays it: the
+    replay's outputs equal a direct call's bit for bit, also after the inputs change in place."""
+    p = synth.from_config("3")
+    t = synth.device.to_torch(p, "cuda")
+    kw = dict(H=p.H, Hkv=p.Hkv, D=p.D, Dv=p.Dv, M=p.M, scale=p.scale, causal=p.causal, mask=t["mask"],
+              mask_heads=p.mask_heads)
+    ws = fb.Workspace("cuda")
+    ws.get(fb.fa_back_workspace_size(p.N, p.M, p.H, p.Hkv, p.D, p.Dv))
+    direct = fb.backward(t["q"], t["k"], p.k_type, t["v"], p.v_type, t["dO"], workspace=ws, **kw)
+    out = {k: torch.empty_like(v) for k, v in direct.items()}
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            fb.backward(t["q"], t["k"], p.k_type, t["v"], p.v_type, t["dO"], workspace=ws, out=out, **kw)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert fb.fa_back_get_error() == 0
+    for k in direct:
+        assert torch.equal(out[k], direct[k]), k
+    # new values in the captured input buffers: the replay follows them
+    t["dO"].mul_(0.5)
+    again = fb.backward(t["q"], t["k"], p.k_type, t["v"], p.v_type, t["dO"], workspace=fb.Workspace("cuda"), **kw)
+    g.replay()
+    torch.cuda.synchronize()
+    for k in again:
+        assert torch.equal(out[k], again[k]), k
