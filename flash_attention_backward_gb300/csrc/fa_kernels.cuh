@@ -602,7 +602,7 @@ static __global__ void __launch_bounds__(1024) k_finalize(Params p) {
   const float invM = p.M > 0 ? 1.f / (float)p.M : 0.f;
   for (int idx = tid; idx < p.Hkv * p.Dv; idx += blockDim.x) {
     float s = 0.f;
-#pragma unroll 8
+#pragma unroll 32
     for (int b = 0; b < p.nbv; ++b) s += p.vsum[((size_t)b * p.Hkv) * p.Dv + idx];
     const float r = s * invM;
     p.rmean[idx] = r;
