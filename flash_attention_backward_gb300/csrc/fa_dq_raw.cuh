@@ -5,8 +5,8 @@
 // TMA-loads both row tiles' dS panels and the tile's raw K rows, decodes the rows once into a
 // binary16 K' tile in shared memory, and issues dQ_a += dS_a K' for both row tiles a = 0, 1, with
 // both 128 x D accumulators in tensor memory (2 D <= 512 columns).  Decoding each K tile once for
-// 256 rows halves the decode work of a one-tile CTA; it overlaps the stream of dS, which bounds
-// the kernel (dS is read once, like k_dq_gemm's).
+// 256 rows halves the decode work of a one-tile CTA, and the decode overlaps the stream of dS
+// (read once, like k_dq_gemm's).
 //
 // Warp roles: 0 producer (dS panels and raw K rows; the whole warp for 4-byte copies), 1 tensor
 // memory owner and MMA issuer, 2 .. 2+NDEC-1 decoders; warps 2-9 then read the accumulators out
@@ -18,7 +18,7 @@ namespace fab {
 
 template <int D, int BK>
 struct DqRawCfg {
-  static constexpr int NDEC = 12;  // decoding one K tile takes longer than its two products
+  static constexpr int NDEC = 12;  // a K tile's decode takes about as long as its two products
   static constexpr int NT = 32 * (2 + NDEC);
   static constexpr int AB = 128 * BK * 2;  // one row tile's dS panels for one key tile
   static constexpr int KB = BK * D * 2;    // binary16 K' tile
