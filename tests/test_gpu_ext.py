@@ -1,15 +1,16 @@
 """Score extensions (fa_back_ext): ALiBi slopes, a logit soft cap and per-head sink logits, CUDA
 path against the oracle's double-precision definition of each, on every plan level.
 
-Tolerance as for the plain operation: NMSE <= 1e-5 per component (dQ, dK, dV, lse, delta and,
-with sinks, dsinks); lse = -inf positions agree exactly; rows without a key give delta = 0 and a
-zero dQ row.
+Tolerance as for the plain operation: NMSE <= 1e-5 per component (dQ, dK, dV, lse, delta);
+lse = -inf positions agree exactly; rows without a key give delta = 0 and a zero dQ row.  dsinks,
+a sum over rows whose terms can cancel, passes at NMSE <= 1e-5 or within delta's per-row error
+of the sum of its terms' magnitudes (metrics.check_dsinks).
 """
 import numpy as np
 import pytest
 
 import synth
-from metrics import NMSE_TOL, check_components, nmse
+from metrics import NMSE_TOL, check_components, check_dsinks, nmse
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -73,8 +74,7 @@ def ext_parity(fb, p, level=2):
     assert np.all(got["dQ"][dead] == 0.0)
     if p.sinks is not None:
         assert "k_sink_grad" in launched, launched
-        res["dsinks"] = nmse(got["dsinks"], ref["dsinks"])
-        assert res["dsinks"] <= NMSE_TOL, res
+        res["dsinks"] = check_dsinks(got["dsinks"], ref, p.sinks)
     return res
 
 
@@ -119,7 +119,7 @@ def test_ext_on_the_long_context_shape_sampled(fb):
            "dV": got["dV"][keys]}
     print(check_components(sub, ref))
     # dsinks sums over every row: the sampled oracle has all lse and delta, so its dsinks is exact
-    assert nmse(got["dsinks"], ref["dsinks"]) <= NMSE_TOL
+    check_dsinks(got["dsinks"], ref, p.sinks)
 
 
 def test_ext_off_is_fa_back(fb):

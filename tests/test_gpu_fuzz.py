@@ -1,0 +1,93 @@
+"""Seeded random problems against the oracle, on every plan level.
+
+Each case draws its shape (ragged N and M, GQA ratio, D and Dv), cache types, mask kind, causal
+tail and score extensions from a seeded generator, then runs the CUDA path with the workspace
+of one plan level and compares every component with the oracle (NMSE <= 1e-5; lse = -inf
+positions exact; rows without keys give delta = 0 and dQ = 0; dsinks as check_dsinks states).
+The draws cover combinations that the hand-picked cases do not.
+"""
+import numpy as np
+import pytest
+
+import synth
+from metrics import check_components, check_dsinks
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TYPES = ["f32", "f16", "q8_0", "q4_0"]
+HEADS = [(1, 1), (2, 1), (4, 2), (6, 2), (8, 2), (4, 4), (12, 4)]
+DIMS = [64, 128, 256]
+
+
+def draw(case: int) -> dict:
+    """The problem of fuzz case `case` (a pure function of the case number)."""
+    rng = np.random.default_rng(91000 + case)
+    H, Hkv = HEADS[rng.integers(len(HEADS))]
+    D = int(rng.choice(DIMS))
+    Dv = int(rng.choice(DIMS)) if rng.random() < 0.3 else D
+    N = int(rng.integers(1, 160))
+    M = int(rng.integers(1, 1500))
+    kw = dict(N=N, M=M, H=H, Hkv=Hkv, D=D, Dv=Dv, k_type=TYPES[rng.integers(4)], v_type=TYPES[rng.integers(4)],
+              causal=bool(rng.random() < 0.5), seed=92000 + case)
+    mk = rng.random()
+    if mk < 0.25:
+        kw.update(mask="random", mask_p=float(rng.uniform(0.0, 0.3)), full_rows=int(rng.integers(0, 3)),
+                  mask_heads=int(rng.choice([1, H])))
+    elif mk < 0.4:
+        kw.update(mask="finite", mask_p=float(rng.uniform(0.0, 0.2)), full_rows=int(rng.integers(0, 2)),
+                  mask_heads=int(rng.choice([1, H])))
+    if rng.random() < 0.3:  # score extensions, each on its own
+        kw.update(alibi=bool(rng.random() < 0.5), softcap=float(rng.choice([0.0, 2.0, 10.0])),
+                  sinks=float(rng.uniform(0.5, 2.0)) if rng.random() < 0.5 else None)
+    return kw
+
+
+@pytest.fixture(scope="module")
+def fb():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import flash_attention_backward_gb300 as m
+    from flash_attention_backward_gb300 import build
+    build.build()
+    return m
+
+
+def level_workspace(fb, p, level):
+    lo = fb.fa_back_workspace_size_min(p.N, p.M, p.H, p.Hkv, p.D, p.Dv)
+    hi = fb.fa_back_workspace_size(p.N, p.M, p.H, p.Hkv, p.D, p.Dv)
+    if level == 0:
+        return lo
+    if level == 2:
+        return hi
+    for k in range(201):
+        w = lo + (hi - lo) * k // 200
+        if fb.fa_back_plan_info(p.N, p.M, p.H, p.Hkv, p.D, p.Dv, w)[1] == level:
+            return w
+    return None
+
+
+@pytest.mark.parametrize("case", range(32))
+def test_fuzz_against_the_oracle(fb, case):
+    import oracle
+    kw = draw(case)
+    p = synth.make_problem(f"fuzz{case}", **kw)
+    level = case % 4  # 0, 1, 2, 3 in turn
+    ws = level_workspace(fb, p, level)
+    if ws is None:
+        ws, level = fb.fa_back_workspace_size(p.N, p.M, p.H, p.Hkv, p.D, p.Dv), 2
+    t = synth.device.to_torch(p, "cuda")
+    dev = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to("cuda")
+    out = fb.backward(t["q"], t["k"], p.k_type, t["v"], p.v_type, t["dO"], H=p.H, Hkv=p.Hkv, D=p.D, Dv=p.Dv,
+                      M=p.M, scale=p.scale, causal=p.causal, mask=t["mask"], mask_heads=p.mask_heads,
+                      workspace_bytes=ws, alibi_slopes=dev(p.alibi), softcap=p.softcap, sinks=dev(p.sinks))
+    torch.cuda.synchronize()
+    assert fb.fa_back_get_error() == 0
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    ref = oracle.fa_back(p)
+    res = check_components(got, ref)
+    dead = ~np.isfinite(ref["lse"])
+    assert np.all(got["dQ"][dead] == 0.0)
+    if p.sinks is not None:
+        res["dsinks"] = check_dsinks(got["dsinks"], ref, p.sinks)
+    print(case, level, {k: v for k, v in kw.items() if k != "seed"}, res)
