@@ -91,3 +91,43 @@ def test_fuzz_against_the_oracle(fb, case):
     if p.sinks is not None:
         res["dsinks"] = check_dsinks(got["dsinks"], ref, p.sinks)
     print(case, level, {k: v for k, v in kw.items() if k != "seed"}, res)
+
+
+def draw_precision(case: int) -> dict:
+    """Precision stress inside the envelope the design states (logits up to about 2): a V that is
+    nearly constant along the keys (offset much larger than its spread), tiny dO, per-row ranges of
+    Q and dO rows, larger Q."""
+    kw = draw(1000 + case)
+    rng = np.random.default_rng(93000 + case)
+    kind = case % 4
+    if kind == 0:
+        kw.update(v_offset=float(rng.choice([3.0, 10.0])), v_sigma=float(rng.choice([0.01, 0.05])))
+    elif kind == 1:
+        kw.update(do_sigma=1e-6)
+    elif kind == 2:
+        kw.update(row_decades=float(rng.uniform(1.0, 2.5)), scale=1e-3 / kw["D"] ** 0.5)
+    else:
+        kw.update(q_sigma=2.0)
+    for k in ("alibi", "softcap", "sinks"):  # the plain operation
+        kw.pop(k, None)
+    return kw
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_fuzz_precision_against_the_oracle(fb, case):
+    import oracle
+    kw = draw_precision(case)
+    p = synth.make_problem(f"fuzzp{case}", **kw)
+    level = (case // 4) % 4
+    ws = level_workspace(fb, p, level)
+    if ws is None:
+        ws, level = fb.fa_back_workspace_size(p.N, p.M, p.H, p.Hkv, p.D, p.Dv), 2
+    t = synth.device.to_torch(p, "cuda")
+    out = fb.backward(t["q"], t["k"], p.k_type, t["v"], p.v_type, t["dO"], H=p.H, Hkv=p.Hkv, D=p.D, Dv=p.Dv,
+                      M=p.M, scale=p.scale, causal=p.causal, mask=t["mask"], mask_heads=p.mask_heads,
+                      workspace_bytes=ws)
+    torch.cuda.synchronize()
+    assert fb.fa_back_get_error() == 0
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    res = check_components(got, oracle.fa_back(p))
+    print(case, level, {k: v for k, v in kw.items() if k != "seed"}, res)
