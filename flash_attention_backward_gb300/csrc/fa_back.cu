@@ -136,8 +136,8 @@ static int device_sms(int* major, int* minor) {
 // (the read-out measures each kernel from the marker recorded before it)
 static const char* const kKernelNames[kProfSlots] = {
     "k_row_stats", "k_vsum", "k_finalize", "k_convert", "k_predecode", "k_rows_lse", "k_lse_merge", "k_rows_dq",
-    "k_dq_reduce", "k_cols", "k_dq_gemm", "k_stats_in", "k_fwd_lse", "k_fwd_o", "k_o_reduce", "k_cols_rowscale",
-    "k_sink_grad", "k_dq_raw"};
+    "k_dq_reduce", "k_cols", "k_dq_gemm", "k_stats_in", "k_fwd", "k_fwd_merge", "k_cols_rowscale", "k_sink_grad",
+    "k_dq_raw"};
 Profiler g_prof;
 
 // Failure-detection hook: the wait limit of the next call's kernels plus one (0: none pending).

@@ -1362,18 +1362,16 @@ static __global__ void __launch_bounds__(Rows2Cfg<D, Dv, BK, MODE>::NT, 1)
 
 template <int D, int Dv, int BK, int MODE>
 struct Rows3Cfg {
-  // MODE 0: LSE/D pass; 1: dQ pass; 2: forward O pass (O += P V'); 3: forward LSE pass (no dP)
-  static constexpr bool ROWQ = MODE == 1 || MODE == 2;    // Q tile in shared memory; a product
-                                                          // over the row's P or dS panel
-  static constexpr bool HAS_DP = MODE == 0 || MODE == 1;  // dP = dO' V'^T is formed
-  static constexpr bool LOADS_V = MODE != 3;
+  // MODE 0: LSE/D pass; 1: dQ pass
+  static_assert(MODE == 0 || MODE == 1, "pass");
+  static constexpr bool ROWQ = MODE == 1;  // Q tile in shared memory; a product over the row's dS panel
   static constexpr int QB = ROWQ ? 128 * D * 2 : 0;
   static constexpr int KB = BK * D * 2, VB = BK * Dv * 2;
   static constexpr int SB = ROWQ ? 128 * BK * 2 : 0;
   static constexpr int NCH = BK / 32;  // 32-key chunks per tile
   static constexpr int NSOFT = 4 * NCH;
   static constexpr int NT = 32 * (2 + NSOFT);
-  static constexpr int MERGE_BYTES = (MODE == 0 || MODE == 3) ? (NCH - 1) * 128 * 3 * 4 : 0;
+  static constexpr int MERGE_BYTES = MODE == 0 ? (NCH - 1) * 128 * 3 * 4 : 0;
   static constexpr int BAR_BYTES = 512 + MERGE_BYTES;
   static constexpr int SMEM_MAX = 232448;
   static constexpr int AVAIL = SMEM_MAX - 1024 - BAR_BYTES - QB - SB;
@@ -1399,14 +1397,13 @@ struct Rows3Cfg {
   static constexpr int OFF_S = OFF_V + VSTAGES * VB;
   static constexpr int OFF_BAR = OFF_S + SB;
   static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;  // + 1024 for aligning the base
-  // tensor-memory columns: [Q' (LSE passes)] [dO' (MODE 0, 1)] [S] [dP (MODE 0, 1)] [accumulator:
-  // dQ (MODE 1) or O (MODE 2)]
+  // tensor-memory columns: [Q' (LSE/D pass)] [dO'] [S] [dP] [dQ accumulator (dQ pass)]
   static constexpr int T_Q = 0;
   static constexpr int T_O = ROWQ ? 0 : D / 2;
-  static constexpr int T_S = MODE == 2 ? 0 : T_O + Dv / 2;
+  static constexpr int T_S = T_O + Dv / 2;
   static constexpr int T_P = T_S + BK;
-  static constexpr int T_ACC = HAS_DP ? T_P + BK : T_S + BK;
-  static constexpr int ACC_N = MODE == 1 ? D : MODE == 2 ? Dv : 0;  // accumulator columns
+  static constexpr int T_ACC = T_P + BK;
+  static constexpr int ACC_N = ROWQ ? D : 0;  // accumulator columns
   static constexpr int TCOLS = pow2_at_least(T_ACC + ACC_N);
   static_assert(KB + VB <= AVAIL && SMEM <= SMEM_MAX, "shared memory budget");
   static_assert(TCOLS <= 512, "tensor memory budget");
@@ -1427,7 +1424,7 @@ enum {
   R3_ACC_FULL,
   R3_Q_FULL,
   R3_OPS_READY,
-  R3_DRAIN0,  // the producer's dQ / O products, committed after an abort
+  R3_DRAIN0,  // the producer's dQ products, committed after an abort
   R3_DRAIN1,  // the issuer's S/dP products, committed after an abort
   R3_COUNT
 };
@@ -1498,22 +1495,20 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tmK);
-      if (C::LOADS_V) prefetch_tmap(&tmV);
+      prefetch_tmap(&tmV);
       if (C::ROWQ && ntiles > 0) {
         mbar_arrive_expect_tx(&bar[R3_Q_FULL], (uint32_t)C::QB);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) tma_load_3d(sQ + c * 128 * 128, &tmQ, &bar[R3_Q_FULL], c * 64, r0, hk);
       }
-      // the product over the row tile's dS / P panel, beside the S/dP stream of warp 1:
-      // dQ += dS(t) K'(t) (dQ pass) or O += P(t) V'(t) (forward O pass); it frees the stage it read
+      // the dQ pass's product over the row tile's dS panel, beside the S/dP stream of warp 1:
+      // dQ += dS(t) K'(t); it frees the K' stage it read
       auto issue_dq = [&](int t) {
         if constexpr (C::ROWQ) {
-          constexpr int NN = MODE == 1 ? D : Dv;
-          constexpr uint32_t ID_A = idesc_f16(128, NN, false, true);
+          constexpr uint32_t ID_A = idesc_f16(128, D, false, true);
           tc_fence_after();
           const uint64_t da = sdesc_sw128(smem_u32(sS), 16, 1024);
-          const uint64_t db = MODE == 1 ? sdesc_sw128(smem_u32(sK + (t % C::KSTAGES) * C::KB), BK * 128, 1024)
-                                        : sdesc_sw128(smem_u32(sV + (t % C::VSTAGES) * C::VB), BK * 128, 1024);
+          const uint64_t db = sdesc_sw128(smem_u32(sK + (t % C::KSTAGES) * C::KB), BK * 128, 1024);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             mma_f16(tbase + C::T_ACC, sdesc_adv(da, (k / 4) * (128 * 128) + (k % 4) * 32), sdesc_adv(db, k * 2048),
@@ -1522,14 +1517,11 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
             mma_commit(&bar[R3_ACC_FULL]);
           } else {
             mma_commit(&bar[R3_DS_EMPTY]);
-            if (MODE == 1)
-              mma_commit(&bar[R3_K_EMPTY + t % C::KSTAGES]);
-            else
-              mma_commit(&bar[R3_V_EMPTY + t % C::VSTAGES]);
+            mma_commit(&bar[R3_K_EMPTY + t % C::KSTAGES]);
           }
         }
       };
-      const int ndq = C::ROWQ ? ntiles : 0, nvt = C::LOADS_V ? ntiles : 0;
+      const int ndq = C::ROWQ ? ntiles : 0, nvt = ntiles;
       int kt = 0, vt = 0, nd = 0;
       uint64_t t0 = globaltimer_ns();
       while (kt < ntiles || vt < nvt || nd < ndq) {
@@ -1595,8 +1587,7 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
             mma_f16_tmem_a(tS, tQ + k * 8, bd, ID_S, k > 0);
         }
         mma_commit(&bar[R3_S_FULL]);
-        if (MODE != 1) mma_commit(&bar[R3_K_EMPTY + ks]);  // only the dQ pass reads K'(t) again
-        if (!C::HAS_DP) continue;
+        if (!C::ROWQ) mma_commit(&bar[R3_K_EMPTY + ks]);  // only the dQ pass reads K'(t) again
         if (!wait(&bar[R3_V_FULL + vs], (t / C::VSTAGES) & 1) || !wait(&bar[R3_P_FREE], (t & 1) ^ 1)) break;
         tc_fence_after();
         const uint64_t dv = sdesc_sw128(smem_u32(sV + vs * C::VB), 16, 1024);
@@ -1622,16 +1613,16 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
     float lse2 = -CUDART_INF_F, dl = 0.f;
     if (C::ROWQ && rvalid) {
       lse2 = p.lse2[(size_t)hk * R + r];
-      if (MODE == 1) dl = p.dlt[(size_t)hk * R + r];
+      dl = p.dlt[(size_t)hk * R + r];
     }
     const bool live = C::ROWQ ? (lse2 > -CUDART_INF_F) : rvalid;
     // the dQ pass scales this row's dS by its own power of two lamr (the product sums over keys only)
-    const float lam = (MODE == 1 && rvalid) ? p.lamr[(size_t)hk * R + r] : st.lam;
+    const float lam = (C::ROWQ && rvalid) ? p.lamr[(size_t)hk * R + r] : st.lam;
     const float c2 = st.c2, dq_fac = st.dq_fac * (st.lam / lam);
     // 2^(t2 + nlse2) = p (0 on a dead row); the exponent also carries log2 of the power-of-two
-    // multiplier of the product's binary16 panel, so the exponential yields it directly: lam * p
-    // in the dQ pass (dS = lam p (dP - delta)), sP * p in the forward O pass
-    const float nlse2 = live ? -lse2 + (float)ilogbf(MODE == 1 ? lam : st.sP) : -CUDART_INF_F;
+    // multiplier lam of the dS panel, so the exponential yields lam * p directly
+    // (dS = lam p (dP - delta))
+    const float nlse2 = live ? -lse2 + (float)ilogbf(lam) : -CUDART_INF_F;
     const float t2off = C::ROWQ ? nlse2 : 0.f;
     const uint32_t sS_u = smem_u32(sS);
     float m2 = -CUDART_INF_F, l = 0.f, lc = 0.f, sd = 0.f, sdc = 0.f;
@@ -1655,7 +1646,7 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
       };
       const size_t rowq = (size_t)hk * R + (rvalid ? r : 0);
       if (!C::ROWQ) put_row(p.q16 + rowq * D, D, C::T_Q);
-      if (C::HAS_DP) put_row(p.do16 + rowq * Dv, Dv, C::T_O);
+      put_row(p.do16 + rowq * Dv, Dv, C::T_O);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -1674,7 +1665,7 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
       if (lane == 0) mbar_arrive(&bar[R3_S_FREE]);
       // log2-domain scores (dQ pass: already minus lse, plus log2(lam)); masked keys -> -inf
       if constexpr (EXT) {
-        ext_scores<MODE == 1 ? 1 : 0>(s, nullptr, j0 + col0, r, hk, t2off, 0.f, jlast, mrow, st, p.alibi, G,
+        ext_scores<MODE>(s, nullptr, j0 + col0, r, hk, t2off, 0.f, jlast, mrow, st, p.alibi, G,
                                       p.M - p.N);
       } else if (mrow == nullptr && (long)(j0 + col0 + 31) <= jlast) {
 #pragma unroll
@@ -1709,24 +1700,22 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
         }
       } else {
 #pragma unroll
-        for (int n = 0; n < 32; ++n) s[n] = ex2(s[n]);  // lam * p or sP * p; 0 for masked keys, dead rows
+        for (int n = 0; n < 32; ++n) s[n] = ex2(s[n]);  // lam * p; 0 for masked keys, dead rows
       }
-      if (C::HAS_DP) {
-        if (!wait(&bar[R3_P_FULL], t & 1)) break;
-        tc_fence_after();
-        tmem_ld32(tbase + C::T_P + lane_off + col0, dp);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[R3_P_FREE]);
-      }
+      if (!wait(&bar[R3_P_FULL], t & 1)) break;
+      tc_fence_after();
+      tmem_ld32(tbase + C::T_P + lane_off + col0, dp);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[R3_P_FREE]);
       if (!C::ROWQ) {
         if (any) {
           float cl = 0.f, cs = 0.f;
 #pragma unroll
           for (int n = 0; n < 32; ++n) {
             cl += s[n];
-            if (C::HAS_DP) cs = fmaf(s[n], dp[n], cs);
+            cs = fmaf(s[n], dp[n], cs);
           }
           // compensated accumulation of the chunk sums
           float y = cl - lc, tt = l + y;
@@ -1737,12 +1726,8 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
       } else {
         uint32_t pk[16];
 #pragma unroll
-        for (int n = 0; n < 32; n += 2) {
-          if (MODE == 1)
-            pk[n / 2] = h2_as_u32(__floats2half2_rn(s[n] * (dp[n] - dl), s[n + 1] * (dp[n + 1] - dl)));
-          else
-            pk[n / 2] = h2_as_u32(__floats2half2_rn(s[n], s[n + 1]));
-        }
+        for (int n = 0; n < 32; n += 2)
+          pk[n / 2] = h2_as_u32(__floats2half2_rn(s[n] * (dp[n] - dl), s[n + 1] * (dp[n + 1] - dl)));
         if (!wait(&bar[R3_DS_EMPTY], (t & 1) ^ 1)) break;
 #pragma unroll
         for (int x = 0; x < 4; ++x)
@@ -1784,20 +1769,14 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
         o[0] = mm, o[1] = L, o[2] = SD;
       }
     } else {
-      // dQ (dQ pass) or O (forward O pass: O = acc / (sP sV) + r for a row with keys, since its
-      // weights sum to one and V' was shifted by r; 0 for a row without keys); with key splits the
-      // scaled partial, completed by the split reduce
-      constexpr int NN = MODE == 1 ? D : Dv;
-      float* out = !rvalid ? nullptr
-                   : p.nsplit > 1 ? p.dqpart + (((size_t)split * p.Hkv + hk) * R + r) * NN
-                   : MODE == 1    ? p.dQ + ((size_t)i * p.H + h) * D
-                                  : p.o_out + ((size_t)i * p.H + h) * Dv;
-      const float fac = MODE == 1 ? dq_fac : 1.f / (st.sP * st.sV);
-      const float* rsh = (MODE == 2 && p.nsplit == 1) ? p.rmean + (size_t)hk * Dv : nullptr;
+      // dQ; with key splits the scaled partial, completed by the split reduce
+      float* out = !rvalid         ? nullptr
+                   : p.nsplit > 1 ? p.dqpart + (((size_t)split * p.Hkv + hk) * R + r) * D
+                                  : p.dQ + ((size_t)i * p.H + h) * D;
       const bool have = ntiles > 0 && wait(&bar[R3_ACC_FULL], 0);
       if (have) tc_fence_after();
 #pragma unroll 1
-      for (int c = col0; c < NN; c += 32 * C::NCH) {
+      for (int c = col0; c < D; c += 32 * C::NCH) {
         float v[32];
         if (have) {
           tmem_ld32(tbase + C::T_ACC + lane_off + c, v);
@@ -1807,11 +1786,7 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
           for (int e = 0; e < 32; ++e) v[e] = 0.f;
         }
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] *= fac;
-        if (rsh) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = live ? v[e] + rsh[c + e] : 0.f;
-        }
+        for (int e = 0; e < 32; ++e) v[e] *= dq_fac;
         if (out) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
@@ -1945,28 +1920,6 @@ static __global__ void __launch_bounds__(256) k_stats_in(Params p) {
   const Stats* st = p.st;
   p.lse2[idx] = lse * kLog2e;
   p.dlt[idx] = (p.delta_in[(size_t)i * p.H + h] - p.dOr[idx]) * (st->sdO * st->sV);
-}
-
-// O = sum of the forward O pass's split partials in split order, plus the V shift r for a row
-// with keys (its weights sum to one); 0 for a row without keys.
-static __global__ void __launch_bounds__(256) k_o_reduce(Params p) {
-  const long nv = (long)p.Hkv * p.R * (p.Dv / 4);
-  const long idx = (long)blockIdx.x * 256 + threadIdx.x;
-  if (idx >= nv) return;
-  const long row = idx / (p.Dv / 4);
-  const int c = (int)(idx % (p.Dv / 4)) * 4;
-  const int hk = (int)(row / p.R), r = (int)(row % p.R);
-  const int i = r / p.G, h = hk * p.G + r % p.G;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (p.lse2[row] > -CUDART_INF_F) {
-    for (int s = 0; s < p.nsplit; ++s) {
-      const float4 x = *reinterpret_cast<const float4*>(p.dqpart + (((size_t)s * p.Hkv + hk) * p.R + r) * p.Dv + c);
-      acc.x += x.x, acc.y += x.y, acc.z += x.z, acc.w += x.w;
-    }
-    const float* rm = p.rmean + (size_t)hk * p.Dv + c;
-    acc.x += rm[0], acc.y += rm[1], acc.z += rm[2], acc.w += rm[3];
-  }
-  *reinterpret_cast<float4*>(p.o_out + ((size_t)i * p.H + h) * p.Dv + c) = acc;
 }
 
 // dQ = sum of the split partials, in split order.

@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "fa_dq_raw.cuh"
+#include "fa_fwd.cuh"
 #include "fa_kernels.cuh"
 #include "fa_lse_pair.cuh"
 
@@ -72,11 +73,10 @@ inline bool make_map(CUtensorMap* m, void* base, int d0, int d1, int d2, int row
 // ------------------------------------------------------------------------------------------------
 // measurement hook: one CUDA event before the sequence and one after each launch
 
-constexpr int kProfCalls = 256, kProfSlots = 18;
+constexpr int kProfCalls = 256, kProfSlots = 17;
 enum {
   KS_STATS = 0, KS_VSUM, KS_FINAL, KS_CONVERT, KS_PREDECODE, KS_ROWS_LSE, KS_MERGE, KS_ROWS_DQ, KS_DQ_REDUCE,
-  KS_COLS, KS_DQ_GEMM, KS_STATS_IN, KS_FWD_LSE, KS_FWD_O, KS_O_REDUCE, KS_COLS_ROWSCALE, KS_SINK_GRAD, KS_DQ_RAW,
-  KS_N
+  KS_COLS, KS_DQ_GEMM, KS_STATS_IN, KS_FWD, KS_FWD_MERGE, KS_COLS_ROWSCALE, KS_SINK_GRAD, KS_DQ_RAW, KS_N
 };
 
 struct Profiler {
@@ -353,42 +353,32 @@ cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& tmQ, co
   return cudaGetLastError();
 }
 
-// Forward: lse by the LSE pass without dP (MODE 3), then O += P V' per row tile with P from that
-// lse (MODE 2), and the split reduce.  Plan level 1 (binary16 K'/V' copies, no stored dS).
+// Forward: the one-pass kernel (online softmax, O accumulated in tensor memory) over the binary16
+// K'/V' copies in 64-key tiles, then, with key splits, the fixed-order merge of the partials.
+// Plan level 1 (the copies, no stored dS).
 template <int D, int Dv>
 cudaError_t run_forward(const Params& p, const Plan& P, const CUtensorMap& tmQ, const CUtensorMap&,
-                               cudaStream_t s, CallRec& rec) {
-  constexpr int BK = (D + Dv <= 256) ? 128 : 64;
-  constexpr int BKL = kBKLse;
-  using FL = Rows3Cfg<D, Dv, BKL, 3>;
-  using FO = Rows3Cfg<D, Dv, BK, 2>;
-  Params pl = p;
-  pl.nKT = (p.M + BKL - 1) / BKL;
-  pl.kt_per_split = p.kt_per_split / (BKL / BK);
-  const dim3 grid(P.nQT, p.Hkv, P.nsplit);
-  CUtensorMap tkl, tko, tvo;
-  if (!make_map(&tkl, p.kd, 64, p.M, p.Hkv * (D / 64), BKL) || !make_map(&tko, p.kd, 64, p.M, p.Hkv * (D / 64), BK) ||
-      !make_map(&tvo, p.vd, 64, p.M, p.Hkv * (Dv / 64), BK))
+                        cudaStream_t s, CallRec& rec) {
+  using F = Fwd1Cfg<D, Dv>;
+  Params pf = p;
+  pf.nKT = (p.M + F::BK - 1) / F::BK;
+  pf.kt_per_split = p.kt_per_split * (P.BK / F::BK);  // the plan's splits in 64-key tiles
+  CUtensorMap tk, tv;
+  if (!make_map(&tk, p.kd, 64, p.M, p.Hkv * (D / 64), F::BK) || !make_map(&tv, p.vd, 64, p.M, p.Hkv * (Dv / 64), F::BK))
     return cudaErrorInvalidValue;
   cudaError_t e;
-  if ((e = set_smem(k_rows3<D, Dv, BKL, 3>, FL::SMEM)) != cudaSuccess) return e;
-  if ((e = set_smem(k_rows3<D, Dv, BK, 2>, FO::SMEM)) != cudaSuccess) return e;
+  if ((e = set_smem(k_fwd1<D, Dv>, F::SMEM)) != cudaSuccess) return e;
   const long units = (long)p.M * p.Hkv * ((D + Dv) / 8);
   k_predecode<<<(unsigned)std::min<long>((units + 255) / 256, 16L * P.nsm), 256, 0, s>>>(p);
   rec.mark(KS_PREDECODE);
-  k_rows3<D, Dv, BKL, 3><<<grid, FL::NT, FL::SMEM, s>>>(tmQ, tkl, tkl, pl);  // no V' (its map unused)
-  rec.mark(KS_FWD_LSE);
-  k_lse_merge<<<(unsigned)(((long)p.Hkv * P.R + 255) / 256), 256, 0, s>>>(pl);
-  rec.mark(KS_MERGE);
-  k_rows3<D, Dv, BK, 2><<<grid, FO::NT, FO::SMEM, s>>>(tmQ, tko, tvo, p);
-  rec.mark(KS_FWD_O);
+  k_fwd1<D, Dv><<<dim3(P.nQT, p.Hkv, P.nsplit), F::NT, F::SMEM, s>>>(tmQ, tk, tv, pf);
+  rec.mark(KS_FWD);
   if (P.nsplit > 1) {
-    k_o_reduce<<<(unsigned)(((long)p.Hkv * P.R * (Dv / 4) + 255) / 256), 256, 0, s>>>(p);
-    rec.mark(KS_O_REDUCE);
+    k_fwd_merge<<<(unsigned)(((long)p.Hkv * P.R * (Dv / 4) + 255) / 256), 256, 0, s>>>(pf);
+    rec.mark(KS_FWD_MERGE);
   }
   return cudaGetLastError();
 }
-
 
 using RunFn = cudaError_t (*)(const Params&, const Plan&, const CUtensorMap&, const CUtensorMap&, cudaStream_t,
                               CallRec&);

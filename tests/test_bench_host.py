@@ -75,7 +75,7 @@ def test_traffic_record_of_the_long_context_workload():
 def test_kernel_products_name_the_profiled_kernels():
     # the roofline's dominant kernel is looked up by these names in the library's profile record
     names = {"k_row_stats", "k_vsum", "k_finalize", "k_convert", "k_predecode", "k_rows_lse", "k_lse_merge",
-             "k_rows_dq", "k_dq_reduce", "k_cols", "k_dq_gemm", "k_stats_in", "k_fwd_lse", "k_fwd_o", "k_o_reduce",
+             "k_rows_dq", "k_dq_reduce", "k_cols", "k_dq_gemm", "k_stats_in", "k_fwd", "k_fwd_merge",
              "k_cols_rowscale", "k_sink_grad", "k_dq_raw"}
     src = open(os.path.join(ROOT, "flash_attention_backward_gb300", "csrc", "fa_back.cu")).read()
     for n in names:
