@@ -2,46 +2,50 @@
 //
 // A CTA owns 128 rows (r = i*G + g of one KV head) and the key tiles of one split, 64 keys per
 // tile.  Per tile t:
-//   S(t) = Q' K'(t)^T into one of two tensor-memory slots (Q' in shared memory, K-major);
-//   the softmax thread of each row takes its 64 scores, raises its running maximum m if needed,
-//   writes P = sP * 2^(s - m) as binary16 pairs over the first half of the same slot, and adds
-//   the unscaled sum to l;
+//   S(t) = Q' K'(t)^T into one of two tensor-memory slots (Q' in tensor memory as the A operand,
+//   K' from shared memory, K-major);
+//   the softmax thread of each row takes its 64 scores, moves its running maximum m if needed,
+//   writes P = 2^(s - m + kFwdLog2SP) as binary16 pairs over the first half of the same slot,
+//   and adds their sum to l;
 //   O += P(t) V'(t), with P as the tensor-memory A operand and V' as the MN-major B operand.
-// When a row's maximum grows, every earlier product was taken against the old maximum: before it
-// hands P(t) over, the row's thread waits for the product of tile t-1 to finish and multiplies
-// its row of the accumulator by 2^(m_old - m_new) (a tensor-memory read and write of Dv columns;
-// it happens a few times per row, mostly in the first tiles).  P <= sP = 2^15 stays inside
-// binary16's range.  The issuer forms S(t+1) before O += P(t) V'(t), so the softmax of one tile
-// overlaps the products of the next.
+// The running maximum moves only when a score exceeds it by more than kFwdTau (log2 units);
+// below that, P <= 2^(kFwdTau + kFwdLog2SP) = 2^15 stays inside binary16's range.  When it moves,
+// every earlier product was taken against the old maximum: before it hands P(t) over, the row's
+// thread waits for the product of tile t-1 to finish and multiplies its row of the accumulator by
+// 2^(m_old - m_new) (a tensor-memory read and write of Dv columns; with the threshold it is rare
+// after a row's first tiles).  The issuer forms S(t+1) before O += P(t) V'(t), so the softmax of
+// one tile overlaps the products of the next.
 //
-// With one split the epilogue writes O = acc / (sP sV l) + r' (V' holds v - r') and lse; with
-// several, each split writes its unnormalised accumulator and (m, l), which k_fwd_merge combines
-// in split order.
+// With one split the epilogue writes O = acc / (sV l) + r' (V' holds v - r'; acc and l both in
+// units of 2^kFwdLog2SP) and lse; with several, each split writes its unnormalised accumulator
+// and (m, l), which k_fwd_merge combines in split order.
 //
-// Warp roles: 0 producer (TMA of the Q tile and of K'/V' tiles into two rings), 1 tensor-memory
-// owner and MMA issuer, 2-5 softmax and epilogue (one per tensor-memory lane quarter: thread =
-// row).
+// Warp roles: 0 producer (TMA of K'/V' tiles into two rings), 1 tensor-memory owner and MMA
+// issuer, 2-5 softmax and epilogue (one per tensor-memory lane quarter: thread = row; they also
+// write the rows of Q' into tensor memory).
 #pragma once
 #include "fa_kernels.cuh"
 
 namespace fab {
 
+// P = 2^(s - m + kFwdLog2SP) with s - m <= kFwdTau (log2 units), so P <= 2^15
+constexpr float kFwdLog2SP = 7.f, kFwdTau = 8.f, kFwdSP = 128.f;
+
 template <int D, int Dv>
 struct Fwd1Cfg {
   static constexpr int BK = 64;
-  static constexpr int QB = 128 * D * 2, KB = BK * D * 2, VB = BK * Dv * 2;
+  static constexpr int KB = BK * D * 2, VB = BK * Dv * 2;
   static constexpr int BAR_BYTES = 512;
-  static constexpr int AVAIL = 232448 - 1024 - BAR_BYTES - QB;
+  static constexpr int AVAIL = 232448 - 1024 - BAR_BYTES;
   // K'/V' stages (two to four each)
   static constexpr int NSTG = AVAIL / (KB + VB) >= 4 ? 4 : AVAIL / (KB + VB) >= 3 ? 3 : 2;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = QB;
+  static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + NSTG * KB;
   static constexpr int OFF_BAR = OFF_V + NSTG * VB;
   static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;  // + 1024 for aligning the base
-  // tensor memory: [O accumulator: Dv columns] [S / P slot 0: BK] [S / P slot 1: BK]
-  static constexpr int T_O = 0, T_S = Dv;
-  static constexpr int TCOLS = pow2_at_least(Dv + 2 * BK);
+  // tensor memory: [O accumulator: Dv columns] [S / P slot 0: BK] [S / P slot 1: BK] [Q': D / 2]
+  static constexpr int T_O = 0, T_S = Dv, T_Q = Dv + 2 * BK;
+  static constexpr int TCOLS = pow2_at_least(T_Q + D / 2);
   static constexpr int NT = 32 * 6;
   static_assert(NSTG * (KB + VB) <= AVAIL && SMEM <= 232448, "shared memory budget");
   static_assert(TCOLS <= 512, "tensor memory budget");
@@ -57,7 +61,7 @@ enum {
   F_SLOT_FREE = 20,  // [2] the P V' product of the slot's last tile done: the slot may take S again
   F_PV_DONE = 22,    // one phase per P V' product
   F_O_FINAL,         // every P V' product done (the accumulator is final)
-  F_Q_FULL,
+  F_Q_FULL,  // Q' in tensor memory (the 4 softmax warps)
   F_DRAIN,  // the issuer's products, committed after an abort
   F_COUNT
 };
@@ -65,13 +69,11 @@ static_assert(8 * F_COUNT + 8 <= 512, "barrier area");
 
 template <int D, int Dv>
 static __global__ void __launch_bounds__(Fwd1Cfg<D, Dv>::NT, 1)
-    k_fwd1(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-           const __grid_constant__ CUtensorMap tmV, Params p) {
+    k_fwd1(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, Params p) {
   using C = Fwd1Cfg<D, Dv>;
   constexpr int BK = C::BK, NSTG = C::NSTG;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sQ = sm + C::OFF_Q;
   uint8_t* sK = sm + C::OFF_K;
   uint8_t* sV = sm + C::OFF_V;
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
@@ -106,7 +108,7 @@ static __global__ void __launch_bounds__(Fwd1Cfg<D, Dv>::NT, 1)
     }
     mbar_init(&bar[F_PV_DONE], 1);
     mbar_init(&bar[F_O_FINAL], 1);
-    mbar_init(&bar[F_Q_FULL], 1);
+    mbar_init(&bar[F_Q_FULL], 4);
     mbar_init(&bar[F_DRAIN], 1);
     *s_abort = 0;
     fence_mbar_init();
@@ -125,9 +127,6 @@ static __global__ void __launch_bounds__(Fwd1Cfg<D, Dv>::NT, 1)
     if (lane == 0 && ntiles > 0) {
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      mbar_arrive_expect_tx(&bar[F_Q_FULL], (uint32_t)C::QB);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) tma_load_3d(sQ + c * 128 * 128, &tmQ, &bar[F_Q_FULL], c * 64, r0, hk);
       uint64_t t0 = globaltimer_ns();
       while (n_k < ntiles || n_v < ntiles) {
         bool moved = false;
@@ -166,7 +165,6 @@ static __global__ void __launch_bounds__(Fwd1Cfg<D, Dv>::NT, 1)
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t ID_S = idesc_f16(128, BK, false, false);
       constexpr uint32_t ID_O = idesc_f16(128, Dv, false, true);
-      const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);
       // O += P(u) V'(u): P from the slot (binary16 pairs over its first BK / 2 columns)
       auto issue_pv = [&](int u) -> bool {
         const int sl = u & 1, vs = u % NSTG;
@@ -195,8 +193,8 @@ static __global__ void __launch_bounds__(Fwd1Cfg<D, Dv>::NT, 1)
         const uint64_t dk = sdesc_sw128(smem_u32(sK + ks * C::KB), 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_f16(tbase + C::T_S + sl * BK, sdesc_adv(dq, (k / 4) * (128 * 128) + (k % 4) * 32),
-                  sdesc_adv(dk, (k / 4) * (BK * 128) + (k % 4) * 32), ID_S, k > 0);
+          mma_f16_tmem_a(tbase + C::T_S + sl * BK, tbase + C::T_Q + k * 8,
+                         sdesc_adv(dk, (k / 4) * (BK * 128) + (k % 4) * 32), ID_S, k > 0);
         mma_commit(&bar[F_S_FULL + sl]);
         mma_commit(&bar[F_K_EMPTY + ks]);
         if (t > 0) ok = issue_pv(t - 1);
@@ -216,8 +214,28 @@ static __global__ void __launch_bounds__(Fwd1Cfg<D, Dv>::NT, 1)
     const int h = hk * G + (rvalid ? r % G : 0);
     const long jlast = rvalid ? (p.causal ? min((long)p.M - 1, (long)p.M - p.N + i) : (long)p.M - 1) : -1;
     const uint16_t* mrow = p.mask ? p.mask + ((size_t)(h % p.Hm) * p.N + i) * p.M : nullptr;
-    const float c2 = st.c2, sP = st.sP;
-    float m = -CUDART_INF_F, l = 0.f, lc = 0.f;  // running maximum (log2 units), compensated sum
+    const float c2 = st.c2;
+    // running maximum (log2 units), compensated sum of P (units of 2^kFwdLog2SP)
+    float m = -CUDART_INF_F, l = 0.f, lc = 0.f;
+
+    if (ntiles > 0) {
+      // this row of Q' into tensor memory (binary16 pairs per column), the A operand of S
+      const uint4* src = reinterpret_cast<const uint4*>(p.q16 + ((size_t)hk * R + (rvalid ? r : 0)) * D);
+#pragma unroll 1
+      for (int c = 0; c < D / 2; c += 32) {
+        uint32_t wv[32];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+          const uint4 u = rvalid ? __ldg(src + c / 4 + x) : make_uint4(0, 0, 0, 0);
+          wv[4 * x] = u.x, wv[4 * x + 1] = u.y, wv[4 * x + 2] = u.z, wv[4 * x + 3] = u.w;
+        }
+        tmem_st32(tbase + lane_off + C::T_Q + c, wv);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[F_Q_FULL]);
+    }
 
     for (int t = 0; t < ntiles; ++t) {
       const int sl = t & 1;
@@ -230,7 +248,9 @@ static __global__ void __launch_bounds__(Fwd1Cfg<D, Dv>::NT, 1)
       tmem_ld32(tS + 32, x[1]);
       tmem_ld_wait();
       // log2-domain scores; masked keys -> -inf
-      float cmax = -CUDART_INF_F;
+      float mx[8];  // partial maxima (independent chains)
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx[u] = -CUDART_INF_F;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int k0 = j0 + 32 * c;
@@ -251,26 +271,34 @@ static __global__ void __launch_bounds__(Fwd1Cfg<D, Dv>::NT, 1)
           }
         }
 #pragma unroll
-        for (int n = 0; n < 32; ++n) cmax = fmaxf(cmax, x[c][n]);
+        for (int n = 0; n < 32; ++n) mx[n & 7] = fmaxf(mx[n & 7], x[c][n]);
       }
-      // a larger maximum rescales what was summed (and, below, accumulated) against the old one
-      const bool grow = cmax > m && m > -CUDART_INF_F;
+      const float cmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      // a maximum more than kFwdTau above the running one rescales what was summed (and, below,
+      // accumulated) against the old one; the first live tile only sets it
+      const bool grow = m > -CUDART_INF_F && cmax > m + kFwdTau;
       const float f = grow ? ex2(m - cmax) : 1.f;
-      if (cmax > m) {
+      if (grow) {
         l *= f, lc *= f;
+        m = cmax;
+      } else if (m == -CUDART_INF_F) {
         m = cmax;
       }
       uint32_t pk[32];
       float cl = 0.f;
       if (m > -CUDART_INF_F) {
+        const float mP = m - kFwdLog2SP;  // 2^(s - mP) = P
+        float ca[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int n = 0; n < 32; n += 2) {
-            const float e0 = ex2(x[c][n] - m), e1 = ex2(x[c][n + 1] - m);  // 0 for masked keys
-            cl += e0 + e1;
-            pk[16 * c + n / 2] = h2_as_u32(__floats2half2_rn(e0 * sP, e1 * sP));
+            const float e0 = ex2(x[c][n] - mP), e1 = ex2(x[c][n + 1] - mP);  // 0 for masked keys
+            ca[(n >> 1) & 3] += e0 + e1;
+            pk[16 * c + n / 2] = h2_as_u32(__floats2half2_rn(e0, e1));
           }
+        cl = (ca[0] + ca[1]) + (ca[2] + ca[3]);
       } else {
 #pragma unroll
         for (int n = 0; n < 32; ++n) pk[n] = 0u;
@@ -308,7 +336,8 @@ static __global__ void __launch_bounds__(Fwd1Cfg<D, Dv>::NT, 1)
     const bool have = ntiles > 0 && wait(&bar[F_O_FINAL], 0);
     if (have) tc_fence_after();
     const bool live = have && m > -CUDART_INF_F && l > 0.f;
-    const float acc_fac = 1.f / (sP * st.sV);
+    l *= 1.f / kFwdSP;  // exact: a power of two
+    const float acc_fac = 1.f / (kFwdSP * st.sV);
     const bool whole = p.nsplit == 1;
     float* out = !rvalid ? nullptr
                  : whole ? p.o_out + ((size_t)i * p.H + h) * Dv
@@ -348,7 +377,6 @@ static __global__ void __launch_bounds__(Fwd1Cfg<D, Dv>::NT, 1)
   if (*s_abort) {  // the same value in every thread: nothing writes it after the barrier
     const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
     if (warp == 0 && lane == 0) {
-      if (ntiles > 0) mbar_wait_until(&bar[F_Q_FULL], 0, deadline);
       drain_loads(&bar[F_K_FULL], NSTG, n_k, deadline);
       drain_loads(&bar[F_V_FULL], NSTG, n_v, deadline);
     }

@@ -357,7 +357,7 @@ cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& tmQ, co
 // K'/V' copies in 64-key tiles, then, with key splits, the fixed-order merge of the partials.
 // Plan level 1 (the copies, no stored dS).
 template <int D, int Dv>
-cudaError_t run_forward(const Params& p, const Plan& P, const CUtensorMap& tmQ, const CUtensorMap&,
+cudaError_t run_forward(const Params& p, const Plan& P, const CUtensorMap&, const CUtensorMap&,
                         cudaStream_t s, CallRec& rec) {
   using F = Fwd1Cfg<D, Dv>;
   Params pf = p;
@@ -371,7 +371,7 @@ cudaError_t run_forward(const Params& p, const Plan& P, const CUtensorMap& tmQ, 
   const long units = (long)p.M * p.Hkv * ((D + Dv) / 8);
   k_predecode<<<(unsigned)std::min<long>((units + 255) / 256, 16L * P.nsm), 256, 0, s>>>(p);
   rec.mark(KS_PREDECODE);
-  k_fwd1<D, Dv><<<dim3(P.nQT, p.Hkv, P.nsplit), F::NT, F::SMEM, s>>>(tmQ, tk, tv, pf);
+  k_fwd1<D, Dv><<<dim3(P.nQT, p.Hkv, P.nsplit), F::NT, F::SMEM, s>>>(tk, tv, pf);
   rec.mark(KS_FWD);
   if (P.nsplit > 1) {
     k_fwd_merge<<<(unsigned)(((long)p.Hkv * P.R * (Dv / 4) + 255) / 256), 256, 0, s>>>(pf);
