@@ -82,3 +82,18 @@ def test_forward_statistics_feed_the_backward(fb):
     assert fb.fa_back_get_error() == 0
     for n in ("dQ", "dK", "dV"):
         assert nmse(b[n].cpu().numpy(), a[n].cpu().numpy()) <= 1e-6, n
+
+
+def test_forward_rescale_path(fb):
+    """Rows whose logits spread widely (each Q row scaled by its own 10^u, |u| <= 1.5): many rows'
+    maxima over later key tiles exceed their first tile's by more than the kernel's rescale
+    threshold (8 in log2 units), so O rows are rescaled in tensor memory.  The host checks that
+    such rows exist, then O and lse are compared with the oracle."""
+    import oracle
+    p = synth.make_problem("fwd_rescale", N=1024, M=1000, H=20, Hkv=1, D=64, Dv=64, k_type="q8_0", v_type="q8_0",
+                           row_decades=1.5, seed=5100)
+    kd = oracle.dequant(p.k, p.k_type, p.D).reshape(p.M, p.D)  # one KV head
+    s = np.einsum("nhd,md->nhm", p.q.astype(np.float64), kd) * p.scale
+    grow = s[:, :, 64:].max(-1) - s[:, :, :64].max(-1)
+    assert np.count_nonzero(grow > 8.0 * np.log(2.0)) > 1000
+    print(forward_parity(fb, p))

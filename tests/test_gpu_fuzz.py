@@ -1,4 +1,4 @@
-"""Seeded random problems against the oracle, on every plan level.
+"""Seeded random problems against the oracle, on every plan level, and for the forward.
 
 Each case draws its shape (ragged N and M, GQA ratio, D and Dv), cache types, mask kind, causal
 tail and score extensions from a seeded generator, then runs the CUDA path with the workspace
@@ -131,3 +131,39 @@ def test_fuzz_precision_against_the_oracle(fb, case):
     got = {k: v.cpu().numpy() for k, v in out.items()}
     res = check_components(got, oracle.fa_back(p))
     print(case, level, {k: v for k, v in kw.items() if k != "seed"}, res)
+
+
+def draw_forward(case: int) -> dict:
+    """A forward problem: a draw of the kind above without the score extensions; every third case
+    with larger logits (Q sigma 3) and every third with per-row ranges of Q (so rows' running
+    maxima move past the kernel's rescale threshold)."""
+    kw = draw(3000 + case)
+    for k in ("alibi", "softcap", "sinks"):
+        kw.pop(k, None)
+    rng = np.random.default_rng(94000 + case)
+    if case % 3 == 1:
+        kw.update(q_sigma=3.0)
+    elif case % 3 == 2:
+        kw.update(row_decades=float(rng.uniform(0.5, 1.5)))
+    return kw
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_fuzz_forward_against_the_oracle(fb, case):
+    import oracle
+    from metrics import NMSE_TOL, nmse
+    kw = draw_forward(case)
+    p = synth.make_problem(f"fuzzf{case}", **kw)
+    t = synth.device.to_torch(p, "cuda")
+    out = fb.forward(t["q"], t["k"], p.k_type, t["v"], p.v_type, H=p.H, Hkv=p.Hkv, D=p.D, Dv=p.Dv, M=p.M,
+                     scale=p.scale, causal=p.causal, mask=t["mask"], mask_heads=p.mask_heads)
+    torch.cuda.synchronize()
+    assert fb.fa_back_get_error() == 0
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    ref = oracle.fa_forward(p)
+    dead = ~np.isfinite(ref["lse"])
+    assert np.array_equal(np.isneginf(got["lse"]), dead)
+    assert np.all(got["O"][dead] == 0.0)
+    res = {"lse": nmse(got["lse"], ref["lse"]), "O": nmse(got["O"], ref["O"])}
+    print(case, {k: v for k, v in kw.items() if k != "seed"}, res)
+    assert all(v <= NMSE_TOL for v in res.values()), res
