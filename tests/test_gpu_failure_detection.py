@@ -103,3 +103,32 @@ def test_passes_give_up_mid_pipeline_then_the_next_call_is_correct(fb, limit_ns)
 def test_wait_limit_above_the_normal_one_is_rejected(fb):
     assert fb.STATUS[fb.fa_back_test_wait_limit(3_000_000_000)] == "FA_ERR_SHAPE"
 
+
+
+def _run_forward(fb, p):
+    t = synth.device.to_torch(p, "cuda")
+    out = fb.forward(t["q"], t["k"], p.k_type, t["v"], p.v_type, H=p.H, Hkv=p.Hkv, D=p.D, Dv=p.Dv, M=p.M,
+                     scale=p.scale, causal=p.causal, mask=t["mask"], mask_heads=p.mask_heads)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+@pytest.mark.parametrize("limit_ns", [0, 2_000, 20_000])
+def test_forward_gives_up_then_the_next_call_is_correct(fb, limit_ns):
+    """The one-pass forward's abort path: its producer, MMA issuer and softmax warps give up, the
+    loads and products in flight are waited for before tensor memory is freed.  Limit 0 always
+    times out (the issuer's first wait, for Q' in tensor memory, is never complete at once); a
+    few microseconds may or may not.  The next call matches the oracle."""
+    import oracle
+    from metrics import nmse
+    p = synth.from_config("1")
+    assert fb.fa_back_get_error() == 0
+    assert fb.STATUS[fb.fa_back_test_wait_limit(limit_ns)] == "FA_OK"
+    _run_forward(fb, p)
+    status = fb.STATUS[fb.fa_back_get_error()]
+    print(limit_ns, status)
+    assert status in (("FA_ERR_TIMEOUT",) if limit_ns == 0 else ("FA_OK", "FA_ERR_TIMEOUT"))
+    got = _run_forward(fb, p)
+    assert fb.fa_back_get_error() == 0
+    ref = oracle.fa_forward(p)
+    assert nmse(got["O"], ref["O"]) <= NMSE_TOL and nmse(got["lse"], ref["lse"]) <= NMSE_TOL
