@@ -171,9 +171,14 @@ __device__ __forceinline__ __half2 bytes_as_h2_plus1024(uint32_t x) {
 __device__ __forceinline__ uint4 decode8_h(const uint8_t* row, int type, int c0, float sig, const float* shift) {
   uint32_t w[4];
   __half2 sh[4];
+  if (shift) {  // c0 is a multiple of 8: two aligned 16-byte loads
+    const float4 a = *reinterpret_cast<const float4*>(shift + c0), b = *reinterpret_cast<const float4*>(shift + c0 + 4);
+    sh[0] = __floats2half2_rn(a.x, a.y), sh[1] = __floats2half2_rn(a.z, a.w);
+    sh[2] = __floats2half2_rn(b.x, b.y), sh[3] = __floats2half2_rn(b.z, b.w);
+  } else {
 #pragma unroll
-  for (int e = 0; e < 4; ++e)
-    sh[e] = shift ? __floats2half2_rn(shift[c0 + 2 * e], shift[c0 + 2 * e + 1]) : __floats2half2_rn(0.f, 0.f);
+    for (int e = 0; e < 4; ++e) sh[e] = __floats2half2_rn(0.f, 0.f);
+  }
   if (type == kTypeQ8 || type == kTypeQ4) {
     const bool q8 = type == kTypeQ8;
     const uint8_t* b = row + (q8 ? 34 : 18) * (c0 >> 5);
@@ -453,13 +458,17 @@ __device__ __forceinline__ void ext_scores(float* s, float* dp, int j0, int r, i
 // statistics and packing
 
 // Values c0 .. c0+7 of a raw cache row, decoded exactly to f32 (code * d, or the stored value).
+// MAGIC selects how an 8-bit code becomes a float (both exact): an int-to-float conversion, or the
+// byte placed under a float's exponent (fewer conversions, more registers)
+template <bool MAGIC = false>
 __device__ __forceinline__ void decode8_f(const uint8_t* row, int type, int c0, float* x) {
-  if (type == kTypeQ8 || type == kTypeQ4) {
+  if ((type == kTypeQ8 || type == kTypeQ4) && !MAGIC) {
     const bool q8 = type == kTypeQ8;
     const uint8_t* b = row + (q8 ? 34 : 18) * (c0 >> 5);
     const float d = h2f(__ldg(reinterpret_cast<const unsigned short*>(b)));
     const int o = c0 & 31;
     const uint16_t* cp = reinterpret_cast<const uint16_t*>(b + 2 + (q8 ? o : (o & 15)));
+    const int sh = o >= 16 ? 4 : 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const uint32_t pr = __ldg(cp + e);
@@ -467,10 +476,27 @@ __device__ __forceinline__ void decode8_f(const uint8_t* row, int type, int c0, 
         x[2 * e] = (float)(int8_t)(pr & 0xffu) * d;
         x[2 * e + 1] = (float)(int8_t)(pr >> 8) * d;
       } else {
-        const int sh = o >= 16 ? 4 : 0;
         x[2 * e] = (float)((int)((pr >> sh) & 15u) - 8) * d;
         x[2 * e + 1] = (float)((int)((pr >> (8 + sh)) & 15u) - 8) * d;
       }
+    }
+  } else if (type == kTypeQ8 || type == kTypeQ4) {
+    const bool q8 = type == kTypeQ8;
+    const uint8_t* b = row + (q8 ? 34 : 18) * (c0 >> 5);
+    const float d = h2f(__ldg(reinterpret_cast<const unsigned short*>(b)));
+    const int o = c0 & 31;
+    const uint16_t* cp = reinterpret_cast<const uint16_t*>(b + 2 + (q8 ? o : (o & 15)));
+    const int sh = (!q8 && o >= 16) ? 4 : 0;
+    // each code as a biased byte under the exponent of 1.5 * 2^23, which makes the byte the low
+    // mantissa bits: subtracting 1.5 * 2^23 plus the bias gives the code exactly (no int-to-float
+    // conversion), and code * d is exact in f32
+    const float off = q8 ? 12583040.f : 12582920.f;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const uint32_t w = (uint32_t)__ldg(cp + 2 * e) | ((uint32_t)__ldg(cp + 2 * e + 1) << 16);
+      const uint32_t bb = q8 ? (w ^ 0x80808080u) : ((w >> sh) & 0x0f0f0f0fu);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) x[4 * e + k] = (__uint_as_float(__byte_perm(bb, 0x4B400000u, 0x7650 | k)) - off) * d;
     }
   } else if (type == kTypeF16) {
     const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + 2 * c0));
@@ -557,7 +583,7 @@ static __global__ void __launch_bounds__(256) k_vsum(Params p) {
 #pragma unroll 2
     for (long j = ja + warp; j < jb; j += 8) {
       float x[8];
-      decode8_f(p.v + (j * p.Hkv + hk) * p.rbv, p.v_type, c0, x);
+      decode8_f<true>(p.v + (j * p.Hkv + hk) * p.rbv, p.v_type, c0, x);
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] += x[e];
     }
@@ -732,14 +758,22 @@ static __global__ void __launch_bounds__(256) k_convert(Params p) {
 static __global__ void __launch_bounds__(256) k_predecode(Params p) {
   const float sK = p.st->sK, sV = p.st->sV;
   const long uk = (long)p.M * p.Hkv * (p.D / 8), uv = (long)p.M * p.Hkv * (p.Dv / 8);
+  const int lgk = __ffs(p.D / 8) - 1, lgv = __ffs(p.Dv / 8) - 1;  // D / 8 and Dv / 8 are powers of two
+  const bool rows32 = (long)p.M * p.Hkv <= 0x7fffffffL;
   for (long u = (long)blockIdx.x * 256 + threadIdx.x; u < uk + uv; u += (long)gridDim.x * 256) {
     const bool isv = u >= uk;
     const long w = isv ? u - uk : u;
-    const int DD = isv ? p.Dv : p.D;
-    const long row = w / (DD / 8);  // cache row j * Hkv + hk
-    const int c0 = (int)(w % (DD / 8)) * 8;
-    const long j = row / p.Hkv;
-    const int hk = (int)(row % p.Hkv);
+    const int DD = isv ? p.Dv : p.D, lg = isv ? lgv : lgk;
+    const long row = w >> lg;  // cache row j * Hkv + hk
+    const int c0 = (int)(w & ((1 << lg) - 1)) * 8;
+    long j;
+    int hk;
+    if (rows32) {  // the division by Hkv in 32 bits
+      const unsigned r32 = (unsigned)row, j32 = r32 / (unsigned)p.Hkv;
+      j = j32, hk = (int)(r32 - j32 * (unsigned)p.Hkv);
+    } else {
+      j = row / p.Hkv, hk = (int)(row % p.Hkv);
+    }
     const uint8_t* src = (isv ? p.v : p.k) + row * (isv ? p.rbv : p.rbk);
     const uint4 o = decode8_h(src, isv ? p.v_type : p.k_type, c0, isv ? sV : sK,
                               isv ? p.rsh + (size_t)hk * DD : nullptr);
