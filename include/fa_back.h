@@ -181,8 +181,9 @@ fa_status fa_back_ext(const float* q, const void* k, int k_type, const void* v, 
  * mask, causal tail) v and lse [N][H] (natural log), f32.  A row without an allowed key gets
  * O = 0 and lse = -inf.  Arguments as for fa_back(); O and lse are written, 16-byte aligned.
  * The lse it writes, with delta = rowsum(dO o O), is what fa_back_with_stats() takes.
- * Computation: the LSE pass without its dP product, then O += P v' per row tile with P from
- * that lse (binary16 operands as in the backward), key splits reduced in a fixed order.
+ * Computation: one pass per row tile with an online softmax (O accumulated against a running
+ * maximum and rescaled when that maximum moves; binary16 operands as in the backward), key
+ * splits merged in a fixed order.  The result does not depend on timing.
  */
 size_t fa_forward_workspace_size(int N, int M, int H, int Hkv, int D, int Dv);
 fa_status fa_forward(const float* q, const void* k, int k_type, const void* v, int v_type,
