@@ -180,6 +180,13 @@ cudaError_t lse_pair(Params pl, const Plan& P, cudaStream_t s, CallRec& rec) {
     return cudaErrorInvalidValue;
   cudaError_t e;
   if ((e = set_smem(k_lse_pair<D, Dv, EXT>, sm)) != cudaSuccess) return e;
+  // the kernel's per-warpgroup register split must fit the registers it is launched with, or a
+  // warpgroup would wait for registers that never come free
+  static const int launch_regs = [] {
+    cudaFuncAttributes fa;
+    return cudaFuncGetAttributes(&fa, k_lse_pair<D, Dv, EXT>) == cudaSuccess ? fa.numRegs : 0;
+  }();
+  if ((long)launch_regs * L::NT < L::REG_NEED) return cudaErrorInvalidConfiguration;
   k_lse_pair<D, Dv, EXT><<<dim3(2 * ((P.nQT + 1) / 2), pl.Hkv, P.nsplit), L::NT, sm, s>>>(tk, tv, pl);
   rec.mark(KS_ROWS_LSE);
   k_lse_merge<<<(unsigned)(((long)pl.Hkv * P.R + 255) / 256), 256, 0, s>>>(pl);

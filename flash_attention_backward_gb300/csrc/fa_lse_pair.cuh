@@ -20,9 +20,12 @@
 // every pass forms S and dP from identical operands.
 //
 // Warp roles per CTA: 0 producer (TMA of raw rows into a K ring and a V ring), 1 tensor-memory
-// owner (collective allocation) and, in the even CTA, MMA issuer, 2-9 softmax (thread = row and
-// half of the tile's keys), 10-15 decoders.  Every wait is bounded; neither CTA leaves before the
-// other (cluster barrier) or before the products and arrivals aimed at it have landed.
+// owner (collective allocation) and, in the even CTA, MMA issuer, 4-11 softmax (thread = row and
+// half of the tile's keys), 2-3 and 12-19 decoders.  The decode runs on latency (about 0.6
+// instructions per clock over six decoder warps), so it takes ten; the registers that allows come
+// from a split per warpgroup: warpgroups 1 and 2 (softmax) take REG_SOFT each, warpgroups 0, 3
+// and 4 (producer, issuer, decoders) REG_REST.  Every wait is bounded; neither CTA leaves before
+// the other (cluster barrier) or before the products and arrivals aimed at it have landed.
 #pragma once
 #include "fa_kernels.cuh"
 
@@ -62,8 +65,12 @@ struct LsePairCfg {
   static constexpr int KB = HK * D * 2, VB = HK * Dv * 2;
   static constexpr int STAGES = 2;
   static constexpr int NSOFT = 8, NCH = 2;  // softmax warps; key halves per row
-  static constexpr int NDEC = 6;
-  static constexpr int NT = 32 * (2 + NSOFT + NDEC);
+  static constexpr int W_SOFT = 4, W_DEC = W_SOFT + NSOFT;  // first softmax warp; first decoder after them
+  static constexpr int NDEC = 10;                           // decoder warps: 2, 3 and W_DEC ..
+  static constexpr int NT = 32 * (W_DEC + NDEC - 2);
+  static constexpr int REG_SOFT = 128, REG_REST = 72;       // registers per thread after the split
+  static constexpr long REG_NEED = 128L * (2 * REG_SOFT + (NT / 128 - 2) * REG_REST);
+  static_assert(NT % 128 == 0 && W_SOFT % 4 == 0 && NSOFT == 8, "roles on warpgroup boundaries");
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + STAGES * KB;
   static constexpr int OFF_BAR = OFF_V + STAGES * VB;
@@ -173,126 +180,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LsePairCfg<D, Dv>::N
   int n_kraw = 0, n_vraw = 0;  // producer: raw entries loaded
   bool issued = false;         // issuer: any product issued
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      const int tot = ntiles * EPT;
-      int ek = 0, ev = 0, sk = 0, uk = 0, sv = 0, uv = 0;
-      uint64_t t0 = globaltimer_ns();
-      // entry e of a ring holds keys e*KE.. of this CTA's halves of the split's tiles
-      auto load_entry = [&](bool isv, int e, int slot) {
-        const int t = e / EPT, h = e % EPT;
-        const int ja = (kt_begin + t) * BK + (int)rank * HK + h * KE;
-        const int nv = max(0, min(KE, p.M - ja));
-        uint64_t* fb = &bar[(isv ? L_RV_FULL : L_RK_FULL) + slot];
-        if (nv > 0) {
-          mbar_arrive_expect_tx(fb, (uint32_t)(KE * (isv ? p.rbv : p.rbk)));
-          tma_load_3d(isv ? sRawV + slot * vent : sRaw + slot * kent, isv ? &tmV : &tmK, fb, 0, hk, ja);
-        } else {
-          mbar_arrive(fb);
-        }
-      };
-      while (ek < tot || ev < tot) {
-        bool moved = false;
-        if (ek < tot && mbar_try_wait(&bar[L_RK_EMPTY + sk], (uk & 1) ^ 1)) {
-          load_entry(false, ek++, sk);
-          if (++sk == RK) sk = 0, ++uk;
-          moved = true;
-        }
-        if (ev < tot && mbar_try_wait(&bar[L_RV_EMPTY + sv], (uv & 1) ^ 1)) {
-          load_entry(true, ev++, sv);
-          if (++sv == RV) sv = 0, ++uv;
-          moved = true;
-        }
-        if (moved) {
-          t0 = globaltimer_ns();
-        } else {
-          if (*s_abort) break;
-          if (globaltimer_ns() - t0 > p.wait_ns) {
-            *s_abort = 1;
-            record_error(p.err, kErrTimeout);
-            break;
-          }
-        }
-      }
-      n_kraw = ek, n_vraw = ev;
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer (even CTA)
-    if (lead && lane == 0 && ntiles > 0) {
-      constexpr uint32_t ID = idesc_f16(256, BK, false, false);
-      const uint32_t tQ = tbase + C::T_Q, tO = tbase + C::T_O, tS = tbase + C::T_S, tP = tbase + C::T_P;
-      if (poll_c(&bar[L_OPS_READY], 0)) {
-        for (int t = 0; t < ntiles; ++t) {
-          const int s = t & 1;
-          if (!poll_c(&bar[L_K_FULL + s], (t >> 1) & 1) || !poll_c(&bar[L_S_FREE], (t & 1) ^ 1)) break;
-          issued = true;
-          tc_fence_after();
-          const uint64_t db = sdesc_sw128(smem_u32(sK + s * C::KB), 16, 1024);
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_f16_tmem_a_pair(tS, tQ + k * 8, sdesc_adv(db, (k / 4) * (HK * 128) + (k % 4) * 32), ID, k > 0);
-          mma_commit_pair(&bar[L_S_FULL], 3);
-          mma_commit_pair(&bar[L_K_EMPTY + s], 3);
-          if (!poll_c(&bar[L_V_FULL + s], (t >> 1) & 1) || !poll_c(&bar[L_P_FREE], (t & 1) ^ 1)) break;
-          tc_fence_after();
-          const uint64_t dv = sdesc_sw128(smem_u32(sV + s * C::VB), 16, 1024);
-#pragma unroll
-          for (int k = 0; k < Dv / 16; ++k)
-            mma_f16_tmem_a_pair(tP, tO + k * 8, sdesc_adv(dv, (k / 4) * (HK * 128) + (k % 4) * 32), ID, k > 0);
-          mma_commit_pair(&bar[L_P_FULL], 3);
-          mma_commit_pair(&bar[L_V_EMPTY + s], 3);
-        }
-      }
-      if (issued) mma_commit_pair(&bar[L_DRAIN], 1);  // every product above has completed
-    }
-  } else if (warp >= 2 + C::NSOFT) {
-    // ------------------------------------------------------------------ decoders
-    constexpr int NDT = C::NDEC * 32;
-    static_assert(NDT % 64 == 0, "decoder_map needs a multiple of 8 column groups of 8 lanes");
-    const int dt = (warp - 2 - C::NSOFT) * 32 + lane;
-    __half2 vsh[16];
-    load_group_shift<Dv, NDT>(p.rsh + (size_t)hk * Dv, p.v_type, dt, vsh);
-    int sk = 0, uk = 0, sv = 0, uv = 0;  // ring positions
-    bool ok = true;
-    for (int t = 0; ok && t < ntiles; ++t) {
-      const int s = t & 1;
-      const int j0 = (kt_begin + t) * BK + (int)rank * HK;  // first key of this CTA's half
-      if (!wait_c(&bar[L_K_EMPTY + s], ((t >> 1) & 1) ^ 1)) break;
-      const uint32_t kd = smem_u32(sK + s * C::KB), vd = smem_u32(sV + s * C::VB);
-      for (int h = 0; h < EPT; ++h) {
-        if (!(ok = wait(&bar[L_RK_FULL + sk], uk & 1))) break;
-        const int nv = max(0, min(KE, p.M - (j0 + h * KE)));
-        decode_rows<D, HK, NDT, false>(p.k_type, smem_u32(sRaw) + sk * kent, p.rbk_pad, KE, nv, h * KE, kd, st.sK,
-                                       vsh, dt);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[L_RK_EMPTY + sk]);
-        if (++sk == RK) sk = 0, ++uk;
-      }
-      if (!ok) break;
-      fence_proxy_async_smem();  // the tile's binary16 stores, visible to the tensor cores
-      __syncwarp();
-      if (lane == 0) arrive_lead(L_K_FULL + s);
-      if (!wait_c(&bar[L_V_EMPTY + s], ((t >> 1) & 1) ^ 1)) break;
-      for (int h = 0; h < EPT; ++h) {
-        if (!(ok = wait(&bar[L_RV_FULL + sv], uv & 1))) break;
-        const int nv = max(0, min(KE, p.M - (j0 + h * KE)));
-        decode_rows<Dv, HK, NDT, true>(p.v_type, smem_u32(sRawV) + sv * vent, p.rbv_pad, KE, nv, h * KE, vd, st.sV,
-                                       vsh, dt);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[L_RV_EMPTY + sv]);
-        if (++sv == RV) sv = 0, ++uv;
-      }
-      if (!ok) break;
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) arrive_lead(L_V_FULL + s);
-    }
-  } else if (warp >= 2) {
+  // the register split, uniform within each warpgroup: each share governs the code it heads
+  if (warp >= C::W_SOFT && warp < C::W_DEC) {
+    setmaxnreg_inc<C::REG_SOFT>();
     // ------------------------------------------------------------------ softmax
-    const int q4 = warp & 3, ch = (warp - 2) >> 2;  // tensor-memory lane quarter; half of the keys
+    const int q4 = warp & 3, ch = (warp - C::W_SOFT) >> 2;  // tensor-memory lane quarter; half of the keys
     const int row = q4 * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const int col0 = ch * (BK / 2);
@@ -423,8 +315,127 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LsePairCfg<D, Dv>::N
       float* o = p.part + (((size_t)split * p.Hkv + hk) * R + r) * 3;
       o[0] = mm, o[1] = L, o[2] = SD;
     }
+  } else {
+    setmaxnreg_dec<C::REG_REST>();
+    if (warp == 0) {
+      // ------------------------------------------------------------------ producer
+      if (lane == 0) {
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        const int tot = ntiles * EPT;
+        int ek = 0, ev = 0, sk = 0, uk = 0, sv = 0, uv = 0;
+        uint64_t t0 = globaltimer_ns();
+        // entry e of a ring holds keys e*KE.. of this CTA's halves of the split's tiles
+        auto load_entry = [&](bool isv, int e, int slot) {
+          const int t = e / EPT, h = e % EPT;
+          const int ja = (kt_begin + t) * BK + (int)rank * HK + h * KE;
+          const int nv = max(0, min(KE, p.M - ja));
+          uint64_t* fb = &bar[(isv ? L_RV_FULL : L_RK_FULL) + slot];
+          if (nv > 0) {
+            mbar_arrive_expect_tx(fb, (uint32_t)(KE * (isv ? p.rbv : p.rbk)));
+            tma_load_3d(isv ? sRawV + slot * vent : sRaw + slot * kent, isv ? &tmV : &tmK, fb, 0, hk, ja);
+          } else {
+            mbar_arrive(fb);
+          }
+        };
+        while (ek < tot || ev < tot) {
+          bool moved = false;
+          if (ek < tot && mbar_try_wait(&bar[L_RK_EMPTY + sk], (uk & 1) ^ 1)) {
+            load_entry(false, ek++, sk);
+            if (++sk == RK) sk = 0, ++uk;
+            moved = true;
+          }
+          if (ev < tot && mbar_try_wait(&bar[L_RV_EMPTY + sv], (uv & 1) ^ 1)) {
+            load_entry(true, ev++, sv);
+            if (++sv == RV) sv = 0, ++uv;
+            moved = true;
+          }
+          if (moved) {
+            t0 = globaltimer_ns();
+          } else {
+            if (*s_abort) break;
+            if (globaltimer_ns() - t0 > p.wait_ns) {
+              *s_abort = 1;
+              record_error(p.err, kErrTimeout);
+              break;
+            }
+          }
+        }
+        n_kraw = ek, n_vraw = ev;
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------------ MMA issuer (even CTA)
+      if (lead && lane == 0 && ntiles > 0) {
+        constexpr uint32_t ID = idesc_f16(256, BK, false, false);
+        const uint32_t tQ = tbase + C::T_Q, tO = tbase + C::T_O, tS = tbase + C::T_S, tP = tbase + C::T_P;
+        if (poll_c(&bar[L_OPS_READY], 0)) {
+          for (int t = 0; t < ntiles; ++t) {
+            const int s = t & 1;
+            if (!poll_c(&bar[L_K_FULL + s], (t >> 1) & 1) || !poll_c(&bar[L_S_FREE], (t & 1) ^ 1)) break;
+            issued = true;
+            tc_fence_after();
+            const uint64_t db = sdesc_sw128(smem_u32(sK + s * C::KB), 16, 1024);
+  #pragma unroll
+            for (int k = 0; k < D / 16; ++k)
+              mma_f16_tmem_a_pair(tS, tQ + k * 8, sdesc_adv(db, (k / 4) * (HK * 128) + (k % 4) * 32), ID, k > 0);
+            mma_commit_pair(&bar[L_S_FULL], 3);
+            mma_commit_pair(&bar[L_K_EMPTY + s], 3);
+            if (!poll_c(&bar[L_V_FULL + s], (t >> 1) & 1) || !poll_c(&bar[L_P_FREE], (t & 1) ^ 1)) break;
+            tc_fence_after();
+            const uint64_t dv = sdesc_sw128(smem_u32(sV + s * C::VB), 16, 1024);
+  #pragma unroll
+            for (int k = 0; k < Dv / 16; ++k)
+              mma_f16_tmem_a_pair(tP, tO + k * 8, sdesc_adv(dv, (k / 4) * (HK * 128) + (k % 4) * 32), ID, k > 0);
+            mma_commit_pair(&bar[L_P_FULL], 3);
+            mma_commit_pair(&bar[L_V_EMPTY + s], 3);
+          }
+        }
+        if (issued) mma_commit_pair(&bar[L_DRAIN], 1);  // every product above has completed
+      }
+    } else {
+      // ------------------------------------------------------------------ decoders
+      constexpr int NDT = C::NDEC * 32;
+      static_assert(NDT % 64 == 0, "decoder_map needs a multiple of 8 column groups of 8 lanes");
+      const int dt = (warp < C::W_SOFT ? warp - 2 : warp - C::W_DEC + 2) * 32 + lane;
+      __half2 vsh[16];
+      load_group_shift<Dv, NDT>(p.rsh + (size_t)hk * Dv, p.v_type, dt, vsh);
+      int sk = 0, uk = 0, sv = 0, uv = 0;  // ring positions
+      bool ok = true;
+      for (int t = 0; ok && t < ntiles; ++t) {
+        const int s = t & 1;
+        const int j0 = (kt_begin + t) * BK + (int)rank * HK;  // first key of this CTA's half
+        if (!wait_c(&bar[L_K_EMPTY + s], ((t >> 1) & 1) ^ 1)) break;
+        const uint32_t kd = smem_u32(sK + s * C::KB), vd = smem_u32(sV + s * C::VB);
+        for (int h = 0; h < EPT; ++h) {
+          if (!(ok = wait(&bar[L_RK_FULL + sk], uk & 1))) break;
+          const int nv = max(0, min(KE, p.M - (j0 + h * KE)));
+          decode_rows<D, HK, NDT, false>(p.k_type, smem_u32(sRaw) + sk * kent, p.rbk_pad, KE, nv, h * KE, kd, st.sK,
+                                         vsh, dt);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar[L_RK_EMPTY + sk]);
+          if (++sk == RK) sk = 0, ++uk;
+        }
+        if (!ok) break;
+        fence_proxy_async_smem();  // the tile's binary16 stores, visible to the tensor cores
+        __syncwarp();
+        if (lane == 0) arrive_lead(L_K_FULL + s);
+        if (!wait_c(&bar[L_V_EMPTY + s], ((t >> 1) & 1) ^ 1)) break;
+        for (int h = 0; h < EPT; ++h) {
+          if (!(ok = wait(&bar[L_RV_FULL + sv], uv & 1))) break;
+          const int nv = max(0, min(KE, p.M - (j0 + h * KE)));
+          decode_rows<Dv, HK, NDT, true>(p.v_type, smem_u32(sRawV) + sv * vent, p.rbv_pad, KE, nv, h * KE, vd, st.sV,
+                                         vsh, dt);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar[L_RV_EMPTY + sv]);
+          if (++sv == RV) sv = 0, ++uv;
+        }
+        if (!ok) break;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) arrive_lead(L_V_FULL + s);
+      }
+    }
   }
-
   tc_fence_before();
   __syncthreads();
   {
@@ -437,7 +448,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LsePairCfg<D, Dv>::N
     }
     if (warp == 1 && lane == 0 && issued) mbar_wait_until(&bar[L_DRAIN], 0, deadline);
     // the issuer's last commits to this CTA's stage barriers (no one else waits for them)
-    if (warp == 2 + C::NSOFT && lane == 0) {
+    if (warp == 2 && lane == 0) {
       for (int t = max(0, ntiles - 2); t < ntiles; ++t) {
         mbar_wait_until(&bar[L_K_EMPTY + (t & 1)], (t >> 1) & 1, deadline);
         mbar_wait_until(&bar[L_V_EMPTY + (t & 1)], (t >> 1) & 1, deadline);

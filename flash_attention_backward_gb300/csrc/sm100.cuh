@@ -121,6 +121,19 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
 
+// Register split between warpgroups (every warp of a warpgroup executes the same one): dec gives
+// registers back to the CTA's pool, inc waits until the pool holds enough.  The shares of all
+// warpgroups must add up to no more than the launch allocation (threads x registers at launch),
+// or an inc waits for ever; the launching code checks that sum.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Non-blocking test that acquires at cluster scope (for barriers that peer CTAs arrive on).  A
 // thread suspended in try_wait was measured to resume about a microsecond after a remote
 // arrival completed the phase, so these barriers are polled with test_wait instead.
