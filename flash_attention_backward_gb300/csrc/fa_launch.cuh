@@ -296,7 +296,7 @@ cudaError_t dq_raw(Params pr, const Plan& P, const CUtensorMap& tmS, cudaStream_
   if (sm > QC::SMEM_MAX) return cudaErrorInvalidValue;
   cudaError_t e;
   if ((e = set_smem(k_dq_raw<D, BK>, sm)) != cudaSuccess) return e;
-  k_dq_raw<D, BK><<<dim3((P.nQT + 1) / 2, pr.Hkv, P.nsplit), QC::NT, sm, s>>>(tmS, tk, pr);
+  k_dq_raw<D, BK><<<dim3((P.nQT + 1) / 2, pr.Hkv, pr.nsplit), QC::NT, sm, s>>>(tmS, tk, pr);
   rec.mark(KS_DQ_RAW);
   return cudaSuccess;
 }
@@ -351,7 +351,25 @@ cudaError_t run_shape(const Params& p, const Plan& P, const CUtensorMap& tmQ, co
     k_dq_gemm<D, BK><<<grid, 256, GC::SMEM, s>>>(tmS, tkg, p);
     rec.mark(KS_DQ_GEMM);
   } else if (P.dsq) {  // no K' copy: the dQ product decodes raw K tiles itself
-    if ((e = dq_raw<D, BK>(p, P, tmS, s, rec)) != cudaSuccess) return e;
+    // with key splits of its own: its grid has half as many row units, so the plan's split count
+    // can leave a mostly empty last wave; the count that fills whole waves best (at most the
+    // plan's, whose partial buffer it writes), by the plan's cost of waves per split
+    Params pr = p;
+    const long units = (long)((P.nQT + 1) / 2) * p.Hkv;
+    int ns = P.nsplit;
+    double best = 1e30;
+    for (int c = 1; c <= P.nsplit; ++c) {
+      const double cost = (double)((units * c + P.nsm - 1) / P.nsm) / c * (1.0 + 0.01 * c);
+      if (cost < best - 1e-12) best = cost, ns = c;
+    }
+    pr.kt_per_split = (P.nKT + ns - 1) / ns;
+    pr.nsplit = P.nKT > 0 ? (P.nKT + pr.kt_per_split - 1) / pr.kt_per_split : 1;
+    if ((e = dq_raw<D, BK>(pr, P, tmS, s, rec)) != cudaSuccess) return e;
+    if (pr.nsplit > 1) {
+      k_dq_reduce<<<(unsigned)(((long)p.Hkv * P.R * (D / 4) + 255) / 256), 256, 0, s>>>(pr);
+      rec.mark(KS_DQ_REDUCE);
+    }
+    return cudaGetLastError();
   }
   if (P.nsplit_dq > 1) {
     k_dq_reduce<<<(unsigned)(((long)p.Hkv * P.R * (D / 4) + 255) / 256), 256, 0, s>>>(p);
