@@ -4,8 +4,12 @@ Each case draws its shape (ragged N and M, GQA ratio, D and Dv), cache types, ma
 tail and score extensions from a seeded generator, then runs the CUDA path with the workspace
 of one plan level and compares every component with the oracle (NMSE <= 1e-5; lse = -inf
 positions exact; rows without keys give delta = 0 and dQ = 0; dsinks as check_dsinks states).
-The draws cover combinations that the hand-picked cases do not.
+The draws cover combinations that the hand-picked cases do not.  FAB_FUZZ_CASES,
+FAB_FUZZ_PRECISION and FAB_FUZZ_FORWARD set how many draws of each kind run (32, 16 and 16 by
+default), for a wider sweep.
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -17,6 +21,9 @@ pytestmark = pytest.mark.gpu
 
 TYPES = ["f32", "f16", "q8_0", "q4_0"]
 HEADS = [(1, 1), (2, 1), (4, 2), (6, 2), (8, 2), (4, 4), (12, 4)]
+N_CASES = int(os.environ.get("FAB_FUZZ_CASES", "32"))
+N_PRECISION = int(os.environ.get("FAB_FUZZ_PRECISION", "16"))
+N_FORWARD = int(os.environ.get("FAB_FUZZ_FORWARD", "16"))
 DIMS = [64, 128, 256]
 
 
@@ -67,7 +74,7 @@ def level_workspace(fb, p, level):
     return None
 
 
-@pytest.mark.parametrize("case", range(32))
+@pytest.mark.parametrize("case", range(N_CASES))
 def test_fuzz_against_the_oracle(fb, case):
     import oracle
     kw = draw(case)
@@ -113,7 +120,7 @@ def draw_precision(case: int) -> dict:
     return kw
 
 
-@pytest.mark.parametrize("case", range(16))
+@pytest.mark.parametrize("case", range(N_PRECISION))
 def test_fuzz_precision_against_the_oracle(fb, case):
     import oracle
     kw = draw_precision(case)
@@ -148,7 +155,7 @@ def draw_forward(case: int) -> dict:
     return kw
 
 
-@pytest.mark.parametrize("case", range(16))
+@pytest.mark.parametrize("case", range(N_FORWARD))
 def test_fuzz_forward_against_the_oracle(fb, case):
     import oracle
     from metrics import NMSE_TOL, nmse
