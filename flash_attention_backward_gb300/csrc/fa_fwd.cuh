@@ -13,16 +13,19 @@
 // every earlier product was taken against the old maximum: before it hands P(t) over, the row's
 // thread waits for the product of tile t-1 to finish and multiplies its row of the accumulator by
 // 2^(m_old - m_new) (a tensor-memory read and write of Dv columns; with the threshold it is rare
-// after a row's first tiles).  The issuer forms S(t+1) before O += P(t) V'(t), so the softmax of
-// one tile overlaps the products of the next.
+// after a row's first tiles).  Two threads issue the products: one the S products, the other
+// the P V' products, each committing its own (a commit tracks only the committing thread's
+// products).  An issuing thread is held while the pipe is busy and spends about as long again on
+// its waits and commits; with two, one thread's bookkeeping runs while the other's products keep
+// the pipe busy, and the S product of the next tile overlaps the P V' product of this one.
 //
 // With one split the epilogue writes O = acc / (sV l) + r' (V' holds v - r'; acc and l both in
 // units of 2^kFwdLog2SP) and lse; with several, each split writes its unnormalised accumulator
 // and (m, l), which k_fwd_merge combines in split order.
 //
-// Warp roles: 0 producer (TMA of K'/V' tiles into two rings), 1 tensor-memory owner and MMA
-// issuer, 2-5 softmax and epilogue (one per tensor-memory lane quarter: thread = row; they also
-// write the rows of Q' into tensor memory).
+// Warp roles: 0 producer (TMA of K'/V' tiles into two rings), 1 tensor-memory owner and issuer of
+// the S products, 2-5 softmax and epilogue (one per tensor-memory lane quarter: thread = row;
+// they also write the rows of Q' into tensor memory), 6 issuer of the P V' products.
 #pragma once
 #include "fa_kernels.cuh"
 
@@ -46,7 +49,7 @@ struct Fwd1Cfg {
   // tensor memory: [O accumulator: Dv columns] [S / P slot 0: BK] [S / P slot 1: BK] [Q': D / 2]
   static constexpr int T_O = 0, T_S = Dv, T_Q = Dv + 2 * BK;
   static constexpr int TCOLS = pow2_at_least(T_Q + D / 2);
-  static constexpr int NT = 32 * 6;
+  static constexpr int NT = 32 * 7;
   static_assert(NSTG * (KB + VB) <= AVAIL && SMEM <= 232448, "shared memory budget");
   static_assert(TCOLS <= 512, "tensor memory budget");
 };
@@ -62,7 +65,8 @@ enum {
   F_PV_DONE = 22,    // one phase per P V' product
   F_O_FINAL,         // every P V' product done (the accumulator is final)
   F_Q_FULL,  // Q' in tensor memory (the 4 softmax warps)
-  F_DRAIN,  // the issuer's products, committed after an abort
+  F_DRAIN,     // the S issuer's products, committed after an abort
+  F_DRAIN_PV,  // the P V' issuer's products, committed after an abort
   F_COUNT
 };
 static_assert(8 * F_COUNT + 8 <= 512, "barrier area");
@@ -110,6 +114,7 @@ static __global__ void __launch_bounds__(Fwd1Cfg<D, Dv>::NT, 1)
     mbar_init(&bar[F_O_FINAL], 1);
     mbar_init(&bar[F_Q_FULL], 4);
     mbar_init(&bar[F_DRAIN], 1);
+    mbar_init(&bar[F_DRAIN_PV], 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -120,7 +125,7 @@ static __global__ void __launch_bounds__(Fwd1Cfg<D, Dv>::NT, 1)
   const Waiter wait{s_abort, p.err, p.wait_ns};
   const Stats st = *p.st;
   int n_k = 0, n_v = 0;  // producer: K' and V' tiles loaded
-  bool issued = false;   // issuer: any product issued
+  bool issued = false;   // an issuer: any product issued
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
@@ -161,27 +166,12 @@ static __global__ void __launch_bounds__(Fwd1Cfg<D, Dv>::NT, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------------ S issuer
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t ID_S = idesc_f16(128, BK, false, false);
-      constexpr uint32_t ID_O = idesc_f16(128, Dv, false, true);
-      // O += P(u) V'(u): P from the slot (binary16 pairs over its first BK / 2 columns)
-      auto issue_pv = [&](int u) -> bool {
-        const int sl = u & 1, vs = u % NSTG;
-        if (!wait(&bar[F_P_FULL + sl], (u >> 1) & 1) || !wait(&bar[F_V_FULL + vs], (u / NSTG) & 1)) return false;
-        tc_fence_after();
-        const uint64_t dv = sdesc_sw128(smem_u32(sV + vs * C::VB), BK * 128, 1024);
-        const uint32_t ta = tbase + C::T_S + sl * BK;
-#pragma unroll
-        for (int k = 0; k < BK / 16; ++k)
-          mma_f16_tmem_a(tbase + C::T_O, ta + k * 8, sdesc_adv(dv, k * 2048), ID_O, (u > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&bar[F_V_EMPTY + vs]);
-        mma_commit(&bar[F_SLOT_FREE + sl]);
-        mma_commit(&bar[F_PV_DONE]);
-        return true;
-      };
       bool ok = wait(&bar[F_Q_FULL], 0);
-      // S(t) into slot t & 1 once the slot's previous tile is done, then O += P(t-1) V'(t-1)
+      // S(t) into slot t & 1 once K'(t) has landed and the P V' product of the slot's last tile
+      // (t - 2) is done
       for (int t = 0; ok && t < ntiles; ++t) {
         const int sl = t & 1, ks = t % NSTG;
         if (!wait(&bar[F_K_FULL + ks], (t / NSTG) & 1) || !wait(&bar[F_SLOT_FREE + sl], ((t >> 1) & 1) ^ 1)) {
@@ -197,11 +187,34 @@ static __global__ void __launch_bounds__(Fwd1Cfg<D, Dv>::NT, 1)
                          sdesc_adv(dk, (k / 4) * (BK * 128) + (k % 4) * 32), ID_S, k > 0);
         mma_commit(&bar[F_S_FULL + sl]);
         mma_commit(&bar[F_K_EMPTY + ks]);
-        if (t > 0) ok = issue_pv(t - 1);
       }
-      if (ok) ok = issue_pv(ntiles - 1);
-      if (ok) mma_commit(&bar[F_O_FINAL]);
       if (issued) mma_commit(&bar[F_DRAIN]);  // every product issued above (also after an abort)
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------------ P V' issuer
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t ID_O = idesc_f16(128, Dv, false, true);
+      bool ok = true;
+      // O += P(u) V'(u): P from its slot (binary16 pairs over the first BK / 2 columns)
+      for (int u = 0; ok && u < ntiles; ++u) {
+        const int sl = u & 1, vs = u % NSTG;
+        if (!wait(&bar[F_P_FULL + sl], (u >> 1) & 1) || !wait(&bar[F_V_FULL + vs], (u / NSTG) & 1)) {
+          ok = false;
+          break;
+        }
+        issued = true;
+        tc_fence_after();
+        const uint64_t dv = sdesc_sw128(smem_u32(sV + vs * C::VB), BK * 128, 1024);
+        const uint32_t ta = tbase + C::T_S + sl * BK;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)
+          mma_f16_tmem_a(tbase + C::T_O, ta + k * 8, sdesc_adv(dv, k * 2048), ID_O, (u > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&bar[F_V_EMPTY + vs]);
+        mma_commit(&bar[F_SLOT_FREE + sl]);
+        mma_commit(&bar[F_PV_DONE]);
+      }
+      if (ok) mma_commit(&bar[F_O_FINAL]);
+      if (issued) mma_commit(&bar[F_DRAIN_PV]);
     }
   } else {
     // ------------------------------------------------------------------ softmax, then epilogue
@@ -381,6 +394,7 @@ static __global__ void __launch_bounds__(Fwd1Cfg<D, Dv>::NT, 1)
       drain_loads(&bar[F_V_FULL], NSTG, n_v, deadline);
     }
     if (warp == 1 && lane == 0 && issued) mbar_wait_until(&bar[F_DRAIN], 0, deadline);
+    if (warp == 6 && lane == 0 && issued) mbar_wait_until(&bar[F_DRAIN_PV], 0, deadline);
     __syncthreads();
   }
   if (warp == 1) {
