@@ -393,6 +393,9 @@ def run_ours(args):
     # result copy, which nothing overlaps, are spread over the same K steps
     e_steps = max(2, args.steps)
 
+    host_ms = {}  # host time per step to enqueue the copies and the call
+    phases = {}   # serial form: per step, ms of input copies, the call and result copies
+
     def run_e2e(pipelined: bool) -> float:
         s_c = stream
         s_in = torch.cuda.Stream(dev) if pipelined else s_c
@@ -401,16 +404,23 @@ def run_ours(args):
         ev_c = [torch.cuda.Event() for _ in range(2)]
         ev_out = [torch.cuda.Event() for _ in range(2)]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tev = [] if not pipelined else None  # serial form: phase boundaries on the one stream
         torch.cuda.synchronize()
+        h0 = time.perf_counter()
         e0.record(s_in)
         for i in range(e_steps):
             b = i % 2 if pipelined else 0
+            if tev is not None:
+                tev.append([torch.cuda.Event(enable_timing=True) for _ in range(4)])
+                tev[-1][0].record(s_c)
             if pipelined and i >= 2:
                 s_in.wait_event(ev_c[b])  # inputs b are read by compute(i-2)
             with torch.cuda.stream(s_in):
                 for k in keys_in:
                     din[b][k].copy_(hq[k], non_blocking=True)
             ev_in[b].record(s_in)
+            if tev is not None:
+                tev[-1][1].record(s_c)
             s_c.wait_event(ev_in[b])
             if pipelined and i >= 2:
                 s_c.wait_event(ev_out[b])  # outputs b still being copied back for step i-2
@@ -418,13 +428,21 @@ def run_ours(args):
                         D=p.D, Dv=p.Dv, M=p.M, scale=p.scale, causal=p.causal, mask=din[b]["mask"],
                         mask_heads=p.mask_heads, out=dout[b], workspace=ws, stream=s_c)
             ev_c[b].record(s_c)
+            if tev is not None:
+                tev[-1][2].record(s_c)
             s_out.wait_event(ev_c[b])
             with torch.cuda.stream(s_out):
                 for k, v in dout[b].items():
                     hout[b][k].copy_(v, non_blocking=True)
             ev_out[b].record(s_out)
+            if tev is not None:
+                tev[-1][3].record(s_c)
         e1.record(s_out)
+        host_ms[pipelined] = (time.perf_counter() - h0) * 1e3 / e_steps  # enqueueing only: no wait inside
         torch.cuda.synchronize()
+        if tev is not None:
+            phases.update({k: sum(ev[a].elapsed_time(ev[a + 1]) for ev in tev) / e_steps
+                           for a, k in enumerate(("h2d_ms", "call_ms", "d2h_ms"))})
         return e0.elapsed_time(e1) / e_steps
 
     def copy_ms(h2d_dir: bool) -> float:
@@ -499,7 +517,10 @@ def run_ours(args):
                     "d2h_bytes_per_step": d2h,
                     "pipelining": "input copy, backward and result copy on three streams, double-buffered",
                     "steps": e_steps,
-                    "serial": {"value": job_tflops(world, flops, e2e_serial_ms), "ms_per_step": e2e_serial_ms},
+                    # host time per step spent enqueueing (above ms_per_step, the GPU waits on the host)
+                    "host_enqueue_ms_per_step": host_ms.get(True),
+                    "serial": {"value": job_tflops(world, flops, e2e_serial_ms), "ms_per_step": e2e_serial_ms,
+                               "phases": phases},
                     # what the overlap has to hide: each direction's copies alone, and the host
                     # setting that would serialise the three streams if set to 1
                     "copies": {"h2d_ms": h2d_ms, "d2h_ms": d2h_ms, "h2d_GBps": h2d / (h2d_ms * 1e6),
