@@ -1404,7 +1404,12 @@ struct Rows3Cfg {
   static constexpr int SB = ROWQ ? 128 * BK * 2 : 0;
   static constexpr int NCH = BK / 32;  // 32-key chunks per tile
   static constexpr int NSOFT = 4 * NCH;
-  static constexpr int NT = 32 * (2 + NSOFT);
+  // the dQ pass issues dP from a thread of its own (after the softmax warps): its N = 64 products
+  // leave one issuing thread's waits and commits exposed; the LSE pass keeps S and dP on one
+  // thread (its N = 128 products hide them, and a separate dP thread let S run ahead of dP)
+  static constexpr bool DP_OWN = MODE == 1;
+  static constexpr int W_DP = 2 + NSOFT;
+  static constexpr int NT = 32 * (2 + NSOFT + (DP_OWN ? 1 : 0));
   static constexpr int MERGE_BYTES = MODE == 0 ? (NCH - 1) * 128 * 3 * 4 : 0;
   static constexpr int BAR_BYTES = 512 + MERGE_BYTES;
   static constexpr int SMEM_MAX = 232448;
@@ -1459,7 +1464,8 @@ enum {
   R3_Q_FULL,
   R3_OPS_READY,
   R3_DRAIN0,  // the producer's dQ products, committed after an abort
-  R3_DRAIN1,  // the issuer's S/dP products, committed after an abort
+  R3_DRAIN1,  // the S/dP issuer's products, committed after an abort
+  R3_DRAIN2,  // the dP issuer's products (dQ pass), committed after an abort
   R3_COUNT
 };
 static_assert(8 * R3_COUNT + 8 <= 512, "barrier area");
@@ -1513,6 +1519,7 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
     mbar_init(&bar[R3_OPS_READY], C::NSOFT);
     mbar_init(&bar[R3_DRAIN0], 1);
     mbar_init(&bar[R3_DRAIN1], 1);
+    mbar_init(&bar[R3_DRAIN2], 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -1523,7 +1530,7 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
   const Waiter wait{s_abort, p.err, p.wait_ns};
   const Stats st = *p.st;
   int n_kload = 0, n_vload = 0, n_prod = 0;  // producer: K' and V' tiles loaded, products issued
-  bool s_issued = false;                     // issuer: any S product issued
+  bool s_issued = false;                     // an issuer: any product issued
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
@@ -1622,7 +1629,28 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
         }
         mma_commit(&bar[R3_S_FULL]);
         if (!C::ROWQ) mma_commit(&bar[R3_K_EMPTY + ks]);  // only the dQ pass reads K'(t) again
+        if constexpr (!C::DP_OWN) {
+          if (!wait(&bar[R3_V_FULL + vs], (t / C::VSTAGES) & 1) || !wait(&bar[R3_P_FREE], (t & 1) ^ 1)) break;
+          tc_fence_after();
+          const uint64_t dv = sdesc_sw128(smem_u32(sV + vs * C::VB), 16, 1024);
+#pragma unroll
+          for (int k = 0; k < Dv / 16; ++k)
+            mma_f16_tmem_a(tP, tO + k * 8, sdesc_adv(dv, (k / 4) * (BK * 128) + (k % 4) * 32), ID_S, k > 0);
+          mma_commit(&bar[R3_P_FULL]);
+          mma_commit(&bar[R3_V_EMPTY + vs]);
+        }
+      }
+    }
+  } else if (C::DP_OWN && warp == C::W_DP) {
+    // ------------------------------------------------------------------ dP issuer (dQ pass)
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t ID_S = idesc_f16(128, BK, false, false);
+      const uint32_t tO = tbase + C::T_O, tP = tbase + C::T_P;
+      const bool ok = wait(&bar[R3_OPS_READY], 0);  // dO' in tensor memory
+      for (int t = 0; ok && t < ntiles; ++t) {
+        const int vs = t % C::VSTAGES;
         if (!wait(&bar[R3_V_FULL + vs], (t / C::VSTAGES) & 1) || !wait(&bar[R3_P_FREE], (t & 1) ^ 1)) break;
+        s_issued = true;
         tc_fence_after();
         const uint64_t dv = sdesc_sw128(smem_u32(sV + vs * C::VB), 16, 1024);
 #pragma unroll
@@ -1843,9 +1871,10 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
         mbar_wait_until(&bar[R3_DRAIN0], 0, deadline);
       }
     }
-    if (warp == 1 && lane == 0 && s_issued) {
-      mma_commit(&bar[R3_DRAIN1]);
-      mbar_wait_until(&bar[R3_DRAIN1], 0, deadline);
+    if ((warp == 1 || (C::DP_OWN && warp == C::W_DP)) && lane == 0 && s_issued) {
+      uint64_t* dr = &bar[warp == 1 ? R3_DRAIN1 : R3_DRAIN2];
+      mma_commit(dr);
+      mbar_wait_until(dr, 0, deadline);
     }
     __syncthreads();
   }
