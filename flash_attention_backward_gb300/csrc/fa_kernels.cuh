@@ -1404,10 +1404,12 @@ struct Rows3Cfg {
   static constexpr int SB = ROWQ ? 128 * BK * 2 : 0;
   static constexpr int NCH = BK / 32;  // 32-key chunks per tile
   static constexpr int NSOFT = 4 * NCH;
-  // the dQ pass issues dP from a thread of its own (after the softmax warps): its N = 64 products
-  // leave one issuing thread's waits and commits exposed; the LSE pass keeps S and dP on one
-  // thread (its N = 128 products hide them, and a separate dP thread let S run ahead of dP)
-  static constexpr bool DP_OWN = MODE == 1;
+  // dP is issued by a thread of its own (after the softmax warps), so one issuing thread's waits
+  // and commits run while the other's products keep the pipe fed.  In the LSE pass the two take
+  // turns, S(t), dP(t), S(t+1), ..., each waiting for the other's products of the previous step to
+  // be issued: left free, S ran ahead of dP, which waits for the single V' stage
+  static constexpr bool DP_OWN = true;
+  static constexpr bool ALT = MODE == 0;
   static constexpr int W_DP = 2 + NSOFT;
   static constexpr int NT = 32 * (2 + NSOFT + (DP_OWN ? 1 : 0));
   static constexpr int MERGE_BYTES = MODE == 0 ? (NCH - 1) * 128 * 3 * 4 : 0;
@@ -1465,7 +1467,9 @@ enum {
   R3_OPS_READY,
   R3_DRAIN0,  // the producer's dQ products, committed after an abort
   R3_DRAIN1,  // the S/dP issuer's products, committed after an abort
-  R3_DRAIN2,  // the dP issuer's products (dQ pass), committed after an abort
+  R3_DRAIN2,  // the dP issuer's products, committed after an abort
+  R3_S_ISSUED,   // S(t) issued (LSE pass: the dP thread's turn)
+  R3_DP_ISSUED,  // dP(t) issued (LSE pass: the S thread's turn)
   R3_COUNT
 };
 static_assert(8 * R3_COUNT + 8 <= 512, "barrier area");
@@ -1520,6 +1524,8 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
     mbar_init(&bar[R3_DRAIN0], 1);
     mbar_init(&bar[R3_DRAIN1], 1);
     mbar_init(&bar[R3_DRAIN2], 1);
+    mbar_init(&bar[R3_S_ISSUED], 1);
+    mbar_init(&bar[R3_DP_ISSUED], 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -1615,6 +1621,7 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
       for (int t = 0; ok && t < ntiles; ++t) {
         const int ks = t % C::KSTAGES, vs = t % C::VSTAGES;
         if (!wait(&bar[R3_K_FULL + ks], (t / C::KSTAGES) & 1) || !wait(&bar[R3_S_FREE], (t & 1) ^ 1)) break;
+        if (C::ALT && t > 0 && !wait(&bar[R3_DP_ISSUED], (t - 1) & 1)) break;
         s_issued = true;
         tc_fence_after();
         const uint64_t db = sdesc_sw128(smem_u32(sK + ks * C::KB), 16, 1024);
@@ -1629,6 +1636,7 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
         }
         mma_commit(&bar[R3_S_FULL]);
         if (!C::ROWQ) mma_commit(&bar[R3_K_EMPTY + ks]);  // only the dQ pass reads K'(t) again
+        if (C::ALT) mbar_arrive(&bar[R3_S_ISSUED]);
         if constexpr (!C::DP_OWN) {
           if (!wait(&bar[R3_V_FULL + vs], (t / C::VSTAGES) & 1) || !wait(&bar[R3_P_FREE], (t & 1) ^ 1)) break;
           tc_fence_after();
@@ -1642,13 +1650,14 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
       }
     }
   } else if (C::DP_OWN && warp == C::W_DP) {
-    // ------------------------------------------------------------------ dP issuer (dQ pass)
+    // ------------------------------------------------------------------ dP issuer
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t ID_S = idesc_f16(128, BK, false, false);
       const uint32_t tO = tbase + C::T_O, tP = tbase + C::T_P;
       const bool ok = wait(&bar[R3_OPS_READY], 0);  // dO' in tensor memory
       for (int t = 0; ok && t < ntiles; ++t) {
         const int vs = t % C::VSTAGES;
+        if (C::ALT && !wait(&bar[R3_S_ISSUED], t & 1)) break;
         if (!wait(&bar[R3_V_FULL + vs], (t / C::VSTAGES) & 1) || !wait(&bar[R3_P_FREE], (t & 1) ^ 1)) break;
         s_issued = true;
         tc_fence_after();
@@ -1658,6 +1667,7 @@ static __global__ void __launch_bounds__(Rows3Cfg<D, Dv, BK, MODE>::NT, 1)
           mma_f16_tmem_a(tP, tO + k * 8, sdesc_adv(dv, (k / 4) * (BK * 128) + (k % 4) * 32), ID_S, k > 0);
         mma_commit(&bar[R3_P_FULL]);
         mma_commit(&bar[R3_V_EMPTY + vs]);
+        if (C::ALT) mbar_arrive(&bar[R3_DP_ISSUED]);
       }
     }
   } else {
