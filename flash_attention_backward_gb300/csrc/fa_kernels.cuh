@@ -513,52 +513,95 @@ __device__ __forceinline__ void decode8_f(const uint8_t* row, int type, int c0, 
   }
 }
 
-// One warp per row of Q, dO, K^ or V^ (lane = 8 consecutive values): max |x| and max squared
-// row norm, reduced per block.
+// max |x| and the sum of x^2 over values c0 .. c0+7 of a row.  For q8_0 and q4_0 both come from
+// the codes by four-way byte arithmetic: max |code| times |d| (exact, as the decoded values'
+// maximum is) and the integer sum of code^2 times d^2.
+template <int TYPE>
+__device__ __forceinline__ void values8_stats(const uint8_t* row, int c0, float& am, float& ss) {
+  if constexpr (TYPE == kTypeQ8 || TYPE == kTypeQ4) {
+    constexpr bool q8 = TYPE == kTypeQ8;
+    const uint8_t* b = row + (q8 ? 34 : 18) * (c0 >> 5);
+    const float d = h2f(__ldg(reinterpret_cast<const unsigned short*>(b)));
+    const int o = c0 & 31;
+    const uint16_t* cp = reinterpret_cast<const uint16_t*>(b + 2 + (q8 ? o : (o & 15)));
+    uint32_t w[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      w[e] = (uint32_t)__ldg(cp + 2 * e) | ((uint32_t)__ldg(cp + 2 * e + 1) << 16);
+      if (!q8) w[e] = __vsub4((w[e] >> (o >= 16 ? 4 : 0)) & 0x0f0f0f0fu, 0x08080808u);  // signed codes
+    }
+    // per-byte |code|, read as unsigned (the code -128 gives the byte 0x80, i.e. 128)
+    const uint32_t a = __vmaxu4(__vabs4(w[0]), __vabs4(w[1]));
+    const uint32_t m = max(max(a & 0xffu, (a >> 8) & 0xffu), max((a >> 16) & 0xffu, a >> 24));
+    const int q2 = __dp4a((int)w[0], (int)w[0], __dp4a((int)w[1], (int)w[1], 0));
+    am = (float)m * fabsf(d);
+    ss = (float)q2 * (d * d);
+  } else {
+    float x[8];
+    decode8_f(row, TYPE, c0, x);
+    am = 0.f, ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(x[e])), ss = fmaf(x[e], x[e], ss);
+  }
+}
+
+// Sums over the 32 lanes of four values at once (six exchanges instead of twenty): lane l ends
+// with the sum of value 2 * bit4(l) + bit3(l).
+__device__ __forceinline__ float warp_sum4(const float* a, int lane) {
+  const bool h16 = (lane & 16) != 0, h8 = (lane & 8) != 0;
+  const float b0 = (h16 ? a[2] : a[0]) + __shfl_xor_sync(0xffffffffu, h16 ? a[0] : a[2], 16);
+  const float b1 = (h16 ? a[3] : a[1]) + __shfl_xor_sync(0xffffffffu, h16 ? a[1] : a[3], 16);
+  float c = (h8 ? b1 : b0) + __shfl_xor_sync(0xffffffffu, h8 ? b0 : b1, 8);
+  c += __shfl_xor_sync(0xffffffffu, c, 4);
+  c += __shfl_xor_sync(0xffffffffu, c, 2);
+  c += __shfl_xor_sync(0xffffffffu, c, 1);
+  return c;
+}
+
+// One tensor's rows (nrows rows of DD values, rstride bytes apart), one warp per row and four rows
+// per step (lane = 8 consecutive values): this lane's max |x| and max squared row norm.
+template <int TYPE>
+__device__ __forceinline__ void rows_stats(const uint8_t* base, long nrows, size_t rstride, int DD, long gw,
+                                           long nw, int lane, float& amx, float& nrm) {
+  const int c0 = lane * 8;
+  const bool on = c0 < DD;
+  for (long r0 = gw; r0 < nrows; r0 += 4 * nw) {
+    float am[4], ss[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const long r = r0 + u * nw;
+      am[u] = 0.f, ss[u] = 0.f;
+      if (on && r < nrows) values8_stats<TYPE>(base + r * rstride, c0, am[u], ss[u]);
+    }
+    amx = fmaxf(amx, fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3])));
+    nrm = fmaxf(nrm, warp_sum4(ss, lane));
+  }
+}
+__device__ __forceinline__ void rows_stats_of(int type, const uint8_t* base, long nrows, size_t rstride, int DD,
+                                              long gw, long nw, int lane, float& amx, float& nrm) {
+  if (type == kTypeQ8) rows_stats<kTypeQ8>(base, nrows, rstride, DD, gw, nw, lane, amx, nrm);
+  else if (type == kTypeQ4) rows_stats<kTypeQ4>(base, nrows, rstride, DD, gw, nw, lane, amx, nrm);
+  else if (type == kTypeF16) rows_stats<kTypeF16>(base, nrows, rstride, DD, gw, nw, lane, amx, nrm);
+  else rows_stats<kTypeF32>(base, nrows, rstride, DD, gw, nw, lane, amx, nrm);
+}
+
+// Max |x| and max squared row norm of Q, dO, K^ and V^ (one tensor after the other, every warp of
+// the grid taking its share of each), reduced per block.
 static __global__ void __launch_bounds__(256) k_row_stats(Params p) {
   __shared__ float red[8][4][2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long gw = (long)blockIdx.x * 8 + warp, nw = (long)gridDim.x * 8;
   const long nQ = (long)p.N * p.H, nK = (long)p.M * p.Hkv;
-  const long tot = 2 * nQ + 2 * nK;
   float amax[4] = {0, 0, 0, 0}, nrm[4] = {0, 0, 0, 0};
-  const int c0 = lane * 8;
-  // four rows per step: their loads are issued before any of their reductions
-  const long step = (long)gridDim.x * 8;
-  for (long rw0 = (long)blockIdx.x * 8 + warp; rw0 < tot; rw0 += 4 * step) {
-    float x[4][8];
-    int tt[4];
+  rows_stats<kTypeF32>(reinterpret_cast<const uint8_t*>(p.q), nQ, (size_t)p.D * 4, p.D, gw, nw, lane, amax[0],
+                       nrm[0]);
+  if (p.dO != nullptr)  // the forward has no dO
+    rows_stats<kTypeF32>(reinterpret_cast<const uint8_t*>(p.dO), nQ, (size_t)p.Dv * 4, p.Dv, gw, nw, lane, amax[1],
+                         nrm[1]);
+  rows_stats_of(p.k_type, p.k, nK, p.rbk, p.D, gw, nw, lane, amax[2], nrm[2]);
+  rows_stats_of(p.v_type, p.v, nK, p.rbv, p.Dv, gw, nw, lane, amax[3], nrm[3]);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const long rw = rw0 + u * step;
-      int t = -1;
-      long r = 0;
-      if (rw < nQ) t = 0, r = rw;
-      else if (rw < 2 * nQ) t = 1, r = rw - nQ;
-      else if (rw < 2 * nQ + nK) t = 2, r = rw - 2 * nQ;
-      else if (rw < tot) t = 3, r = rw - 2 * nQ - nK;
-      if (t == 1 && p.dO == nullptr) t = -1;  // the forward has no dO
-      tt[u] = t;
-      const int DD = (t == 0 || t == 2) ? p.D : p.Dv;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[u][e] = 0.f;
-      if (t >= 0 && c0 < DD) {
-        if (t == 0) decode8_f(reinterpret_cast<const uint8_t*>(p.q + r * p.D), kTypeF32, c0, x[u]);
-        else if (t == 1) decode8_f(reinterpret_cast<const uint8_t*>(p.dO + r * p.Dv), kTypeF32, c0, x[u]);
-        else if (t == 2) decode8_f(p.k + r * p.rbk, p.k_type, c0, x[u]);
-        else decode8_f(p.v + r * p.rbv, p.v_type, c0, x[u]);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      float am = 0.f, ss = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(x[u][e])), ss = fmaf(x[u][e], x[u][e], ss);
-      am = warp_max(am);
-      ss = warp_sum(ss);
-      const int t = tt[u];
-      if (t >= 0) amax[t] = fmaxf(amax[t], am), nrm[t] = fmaxf(nrm[t], ss);
-    }
-  }
+  for (int t = 0; t < 4; ++t) amax[t] = warp_max(amax[t]), nrm[t] = warp_max(nrm[t]);
   if (lane == 0)
     for (int t = 0; t < 4; ++t) red[warp][t][0] = amax[t], red[warp][t][1] = nrm[t];
   __syncthreads();
@@ -569,6 +612,28 @@ static __global__ void __launch_bounds__(256) k_row_stats(Params p) {
     p.bstat[((size_t)blockIdx.x * 4 + t) * 2 + w] = m;
   }
 }
+// This warp's keys ja + warp, ja + warp + 8, ... < jb of V^ (head hk), added to acc in key order;
+// four keys' loads are issued before their additions.
+template <int TYPE>
+__device__ __forceinline__ void vsum_keys(const Params& p, int hk, long ja, long jb, int warp, int c0, float* acc) {
+  long j = ja + warp;
+  for (; j + 24 < jb; j += 32) {
+    float x[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) decode8_f<true>(p.v + ((j + 8 * u) * p.Hkv + hk) * p.rbv, TYPE, c0, x[u]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += x[u][e];
+  }
+  for (; j < jb; j += 8) {
+    float x[8];
+    decode8_f<true>(p.v + (j * p.Hkv + hk) * p.rbv, TYPE, c0, x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] += x[e];
+  }
+}
+
 static __global__ void __launch_bounds__(256) k_vsum(Params p) {
   // block = (chunk, hk); its eight warps take every eighth key of the chunk and their sums are
   // added in warp order, so the result does not depend on timing
@@ -580,13 +645,10 @@ static __global__ void __launch_bounds__(256) k_vsum(Params p) {
   const long ja = (long)chunk * per, jb = min((long)p.M, ja + per);
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   if (c0 < p.Dv) {
-#pragma unroll 2
-    for (long j = ja + warp; j < jb; j += 8) {
-      float x[8];
-      decode8_f<true>(p.v + (j * p.Hkv + hk) * p.rbv, p.v_type, c0, x);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] += x[e];
-    }
+    if (p.v_type == kTypeQ8) vsum_keys<kTypeQ8>(p, hk, ja, jb, warp, c0, acc);
+    else if (p.v_type == kTypeQ4) vsum_keys<kTypeQ4>(p, hk, ja, jb, warp, c0, acc);
+    else if (p.v_type == kTypeF16) vsum_keys<kTypeF16>(p, hk, ja, jb, warp, c0, acc);
+    else vsum_keys<kTypeF32>(p, hk, ja, jb, warp, c0, acc);
 #pragma unroll
     for (int e = 0; e < 8; ++e) part[warp][c0 + e] = acc[e];
   }
