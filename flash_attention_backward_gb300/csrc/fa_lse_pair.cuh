@@ -447,8 +447,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LsePairCfg<D, Dv>::N
       }
     }
     if (warp == 1 && lane == 0 && issued) mbar_wait_until(&bar[L_DRAIN], 0, deadline);
-    // the issuer's last commits to this CTA's stage barriers (no one else waits for them)
-    if (warp == 2 && lane == 0) {
+    // the issuer's last commits to this CTA's stage barriers (no one else waits for them).  After
+    // an abort the tiles may not all have been issued; the products that were have landed once the
+    // even CTA's issuer has seen L_DRAIN (its last commit, taken in order), before the cluster
+    // barrier below that both CTAs pass before leaving
+    if (warp == 2 && lane == 0 && !*s_abort) {
       for (int t = max(0, ntiles - 2); t < ntiles; ++t) {
         mbar_wait_until(&bar[L_K_EMPTY + (t & 1)], (t >> 1) & 1, deadline);
         mbar_wait_until(&bar[L_V_EMPTY + (t & 1)], (t >> 1) & 1, deadline);
