@@ -281,8 +281,8 @@ fa_status fa_back_profile(int enable);
 int fa_back_profile_read(float* ms_sum, int* launches, const char** names, int max_kernels);
 
 /*
- * fa_back() for callers that cannot allocate device memory (no counterpart in the paper: the
- * pages' operator has no workspace argument).  Some callers cannot hand the library a
+ * fa_back() for callers that cannot allocate device memory.  "CUDA: FLASH_ATTN_BACK kernels"
+ * defines no such entry point: its operator takes no workspace argument at all.  Some callers cannot hand the library a
  * workspace: graph executors that own every device buffer through their own pool and give an
  * operator no scratch pointer, and services that allocate nothing once they are set up.  This
  * entry point takes the same arguments as fa_back() minus the workspace and uses instead one
