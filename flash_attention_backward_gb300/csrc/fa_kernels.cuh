@@ -163,15 +163,9 @@ __device__ __forceinline__ __half2 bytes_as_h2_plus1024(uint32_t x) {
   return u32_as_h2(__byte_perm(x, 0x64646464u, 0x5140));
 }
 
-// Decode 8 consecutive values c0..c0+7 (c0 % 8 == 0) of a raw row into four packed binary16
-// pairs, out = x^ * sig - shift (shift may be null; shift[c] is an exact binary16 value).
-// Codes are turned into exact binary16 integers in pairs; one fused multiply-add then applies
-// the block scale, the power-of-two operand scale and the shift with a single rounding.  The
-// row pointer may point to global or shared memory.
-__device__ __forceinline__ uint4 decode8_h(const uint8_t* row, int type, int c0, float sig, const float* shift) {
-  uint32_t w[4];
-  __half2 sh[4];
-  if (shift) {  // c0 is a multiple of 8: two aligned 16-byte loads
+// The shifts of columns c0..c0+7 (c0 % 8 == 0) as binary16 pairs; zeros where shift is null.
+__device__ __forceinline__ void shift8_h(const float* shift, int c0, __half2* sh) {
+  if (shift) {  // two aligned 16-byte loads
     const float4 a = *reinterpret_cast<const float4*>(shift + c0), b = *reinterpret_cast<const float4*>(shift + c0 + 4);
     sh[0] = __floats2half2_rn(a.x, a.y), sh[1] = __floats2half2_rn(a.z, a.w);
     sh[2] = __floats2half2_rn(b.x, b.y), sh[3] = __floats2half2_rn(b.z, b.w);
@@ -179,6 +173,15 @@ __device__ __forceinline__ uint4 decode8_h(const uint8_t* row, int type, int c0,
 #pragma unroll
     for (int e = 0; e < 4; ++e) sh[e] = __floats2half2_rn(0.f, 0.f);
   }
+}
+
+// Decode 8 consecutive values c0..c0+7 (c0 % 8 == 0) of a raw row into four packed binary16
+// pairs, out = x^ * sig - shift (sh: the shifts from shift8_h, each an exact binary16 value).
+// Codes are turned into exact binary16 integers in pairs; one fused multiply-add then applies
+// the block scale, the power-of-two operand scale and the shift with a single rounding.  The
+// row pointer may point to global or shared memory.
+__device__ __forceinline__ uint4 decode8_h_sh(const uint8_t* row, int type, int c0, float sig, const __half2* sh) {
+  uint32_t w[4];
   if (type == kTypeQ8 || type == kTypeQ4) {
     const bool q8 = type == kTypeQ8;
     const uint8_t* b = row + (q8 ? 34 : 18) * (c0 >> 5);
@@ -216,6 +219,11 @@ __device__ __forceinline__ uint4 decode8_h(const uint8_t* row, int type, int c0,
     }
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ uint4 decode8_h(const uint8_t* row, int type, int c0, float sig, const float* shift) {
+  __half2 sh[4];
+  shift8_h(shift, c0, sh);
+  return decode8_h_sh(row, type, c0, sig, sh);
 }
 
 // ---- decoders of the row passes: raw rows staged in shared memory -> binary16 operand tiles
@@ -812,36 +820,41 @@ static __global__ void __launch_bounds__(256) k_convert(Params p) {
   if (threadIdx.x == 0 && s_lexp != INT_MIN) atomicMax(&p.st->lamr_exp, s_lexp);
 }
 
-// Binary16 operand copies of the cache for the producer-fed row passes: K'[hk][j] = k^_j sK and
-// V'[hk][j] = v^_j sV - r' sV, with the rounding of the in-kernel decoders (decode8_h), so both
-// row-pass variants see the same operands.  Thread = 8 values; cache rows are read in order.
-// The copies are panel-major, [hk][64-column panel][key][64]: the TMA box of one operand panel
-// (BK keys x 64 columns) is then one contiguous block.
+// One KV head's K' or V' rows (keys 0..M-1 of head hk, DD values each) into the panel-major copy.
+// A thread keeps one group of 8 columns, so its V shifts stay in registers, and walks the keys;
+// the values are decode8_h's, the rounding of every other decoder.
+template <int TYPE>
+__device__ __forceinline__ void predecode_head(const Params& p, const uint8_t* base, size_t rb, int DD, float sig,
+                                               const float* shift, __half* dst, int hk) {
+  const int lg = __ffs(DD / 8) - 1;  // DD / 8 threads per key (a power of two, at most 32)
+  const int c0 = (int)(threadIdx.x & ((1u << lg) - 1)) * 8;
+  const int kps = 256 >> lg;         // keys per block step
+  __half2 sh[4];
+  shift8_h(shift, c0, sh);
+  __half* d0 = dst + ((size_t)hk * (DD / 64) + c0 / 64) * (size_t)p.M * 64 + (c0 & 63);
+  for (long j = (long)blockIdx.x * kps + (threadIdx.x >> lg); j < p.M; j += (long)gridDim.x * kps)
+    *reinterpret_cast<uint4*>(d0 + j * 64) = decode8_h_sh(base + ((size_t)j * p.Hkv + hk) * rb, TYPE, c0, sig, sh);
+}
+
+// Binary16 operand copies of the cache for the producer-fed passes: K'[hk][j] = k^_j sK and
+// V'[hk][j] = v^_j sV - r' sV, with the rounding of the in-kernel decoders (decode8_h), so every
+// plan sees the same operands.  The copies are panel-major, [hk][64-column panel][key][64]: the
+// TMA box of one operand panel (BK keys x 64 columns) is then one contiguous block.  Grid row
+// y < Hkv takes K' of head y, the others V' of head y - Hkv; the cache type is fixed per
+// instantiation of the walk.
 static __global__ void __launch_bounds__(256) k_predecode(Params p) {
-  const float sK = p.st->sK, sV = p.st->sV;
-  const long uk = (long)p.M * p.Hkv * (p.D / 8), uv = (long)p.M * p.Hkv * (p.Dv / 8);
-  const int lgk = __ffs(p.D / 8) - 1, lgv = __ffs(p.Dv / 8) - 1;  // D / 8 and Dv / 8 are powers of two
-  const bool rows32 = (long)p.M * p.Hkv <= 0x7fffffffL;
-  for (long u = (long)blockIdx.x * 256 + threadIdx.x; u < uk + uv; u += (long)gridDim.x * 256) {
-    const bool isv = u >= uk;
-    const long w = isv ? u - uk : u;
-    const int DD = isv ? p.Dv : p.D, lg = isv ? lgv : lgk;
-    const long row = w >> lg;  // cache row j * Hkv + hk
-    const int c0 = (int)(w & ((1 << lg) - 1)) * 8;
-    long j;
-    int hk;
-    if (rows32) {  // the division by Hkv in 32 bits
-      const unsigned r32 = (unsigned)row, j32 = r32 / (unsigned)p.Hkv;
-      j = j32, hk = (int)(r32 - j32 * (unsigned)p.Hkv);
-    } else {
-      j = row / p.Hkv, hk = (int)(row % p.Hkv);
-    }
-    const uint8_t* src = (isv ? p.v : p.k) + row * (isv ? p.rbv : p.rbk);
-    const uint4 o = decode8_h(src, isv ? p.v_type : p.k_type, c0, isv ? sV : sK,
-                              isv ? p.rsh + (size_t)hk * DD : nullptr);
-    __half* dst = (isv ? p.vd : p.kd) + (((size_t)hk * (DD / 64) + c0 / 64) * p.M + j) * 64 + (c0 & 63);
-    *reinterpret_cast<uint4*>(dst) = o;
-  }
+  const bool isv = (int)blockIdx.y >= p.Hkv;
+  const int hk = isv ? (int)blockIdx.y - p.Hkv : (int)blockIdx.y;
+  const int type = isv ? p.v_type : p.k_type, DD = isv ? p.Dv : p.D;
+  const uint8_t* base = isv ? p.v : p.k;
+  const size_t rb = isv ? p.rbv : p.rbk;
+  const float sig = isv ? p.st->sV : p.st->sK;
+  const float* shift = isv ? p.rsh + (size_t)hk * DD : nullptr;
+  __half* dst = isv ? p.vd : p.kd;
+  if (type == kTypeQ8) predecode_head<kTypeQ8>(p, base, rb, DD, sig, shift, dst, hk);
+  else if (type == kTypeQ4) predecode_head<kTypeQ4>(p, base, rb, DD, sig, shift, dst, hk);
+  else if (type == kTypeF16) predecode_head<kTypeF16>(p, base, rb, DD, sig, shift, dst, hk);
+  else predecode_head<kTypeF32>(p, base, rb, DD, sig, shift, dst, hk);
 }
 
 // ------------------------------------------------------------------------------------------------

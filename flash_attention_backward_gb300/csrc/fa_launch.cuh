@@ -194,6 +194,13 @@ cudaError_t lse_pair(Params pl, const Plan& P, cudaStream_t s, CallRec& rec) {
   return cudaGetLastError();
 }
 
+// k_predecode's grid: x walks the keys (each block step covers at least 8 keys), y = 2 * Hkv
+// (the K' and V' heads); about 16 blocks per SM in all.
+inline dim3 predecode_grid(const Params& p, int nsm) {
+  const long gx = std::max(1L, std::min((16L * nsm) / (2L * p.Hkv), ((long)p.M + 7) / 8));
+  return dim3((unsigned)gx, (unsigned)(2 * p.Hkv));
+}
+
 // Row passes over the binary16 K'/V' copies (written here by k_predecode), fed by TMA.
 template <int D, int Dv, int BK, int BKL, bool EXT>
 cudaError_t rows_pre(const Params& pl, const Params& pq, const Plan& P, const CUtensorMap& tmQ, dim3 grid,
@@ -209,8 +216,7 @@ cudaError_t rows_pre(const Params& pl, const Params& pq, const Plan& P, const CU
   cudaError_t e;
   if ((e = set_smem(k_rows3<D, Dv, BKL, 0, EXT>, FL::SMEM)) != cudaSuccess) return e;
   if ((e = set_smem(k_rows3<D, Dv, BK, 1, EXT>, FQ::SMEM)) != cudaSuccess) return e;
-  const long units = (long)pl.M * pl.Hkv * ((D + Dv) / 8);
-  k_predecode<<<(unsigned)std::min<long>((units + 255) / 256, 16L * P.nsm), 256, 0, s>>>(pl);
+  k_predecode<<<predecode_grid(pl, P.nsm), 256, 0, s>>>(pl);
   rec.mark(KS_PREDECODE);
   if (!pl.lse_in) {  // else the per-row values come from the given lse and delta
     k_rows3<D, Dv, BKL, 0, EXT><<<grid, FL::NT, FL::SMEM, s>>>(tmQ, tkl, tvl, pl);
@@ -393,8 +399,7 @@ cudaError_t run_forward(const Params& p, const Plan& P, const CUtensorMap&, cons
     return cudaErrorInvalidValue;
   cudaError_t e;
   if ((e = set_smem(k_fwd1<D, Dv>, F::SMEM)) != cudaSuccess) return e;
-  const long units = (long)p.M * p.Hkv * ((D + Dv) / 8);
-  k_predecode<<<(unsigned)std::min<long>((units + 255) / 256, 16L * P.nsm), 256, 0, s>>>(p);
+  k_predecode<<<predecode_grid(p, P.nsm), 256, 0, s>>>(p);
   rec.mark(KS_PREDECODE);
   k_fwd1<D, Dv><<<dim3(P.nQT, p.Hkv, P.nsplit), F::NT, F::SMEM, s>>>(tk, tv, pf);
   rec.mark(KS_FWD);
