@@ -131,23 +131,6 @@ __host__ __device__ constexpr int pow2_at_least(int x) {
 
 __device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 
-// Scalar decode of element c of a raw row (used by the statistics passes).
-__device__ __forceinline__ float decode_elem(const uint8_t* row, int type, int c) {
-  if (type == kTypeF32) return __ldg(reinterpret_cast<const float*>(row) + c);
-  if (type == kTypeF16) return h2f(__ldg(reinterpret_cast<const unsigned short*>(row) + c));
-  if (type == kTypeQ8) {
-    const uint8_t* b = row + 34 * (c >> 5);
-    const float d = h2f(__ldg(reinterpret_cast<const unsigned short*>(b)));
-    return (float)(int8_t)__ldg(b + 2 + (c & 31)) * d;
-  }
-  const uint8_t* b = row + 18 * (c >> 5);
-  const float d = h2f(__ldg(reinterpret_cast<const unsigned short*>(b)));
-  const int o = c & 31;
-  const uint8_t byte = __ldg(b + 2 + (o & 15));
-  const int nib = o < 16 ? (byte & 15) : (byte >> 4);
-  return (float)(nib - 8) * d;
-}
-
 __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
@@ -382,24 +365,6 @@ __device__ __forceinline__ void decode_tile(const uint8_t* base, int type, int r
     uint4 w = make_uint4(0, 0, 0, 0);
     if (j < M) w = decode8_h(base + ((size_t)j * Hkv + hk) * rb, type, c0, sigma, shift);
     sts_v4(pu + panel_off(BK, row, c0), w);
-  }
-}
-
-// Store 32 binary16 values (one row, columns col0..col0+31 of a [128][BK] panel set).
-template <int BK>
-__device__ __forceinline__ void store_row32(uint8_t* panels, int row, int col0, const float* v, float mul) {
-  const uint32_t pbase = (uint32_t)(col0 / 64) * (128 * 128);
-#pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4) {
-    uint4 w;
-    uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      __half2 hh = __floats2half2_rn(v[q4 * 8 + 2 * e] * mul, v[q4 * 8 + 2 * e + 1] * mul);
-      wp[e] = *reinterpret_cast<uint32_t*>(&hh);
-    }
-    const int col = (col0 & 63) + q4 * 8;
-    *reinterpret_cast<uint4*>(panels + pbase + swz128((uint32_t)row * 128 + (uint32_t)(col / 8) * 16)) = w;
   }
 }
 
