@@ -113,6 +113,18 @@ def test_q8_0_hand_built_blocks(oracle_lib):
     assert np.array_equal(got, want)
 
 
+def test_q8_0_every_code(oracle_lib):
+    """All 256 int8 codes, -128 included (a valid code that the quantizers here never write), in
+    eight blocks with their own scales: each decodes to code times its block's d."""
+    codes = np.arange(-128, 128, dtype=np.int16).astype(np.int8).reshape(8, 32)
+    scales = [1.0, -0.5, 0.125, 3.0, -2.0 ** -14, 7.5, 2.0 ** -20, -1.0]
+    raw = b"".join(_f16_bits(d) + c.tobytes() for d, c in zip(scales, codes))
+    got = oracle_lib.dequant(np.frombuffer(raw, dtype=np.uint8).reshape(1, -1), TYPE_Q8_0, 256)[0]
+    want = np.concatenate([c.astype(np.float64) * np.float64(np.float16(d)) for d, c in zip(scales, codes)])
+    assert np.array_equal(got, want)
+    assert got[0] == -128.0
+
+
 def test_q4_0_nibble_order_ramp(oracle_lib):
     # byte b: low nibble b (element b), high nibble 15-b (element b+16)
     body = bytes(((15 - b) << 4) | b for b in range(16))
